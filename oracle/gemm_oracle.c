@@ -1,0 +1,174 @@
+/*
+ * gemm_oracle.c -- the CPU oracle for the dense GEMM library.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the package smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code, header or constant with the CUDA
+ * library under dense_gemm_11_gb300/csrc.
+ *
+ * What it computes (plain definition, written out):
+ *
+ *   "SGEMM优化，从naive到warptiling", section 项目概况 / 问题与估算:
+ *       C = alpha * A x B + beta * C, A is MxK, B is KxN, C is MxN, all
+ *       row-major float.
+ *   "第24讲 ... GEMM 分块与 Tensor Core 思维", section 0.1: the same product as
+ *       the plain triple loop sum_k A[i][k] * B[k][j].
+ *   "企业官网建设流程全解析" (the DeepGEMM essay), sections 1.3 and 3.2: the
+ *       FP16-input / FP32-accumulate variant folds bias, scale and an
+ *       activation (GELU) into the epilogue.
+ *
+ *   out[i][j] = act( alpha * sum_{k=0}^{K-1} A[i*lda+k] * B[k*ldb+j]
+ *                    + beta * C0[i*ldc+j] + bias[j] )
+ *
+ * Readings where the pages are silent (BLAS convention):
+ *   - beta == 0: C0 is not read (a NaN in C0 does not propagate);
+ *   - alpha == 0 or K == 0: A and B are not read; the product term is 0;
+ *   - bias == NULL: no bias term;  act: 0 = identity, 1 = exact GELU,
+ *     GELU(x) = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))).
+ *
+ * Arithmetic: every input arrives as double (fp32 and fp16 values are
+ * exactly representable in double); the sum over k is taken in double with k
+ * ascending for every (i, j).  The loop order is i, k, j (a row of partial
+ * sums per i) so that B is walked along its rows; that changes no element's
+ * summation order.  Alongside the value the oracle returns the per-element
+ * error scale
+ *
+ *   S[i][j] = |alpha| * sum_k |A[i][k]| * |B[k][j]| + |beta| * |C0[i][j]|
+ *             + |bias[j]|
+ *
+ * used by the tolerance |C - C_ref| <= tol * S + 1e-6.
+ *
+ * Threads: the listed rows are split into contiguous ranges, one per thread.
+ * Build with -ffp-contract=off so that x86 and Arm hosts give the same bits.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    long M, N, K;
+    double alpha, beta;
+    const double *A, *B, *C0, *bias;
+    long lda, ldb, ldc;
+    int act;
+    const long *rows; /* NULL: rows r0..r1 are row numbers themselves */
+    long r0, r1;      /* range of positions in the row list handled here */
+    double *out, *scale;
+    int status;
+} oracle_job;
+
+static double gelu_exact(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+static void *oracle_rows(void *arg) {
+    oracle_job *J = (oracle_job *)arg;
+    const long N = J->N, K = J->K;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double *sab = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    if (!acc || !sab) {
+        free(acc);
+        free(sab);
+        J->status = -1;
+        return NULL;
+    }
+    const int use_product = (J->alpha != 0.0) && (K > 0);
+    for (long p = J->r0; p < J->r1; ++p) {
+        const long i = J->rows ? J->rows[p] : p;
+        for (long j = 0; j < N; ++j) {
+            acc[j] = 0.0;
+            sab[j] = 0.0;
+        }
+        if (use_product) {
+            const double *Ai = J->A + i * J->lda;
+            for (long k = 0; k < K; ++k) {
+                const double a = Ai[k];
+                const double aa = fabs(a);
+                const double *Bk = J->B + k * J->ldb;
+                for (long j = 0; j < N; ++j) {
+                    acc[j] += a * Bk[j];
+                    sab[j] += aa * fabs(Bk[j]);
+                }
+            }
+        }
+        double *o = J->out + p * N;
+        double *s = J->scale ? J->scale + p * N : NULL;
+        for (long j = 0; j < N; ++j) {
+            double v = use_product ? J->alpha * acc[j] : 0.0;
+            double sc = use_product ? fabs(J->alpha) * sab[j] : 0.0;
+            if (J->beta != 0.0) {
+                const double c = J->C0[i * J->ldc + j];
+                v += J->beta * c;
+                sc += fabs(J->beta) * fabs(c);
+            }
+            if (J->bias) {
+                v += J->bias[j];
+                sc += fabs(J->bias[j]);
+            }
+            if (J->act == 1) v = gelu_exact(v);
+            o[j] = v;
+            if (s) s[j] = sc;
+        }
+    }
+    free(acc);
+    free(sab);
+    J->status = 0;
+    return NULL;
+}
+
+/*
+ * oracle_gemm_f64: evaluate the rows listed in rows[0..nrows) (or rows
+ * 0..nrows-1 when rows == NULL) of out = act(alpha*A*B + beta*C0 + bias).
+ * out and scale (scale may be NULL) are nrows x N, row-major, contiguous.
+ * Returns 0 on success, -1 on a bad argument or allocation failure.
+ */
+int oracle_gemm_f64(long M, long N, long K, double alpha, const double *A, long lda,
+                    const double *B, long ldb, double beta, const double *C0, long ldc,
+                    const double *bias, int act, const long *rows, long nrows, double *out,
+                    double *scale, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || nrows < 0 || !out) return -1;
+    if (act != 0 && act != 1) return -1;
+    if (nrows == 0 || N == 0) return 0;
+    if (alpha != 0.0 && K > 0 && (!A || !B || lda < K || ldb < N)) return -1;
+    if (beta != 0.0 && (!C0 || ldc < N)) return -1;
+    for (long p = 0; p < nrows; ++p) {
+        const long i = rows ? rows[p] : p;
+        if (i < 0 || i >= M) return -1;
+    }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads > nrows) nthreads = (int)nrows;
+
+    oracle_job jobs[256];
+    pthread_t tid[256];
+    int started[256];
+    for (int t = 0; t < nthreads; ++t) {
+        oracle_job *J = &jobs[t];
+        J->M = M; J->N = N; J->K = K;
+        J->alpha = alpha; J->beta = beta;
+        J->A = A; J->B = B; J->C0 = C0; J->bias = bias;
+        J->lda = lda; J->ldb = ldb; J->ldc = ldc;
+        J->act = act;
+        J->rows = rows;
+        J->r0 = nrows * t / nthreads;
+        J->r1 = nrows * (t + 1) / nthreads;
+        J->out = out; J->scale = scale;
+        J->status = -1;
+        started[t] = 0;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        started[t] = pthread_create(&tid[t], NULL, oracle_rows, &jobs[t]) == 0;
+    oracle_rows(&jobs[0]);
+    int status = jobs[0].status;
+    for (int t = 1; t < nthreads; ++t) {
+        if (started[t]) {
+            pthread_join(tid[t], NULL);
+        } else {
+            oracle_rows(&jobs[t]); /* could not spawn: do the range here */
+        }
+        if (jobs[t].status != 0) status = -1;
+    }
+    return status;
+}
+
+/* GELU alone, exposed so that its special values can be pinned directly. */
+double oracle_gelu_f64(double x) { return gelu_exact(x); }

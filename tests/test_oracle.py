@@ -1,0 +1,223 @@
+"""Pins for the CPU oracle: closed forms, exact brute force and textbook values.
+
+None of these re-types the oracle's formula in floating point.  The reference
+values come from exact rational arithmetic (fractions.Fraction), exact integer
+arithmetic, closed forms of special matrices (identity, permutation, rank-1,
+zero), and the tabulated standard normal CDF for GELU(x) = x * Phi(x).
+
+Each case is chosen so that a plausible slip in the oracle fails at least one
+of them: a transposed operand (non-square brute force), a wrong leading
+dimension (views with ld > width), a dropped beta*C or bias term (identity,
+beta-only, brute force with bias), bias indexed by row (M != N with bias), a
+tanh-approximate GELU (Phi(1) to 1e-15), a missing |beta||C| in the error
+scale (exact S check).
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _exact(A, B, C0, alpha, beta, bias, K, N):
+    """Exact rational evaluation of alpha*A@B + beta*C0 + bias and of S."""
+    M = A.shape[0]
+    out = [[None] * N for _ in range(M)]
+    sc = [[None] * N for _ in range(M)]
+    fa, fb = Fraction(float(alpha)), Fraction(float(beta))
+    for i in range(M):
+        for j in range(N):
+            s = Fraction(0)
+            sa = Fraction(0)
+            for k in range(K):
+                a, b = Fraction(float(A[i, k])), Fraction(float(B[k, j]))
+                s += a * b
+                sa += abs(a) * abs(b)
+            v = fa * s
+            e = abs(fa) * sa
+            if beta != 0.0:
+                c = Fraction(float(C0[i, j]))
+                v += fb * c
+                e += abs(fb) * abs(c)
+            if bias is not None:
+                v += Fraction(float(bias[j]))
+                e += abs(Fraction(float(bias[j])))
+            out[i][j] = v
+            sc[i][j] = e
+    return out, sc
+
+
+TINY = [(1, 1, 1), (1, 5, 3), (3, 1, 7), (2, 3, 5), (7, 5, 3), (5, 7, 2), (8, 8, 8), (3, 11, 13)]
+
+
+@pytest.mark.parametrize("shape", TINY)
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_bruteforce_fraction(shape, with_bias):
+    M, N, K = shape
+    rng = np.random.default_rng(1000 + M * 100 + N * 10 + K)
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+    C0 = rng.uniform(-1, 1, (M, N)).astype(np.float32)
+    bias = rng.normal(0, 0.1, N).astype(np.float32) if with_bias else None
+    alpha, beta = 0.7, -1.3
+    out, S = oracle.gemm(A, B, C0, alpha=alpha, beta=beta, bias=bias)
+    ex, exS = _exact(A, B, C0, alpha, beta, bias, K, N)
+    eps = np.finfo(np.float64).eps
+    for i in range(M):
+        for j in range(N):
+            ref = ex[i][j]
+            bound = (K + 4) * eps * float(exS[i][j]) + 1e-300
+            assert abs(Fraction(out[i, j]) - ref) <= Fraction(bound), (i, j)
+            assert abs(S[i, j] - float(exS[i][j])) <= (K + 4) * eps * float(exS[i][j])
+
+
+def test_bruteforce_with_leading_dims():
+    """A (M x lda), B (K x ldb), C (M x ldc) with ld > width: only the window counts."""
+    M, N, K = 5, 6, 7
+    lda, ldb, ldc = 9, 11, 8
+    rng = np.random.default_rng(7)
+    A = rng.uniform(-1, 1, (M, lda)).astype(np.float32)
+    B = rng.uniform(-1, 1, (K, ldb)).astype(np.float32)
+    C0 = rng.uniform(-1, 1, (M, ldc)).astype(np.float32)
+    out, _ = oracle.gemm(A, B, C0, alpha=1.5, beta=0.5, K=K, N=N)
+    ex, exS = _exact(A[:, :K], B[:, :N], C0[:, :N], 1.5, 0.5, None, K, N)
+    eps = np.finfo(np.float64).eps
+    for i in range(M):
+        for j in range(N):
+            assert abs(Fraction(out[i, j]) - ex[i][j]) <= Fraction((K + 4) * eps * float(exS[i][j]))
+
+
+def test_identity_left_and_right():
+    rng = np.random.default_rng(3)
+    n, N = 37, 23
+    B = rng.uniform(-1, 1, (n, N)).astype(np.float32)
+    C0 = rng.uniform(-1, 1, (n, N)).astype(np.float32)
+    I = np.eye(n, dtype=np.float32)
+    out, _ = oracle.gemm(I, B, C0, alpha=2.0, beta=0.5)
+    # I @ B = B exactly; 2*B and 0.5*C0 are exact, their sum is one rounding.
+    np.testing.assert_array_equal(out, 2.0 * B.astype(np.float64) + 0.5 * C0.astype(np.float64))
+    A = rng.uniform(-1, 1, (N, n)).astype(np.float32)
+    C1 = rng.uniform(-1, 1, (N, n)).astype(np.float32)
+    out2, _ = oracle.gemm(A, I, C1, alpha=1.0, beta=-0.25)
+    np.testing.assert_array_equal(out2, A.astype(np.float64) - 0.25 * C1.astype(np.float64))
+
+
+def test_permutation_rows():
+    rng = np.random.default_rng(4)
+    n, N = 29, 17
+    perm = rng.permutation(n)
+    P = np.zeros((n, n), dtype=np.float32)
+    P[np.arange(n), perm] = 1.0
+    B = rng.normal(0, 1, (n, N)).astype(np.float32)
+    out, _ = oracle.gemm(P, B)
+    np.testing.assert_array_equal(out, B[perm].astype(np.float64))
+
+
+def test_rank1_closed_form():
+    """a_ik = u_i, b_kj = v_j  =>  C_ij = alpha*K*u_i*v_j + beta*c_ij (dyadic, exact)."""
+    rng = np.random.default_rng(5)
+    M, N, K = 19, 13, 64
+    u = rng.integers(-8, 9, M) / 8.0
+    v = rng.integers(-8, 9, N) / 4.0
+    c = rng.integers(-16, 17, (M, N)) / 16.0
+    A = np.repeat(u[:, None], K, axis=1).astype(np.float32)
+    B = np.repeat(v[None, :], K, axis=0).astype(np.float32)
+    out, _ = oracle.gemm(A, B, c.astype(np.float32), alpha=0.5, beta=0.25)
+    expect = 0.5 * K * np.outer(u, v) + 0.25 * c
+    np.testing.assert_array_equal(out, expect)
+
+
+def test_smallint_exact_against_integer_product():
+    rng = np.random.default_rng(6)
+    M, N, K = 33, 41, 300
+    A = rng.integers(-4, 5, (M, K))
+    B = rng.integers(-4, 5, (K, N))
+    C0 = rng.integers(-4, 5, (M, N))
+    out, _ = oracle.gemm(A.astype(np.float16), B.astype(np.float16), C0.astype(np.float32),
+                         alpha=1.0, beta=2.0)
+    exact = A.astype(np.int64) @ B.astype(np.int64) + 2 * C0.astype(np.int64)
+    np.testing.assert_array_equal(out, exact.astype(np.float64))
+
+
+def test_beta_only_and_degenerate():
+    rng = np.random.default_rng(8)
+    M, N, K = 12, 9, 5
+    C0 = rng.uniform(-1, 1, (M, N)).astype(np.float32)
+    Z = np.zeros((M, K), dtype=np.float32)
+    B = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+    out, _ = oracle.gemm(Z, B, C0, alpha=1.0, beta=0.75)
+    np.testing.assert_array_equal(out, 0.75 * C0.astype(np.float64))
+    # alpha == 0: A and B are not read (NaN inside them must not show).
+    An = np.full((M, K), np.nan, dtype=np.float32)
+    Bn = np.full((K, N), np.nan, dtype=np.float32)
+    out, S = oracle.gemm(An, Bn, C0, alpha=0.0, beta=-2.0)
+    np.testing.assert_array_equal(out, -2.0 * C0.astype(np.float64))
+    np.testing.assert_array_equal(S, 2.0 * np.abs(C0.astype(np.float64)))
+    # K == 0: the product is empty.
+    out, _ = oracle.gemm(np.zeros((M, 0), np.float32), np.zeros((0, N), np.float32), C0,
+                         alpha=1.0, beta=3.0)
+    np.testing.assert_array_equal(out, 3.0 * C0.astype(np.float64))
+    # beta == 0: C is not read.
+    Cn = np.full((M, N), np.nan, dtype=np.float32)
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    out, _ = oracle.gemm(A, B, Cn, alpha=1.0, beta=0.0)
+    assert np.isfinite(out).all()
+
+
+# Standard normal CDF, tabulated values: Phi(1), Phi(-1), Phi(2), Phi(0.5).
+PHI = {1.0: 0.8413447460685429, -1.0: 0.15865525393145707, 2.0: 0.9772498680518208,
+       0.5: 0.6914624612740131, -3.0: 0.0013498980316300946}
+
+
+def test_gelu_special_values():
+    assert oracle.gelu(0.0) == 0.0
+    for x, phi in PHI.items():
+        assert abs(oracle.gelu(x) - x * phi) <= 4e-16 * max(1.0, abs(x))
+    assert oracle.gelu(12.0) == 12.0
+    assert abs(oracle.gelu(-12.0)) < 1e-30
+    # act=1 is applied to the complete pre-activation (product + beta*C + bias).
+    C0 = np.array([[1.0, -1.0]], dtype=np.float32)
+    bias = np.array([1.0, 0.5], dtype=np.float32)
+    out, _ = oracle.gemm(np.zeros((1, 3), np.float32), np.zeros((3, 2), np.float32), C0,
+                         alpha=1.0, beta=1.0, bias=bias, act=1)
+    assert abs(out[0, 0] - 2.0 * PHI[2.0]) < 1e-15
+    assert abs(out[0, 1] - (-0.5) * (1.0 - PHI[0.5])) < 1e-15
+
+
+def test_numpy_blas_crosscheck():
+    rng = np.random.default_rng(9)
+    M, N, K = 64, 48, 80
+    A = rng.normal(0, 1, (M, K)).astype(np.float32)
+    B = rng.normal(0, 1, (K, N)).astype(np.float32)
+    C0 = rng.normal(0, 1, (M, N)).astype(np.float32)
+    out, S = oracle.gemm(A, B, C0, alpha=0.7, beta=-0.3)
+    ref = 0.7 * (A.astype(np.float64) @ B.astype(np.float64)) - 0.3 * C0.astype(np.float64)
+    assert np.all(np.abs(out - ref) <= 1e-13 * S)
+
+
+def test_row_subset_and_threads_are_consistent():
+    rng = np.random.default_rng(10)
+    M, N, K = 50, 31, 70
+    A = rng.normal(0, 1, (M, K)).astype(np.float32)
+    B = rng.normal(0, 1, (K, N)).astype(np.float32)
+    C0 = rng.normal(0, 1, (M, N)).astype(np.float32)
+    full, Sf = oracle.gemm(A, B, C0, alpha=1.0, beta=0.5, threads=1)
+    many, Sm = oracle.gemm(A, B, C0, alpha=1.0, beta=0.5, threads=7)
+    np.testing.assert_array_equal(full, many)
+    np.testing.assert_array_equal(Sf, Sm)
+    rows = [49, 0, 17, 17, 3]
+    sub, Ss = oracle.gemm(A, B, C0, alpha=1.0, beta=0.5, rows=rows, threads=3)
+    np.testing.assert_array_equal(sub, full[rows])
+    np.testing.assert_array_equal(Ss, Sf[rows])
+
+
+def test_rejects_bad_arguments():
+    A = np.zeros((2, 3), np.float32)
+    B = np.zeros((3, 4), np.float32)
+    with pytest.raises(ValueError):
+        oracle.gemm(A, B, None, beta=1.0)
+    with pytest.raises(ValueError):
+        oracle.gemm(A, B, rows=[2])
+    with pytest.raises(ValueError):
+        oracle.gemm(A, B, act=5)
