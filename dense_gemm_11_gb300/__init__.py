@@ -1,0 +1,165 @@
+"""Python binding of libgemm11.so, the GB300 (sm_103a) dense GEMM library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/gemm11.h``.  There is no
+fallback: if the shared library is missing, every call raises.
+
+    gemm_f32(A, B, C, alpha=1.0, beta=0.0)            C = alpha*A@B + beta*C (fp32)
+    gemm_f16_f32acc_epilogue(A, B, C, alpha=1.0, beta=0.0, bias=None, act=0)
+                                                      C = act(alpha*A@B + beta*C + bias)
+
+Tensors are torch CUDA tensors on the current device; A and B may be 2-D
+views with a leading dimension larger than their width (unit column stride).
+Calls are asynchronous on the current torch stream (or ``stream=``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH, build  # noqa: F401  (build() is part of the public API)
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = -1
+GEMM_ERR_UNSUPPORTED = -2
+GEMM_ERR_CUDA = -3
+GEMM_ERR_TIMEOUT = -4
+GEMM_ACT_NONE = 0
+GEMM_ACT_GELU = 1
+
+EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_status_string", "gemm_last_cuda_error",
+                    "gemm_check", "gemm_last_plan", "gemm_last_launch_count")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = status_string(status) if _lib is not None else str(status)
+        if status == GEMM_ERR_CUDA and _lib is not None:
+            msg += f" (cudaError {_lib.gemm_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}")
+
+
+def lib():
+    """The loaded libgemm11.so (ctypes).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libgemm11.so is not built ({LIB_PATH}); call dense_gemm_11_gb300.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            c_int, c_float, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+            L.gemm_f32.restype = c_int
+            L.gemm_f32.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_int, c_void_p, c_int, c_float,
+                                   c_void_p, c_int, c_void_p]
+            L.gemm_f16_f32acc_epilogue.restype = c_int
+            L.gemm_f16_f32acc_epilogue.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_float,
+                                                   c_void_p, c_void_p, c_int, c_void_p]
+            L.gemm_status_string.restype = ctypes.c_char_p
+            L.gemm_status_string.argtypes = [c_int]
+            L.gemm_last_cuda_error.restype = c_int
+            L.gemm_last_cuda_error.argtypes = []
+            L.gemm_check.restype = c_int
+            L.gemm_check.argtypes = [c_void_p]
+            L.gemm_last_plan.restype = ctypes.c_char_p
+            L.gemm_last_plan.argtypes = []
+            L.gemm_last_launch_count.restype = c_int
+            L.gemm_last_launch_count.argtypes = []
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gemm_status_string(int(status)).decode()
+
+
+def last_plan() -> str:
+    return lib().gemm_last_plan().decode()
+
+
+def last_launch_count() -> int:
+    return int(lib().gemm_last_launch_count())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _mat(t, name, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} needs unit column stride")
+    return t.data_ptr(), max(t.stride(0), 1) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def gemm_f32_raw(M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream_ptr=0) -> int:
+    """Direct C-ABI call with integer device pointers; returns the status code."""
+    return lib().gemm_f32(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr), int(lda),
+                          ctypes.c_void_p(B_ptr), int(ldb), float(beta), ctypes.c_void_p(C_ptr), int(ldc),
+                          ctypes.c_void_p(stream_ptr))
+
+
+def gemm_f16_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, stream_ptr=0) -> int:
+    """Direct C-ABI call with integer device pointers; returns the status code."""
+    return lib().gemm_f16_f32acc_epilogue(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr),
+                                          ctypes.c_void_p(B_ptr), float(beta), ctypes.c_void_p(C_ptr),
+                                          ctypes.c_void_p(bias_ptr or None), int(act), ctypes.c_void_p(stream_ptr))
+
+
+def gemm_f32(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, stream=None) -> None:
+    """C = alpha * A @ B + beta * C in true FP32 (CUDA-core FFMA)."""
+    import torch
+    a_ptr, lda = _mat(A, "A", torch.float32)
+    b_ptr, ldb = _mat(B, "B", torch.float32)
+    c_ptr, ldc = _mat(C, "C", torch.float32)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
+    st = lib().gemm_f32(M, N, K, float(alpha), ctypes.c_void_p(a_ptr), lda, ctypes.c_void_p(b_ptr), ldb,
+                        float(beta), ctypes.c_void_p(c_ptr), ldc, _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f32")
+
+
+def gemm_f16_f32acc_epilogue(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: int = 0, *,
+                             stream=None) -> None:
+    """C = act(alpha * A @ B + beta * C + bias): fp16 A, B; fp32 accumulate, bias and C."""
+    import torch
+    for name, t, dt in (("A", A, torch.float16), ("B", B, torch.float16), ("C", C, torch.float32)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dt or t.dim() != 2:
+            raise TypeError(f"{name} must be a 2-D CUDA {dt} tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (leading dimension = width)")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
+    bias_ptr = None
+    if bias is not None:
+        if not bias.is_cuda or bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous():
+            raise TypeError("bias must be a contiguous CUDA float32 tensor of length N")
+        bias_ptr = bias.data_ptr()
+    st = lib().gemm_f16_f32acc_epilogue(M, N, K, float(alpha), ctypes.c_void_p(A.data_ptr()),
+                                        ctypes.c_void_p(B.data_ptr()), float(beta), ctypes.c_void_p(C.data_ptr()),
+                                        ctypes.c_void_p(bias_ptr), int(act), _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_f32acc_epilogue")
+
+
+def check(stream=None) -> int:
+    """Synchronise the stream and return the watchdog status (GEMM_OK or GEMM_ERR_TIMEOUT)."""
+    return int(lib().gemm_check(_stream_handle(stream)))

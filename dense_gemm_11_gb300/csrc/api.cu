@@ -1,0 +1,228 @@
+// api.cu -- the C ABI of libgemm11.so: argument checks, degenerate shapes,
+// dispatch to the FP32 / FP16 paths, status codes, the per-(device, stream)
+// split-K scratch and the device watchdog word.
+#include <cstdint>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/gemm11.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gemm11 {
+
+// One watchdog word per device (every device that loads the library holds a
+// copy); kernels receive its address and OR kWatchdogTimeout into it.
+__device__ unsigned g_watchdog_word;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+thread_local const char *t_last_plan = "none";
+thread_local int t_last_launches = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    int sm_count = 0;
+    unsigned *watchdog = nullptr;
+    cudaError_t init_error = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+struct ScratchEntry {
+    float *partials = nullptr;
+    size_t partial_floats = 0;
+    unsigned *counters = nullptr;
+    size_t ncounters = 0;
+};
+std::mutex g_scratch_mu;
+std::map<std::pair<int, uintptr_t>, ScratchEntry> g_scratch;
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+DeviceState *device_state() {
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return nullptr;
+    DeviceState &s = g_dev[d];
+    std::call_once(s.once, [&s, d] {
+        cudaError_t e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, d);
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void **>(&s.watchdog), g_watchdog_word);
+        s.init_error = e;
+    });
+    return &s;
+}
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    DeviceState *s = device_state();
+    return (s && s->sm_count > 0) ? s->sm_count : 1;
+}
+
+unsigned *watchdog_word() {
+    DeviceState *s = device_state();
+    return s ? s->watchdog : nullptr;
+}
+
+cudaError_t acquire_scratch(cudaStream_t stream, size_t partial_floats, size_t ncounters, Scratch *out) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    ScratchEntry &e = g_scratch[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (e.partial_floats < partial_floats) {
+        // Work already queued on this stream may still use the old buffer.
+        cudaError_t r = cudaStreamSynchronize(stream);
+        if (r != cudaSuccess) return r;
+        if (e.partials) cudaFree(e.partials);
+        e.partials = nullptr;
+        e.partial_floats = 0;
+        size_t want = partial_floats + partial_floats / 4;
+        r = cudaMalloc(&e.partials, want * sizeof(float));
+        if (r != cudaSuccess) return r;
+        e.partial_floats = want;
+    }
+    if (e.ncounters < ncounters) {
+        cudaError_t r = cudaStreamSynchronize(stream);
+        if (r != cudaSuccess) return r;
+        if (e.counters) cudaFree(e.counters);
+        e.counters = nullptr;
+        e.ncounters = 0;
+        size_t want = ncounters < 1024 ? 1024 : ncounters + ncounters / 4;
+        r = cudaMalloc(&e.counters, want * sizeof(unsigned));
+        if (r != cudaSuccess) return r;
+        r = cudaMemset(e.counters, 0, want * sizeof(unsigned));
+        if (r != cudaSuccess) return r;
+        e.ncounters = want;
+    }
+    out->partials = e.partials;
+    out->counters = e.counters;
+    return cudaSuccess;
+}
+
+}  // namespace gemm11
+
+using namespace gemm11;
+
+extern "C" {
+
+int gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+             float *C, int ldc, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) {
+        t_last_plan = "noop_empty";
+        t_last_launches = 0;
+        return GEMM_OK;
+    }
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    const bool product = (K > 0) && (alpha != 0.f);
+    if (product && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CallInfo info;
+    cudaError_t e = product ? run_gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, &info)
+                            : run_scale_c(M, N, beta, C, ldc, nullptr, 0, s, &info);
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_plan = info.plan;
+    t_last_launches = info.launches;
+    return GEMM_OK;
+}
+
+int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
+                             const float *bias, int act, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (act != GEMM_ACT_NONE && act != GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) {
+        t_last_plan = "noop_empty";
+        t_last_launches = 0;
+        return GEMM_OK;
+    }
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    const bool product = (K > 0) && (alpha != 0.f);
+    if (product && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    if (product) {
+        // Tensor-map constraints: 16-byte aligned bases and row strides.
+        const bool ok = (K % 8 == 0) && (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) &&
+                        ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) &&
+                        ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+        if (!ok) return GEMM_ERR_UNSUPPORTED;
+    }
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CallInfo info;
+    cudaError_t e;
+    if (!product) {
+        e = run_scale_c(M, N, beta, C, N, bias, act, s, &info);
+    } else {
+        e = run_gemm_f16(M, N, K, alpha, A, B, beta, C, bias, act, s, &info);
+        if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_plan = info.plan;
+    t_last_launches = info.launches;
+    return GEMM_OK;
+}
+
+const char *gemm_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: arguments outside this path's constraints";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime call failed";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+        default: return "unknown gemm status";
+    }
+}
+
+int gemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gemm_check(void *stream) {
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e);
+    unsigned word = 0;
+    e = cudaMemcpy(&word, ds->watchdog, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (word != 0) {
+        // A CTA that gave up may have left split-K arrival counters non-zero.
+        const int dev = current_device();
+        {
+            std::lock_guard<std::mutex> lock(g_scratch_mu);
+            for (auto &kv : g_scratch)
+                if (kv.first.first == dev && kv.second.counters) {
+                    e = cudaMemset(kv.second.counters, 0, kv.second.ncounters * sizeof(unsigned));
+                    if (e != cudaSuccess) return fail_cuda(e);
+                }
+        }
+        const unsigned zero = 0;
+        e = cudaMemcpy(ds->watchdog, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail_cuda(e);
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+const char *gemm_last_plan(void) { return t_last_plan; }
+
+int gemm_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,548 @@
+// hgemm.cu -- FP16-input / FP32-accumulate GEMM on the 5th-generation tensor
+// cores (tcgen05) of sm_103a, with the bias / scale / GELU epilogue fused.
+//
+//   C = act(alpha * A x B + beta * C + bias),  A: M x K fp16 row-major,
+//   B: K x N fp16 row-major, C: M x N fp32 row-major, bias: N fp32.
+//
+// The DeepGEMM essay "企业官网建设流程全解析" describes the Hopper version of
+// this pipeline: TMA tiles into a 4-stage shared-memory ring guarded by
+// mbarriers (sections 3.2, 3.3), accumulators that never leave the register
+// file until the epilogue (section 4.3), the fused bias/scale/activation
+// epilogue with a single store (sections 1.3, 3.2), an L2-aware tile raster
+// (section 3.4), main tiles plus edge handling and split-K for awkward
+// shapes (sections 5.3, 6.3).  On sm_103a the same ideas map to:
+//   * one persistent CTA per SM, three warp roles: a TMA producer warp, an
+//     MMA warp whose single thread issues tcgen05.mma, and four epilogue
+//     warps;
+//   * the accumulator lives in tensor memory (TMEM), double-buffered, so the
+//     epilogue of tile i overlaps the main loop of tile i+1;
+//   * operand tiles are staged by TMA with the 128-byte swizzle, which is the
+//     canonical layout the MMA reads (A K-major, B MN-major: B is row-major
+//     K x N, so N is its contiguous dimension);
+//   * the epilogue reads TMEM with tcgen05.ld, applies alpha, beta*C, bias
+//     and GELU in registers, stages the 32x32 fp32 block in swizzled shared
+//     memory and writes it with a TMA store (edges clipped by the tensor map);
+//   * small M (<= 64): the product is computed transposed, C^T = B^T A^T, so
+//     that N fills the 128-row side of the MMA and M becomes its N side;
+//   * too few tiles for the SMs: K is split, partial tiles go to a scratch
+//     buffer, and the last epilogue warp to finish a 32-row slice of a tile
+//     (atomic arrival count) adds the slices in split order and runs the
+//     epilogue -- deterministic, and no CTA waits for another.
+// Every mbarrier wait is bounded; a timeout sets the watchdog word and the
+// CTA unwinds (waits for its TMA copies and MMAs, frees TMEM, returns).
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gemm11 {
+namespace {
+
+constexpr int kBM = 128;          // MMA M (rows of the accumulator = TMEM lanes)
+constexpr int kBK = 64;           // k per stage: one 128-byte swizzle row of fp16
+constexpr int kUmmaK = 16;        // k per tcgen05.mma (kind::f16)
+constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiWarps = 4;
+
+struct HgemmArgs {
+    int M, N, K;
+    float alpha, beta;
+    const float *bias;
+    int act;
+    float *C;  // row-major M x N (ldc = N), for beta reads and transposed stores
+    int tiles_m, tiles_n, kb_total, splits, units;
+    float *ws;
+    unsigned *counters;
+    unsigned *err;
+};
+
+__host__ __device__ constexpr int tmem_cols_for(int bn) {
+    return (2 * bn <= 32) ? 32 : (2 * bn <= 64) ? 64 : (2 * bn <= 128) ? 128 : (2 * bn <= 256) ? 256 : 512;
+}
+
+template <int BN, int STAGES, bool SWAP>
+struct HgemmCfg {
+    static constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows of 128 B
+    static constexpr int kBBytes = BN * kBK * 2;   // BN rows (or k-rows) of 128 B
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kCStageBytes = SWAP ? 0 : kEpiWarps * 32 * 32 * 4;
+    static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
+    static constexpr int kTmemCols = tmem_cols_for(BN);
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (and 32-column TMEM reads)");
+    static_assert(SWAP || BN % 64 == 0, "B tile is loaded in 64-column boxes");
+    static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
+};
+
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.f + erff(v * 0.70710678118654752f)); }
+
+struct UnitCoord {
+    int tile, split, m0, n0, kb0, kb1;
+};
+
+__device__ __forceinline__ UnitCoord decode_unit(const HgemmArgs &p, int u, int bn_tile, bool swap) {
+    UnitCoord c;
+    c.tile = u / p.splits;
+    c.split = u % p.splits;
+    if (swap) {
+        c.m0 = 0;
+        c.n0 = c.tile * kBM;
+    } else {
+        // Grouped raster: 8 M-tiles per sweep over N (L2 reuse of B panels).
+        const int group_tiles = 8 * p.tiles_n;
+        const int first_m = (c.tile / group_tiles) * 8;
+        const int gsz = min(p.tiles_m - first_m, 8);
+        c.m0 = (first_m + (c.tile % group_tiles) % gsz) * kBM;
+        c.n0 = ((c.tile % group_tiles) / gsz) * bn_tile;
+    }
+    c.kb0 = static_cast<int>(static_cast<long long>(p.kb_total) * c.split / p.splits);
+    c.kb1 = static_cast<int>(static_cast<long long>(p.kb_total) * (c.split + 1) / p.splits);
+    return c;
+}
+
+__device__ __forceinline__ void flag_timeout(volatile int *abort_flag, unsigned *err) {
+    *abort_flag = 1;
+    atomicOr(err, kWatchdogTimeout);
+}
+
+// Epilogue value for one element.
+__device__ __forceinline__ float epi_value(float acc, const HgemmArgs &p, float cold, float b) {
+    float v = p.alpha * acc;
+    if (p.beta != 0.f) v = fmaf(p.beta, cold, v);
+    v += b;
+    if (p.act == 1) v = gelu_f(v);
+    return v;
+}
+
+template <int BN, int STAGES, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    hgemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_c, const HgemmArgs p) {
+    using Cfg = HgemmCfg<BN, STAGES, SWAP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;                                 // STAGES x 16 KB (MMA operand A)
+    uint8_t *sB = smem + STAGES * Cfg::kABytes;         // STAGES x kBBytes (MMA operand B)
+    uint8_t *sC = sB + STAGES * Cfg::kBBytes;           // 4 x 4 KB epilogue staging
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + Cfg::kCStageBytes);
+    uint64_t *full = bars;                              // TMA -> MMA, per stage
+    uint64_t *empty = bars + STAGES;                    // MMA -> TMA, per stage
+    uint64_t *tfull = bars + 2 * STAGES;                // MMA -> epilogue, per accumulator
+    uint64_t *tempty = bars + 2 * STAGES + 2;           // epilogue -> MMA, per accumulator
+    uint64_t *mma_done = bars + 2 * STAGES + 4;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr int kBnTile = SWAP ? kBM : BN;  // columns of C per tile
+    constexpr uint32_t kIdesc = SWAP ? umma_idesc_f16_f32(kBM, BN, 1, 0) : umma_idesc_f16_f32(kBM, BN, 0, 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        if (!SWAP) tma_prefetch_desc(&tm_c);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    uint32_t armed = 0, armed_parity = 0;  // producer bookkeeping for the final drain
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
+            const UnitCoord c = decode_unit(p, u, kBnTile, SWAP);
+            for (int kb = c.kb0; kb < c.kb1; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+                    flag_timeout(abort_flag, p.err);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+                const int k0 = kb * kBK;
+                uint8_t *a_dst = sA + stage * Cfg::kABytes;
+                uint8_t *b_dst = sB + stage * Cfg::kBBytes;
+                if constexpr (!SWAP) {
+                    tma_load_2d(&tm_a, &full[stage], a_dst, k0, c.m0);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j) tma_load_2d(&tm_b, &full[stage], b_dst + j * 8192, c.n0 + 64 * j, k0);
+                } else {
+                    // MMA operand A = B^T (N rows, MN-major), operand B = A (M rows, K-major).
+                    tma_load_2d(&tm_b, &full[stage], a_dst, c.n0, k0);
+                    tma_load_2d(&tm_b, &full[stage], a_dst + 8192, c.n0 + 64, k0);
+                    tma_load_2d(&tm_a, &full[stage], b_dst, k0, 0);
+                }
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x, ++local) {
+            const UnitCoord c = decode_unit(p, u, kBnTile, SWAP);
+            const int buf = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(&tempty[buf], acc_phase ^ 1u)) {
+                flag_timeout(abort_flag, p.err);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+            bool ok = true;
+            for (int kb = c.kb0; kb < c.kb1; ++kb) {
+                if (!mbar_wait(&full[stage], phase)) {
+                    flag_timeout(abort_flag, p.err);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + stage * Cfg::kABytes);
+                const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                    uint64_t adesc, bdesc;
+                    if constexpr (!SWAP) {
+                        adesc = umma_desc_sw128(a_addr + kk * 32, 16, 1024);      // K-major: +32 B per k16
+                        bdesc = umma_desc_sw128(b_addr + kk * 2048, 8192, 1024);  // MN-major: +2 k-groups
+                    } else {
+                        adesc = umma_desc_sw128(a_addr + kk * 2048, 8192, 1024);
+                        bdesc = umma_desc_sw128(b_addr + kk * 32, 16, 1024);
+                    }
+                    umma_f16(d_tmem, adesc, bdesc, kIdesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(&tfull[buf]);  // accumulator complete
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue warps
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        float *stage_c = reinterpret_cast<float *>(sC + (warp - 2) * 4096);
+        int local = 0;
+        for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x, ++local) {
+            const UnitCoord c = decode_unit(p, u, kBnTile, SWAP);
+            const int buf = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(&tfull[buf], acc_phase)) {
+                flag_timeout(abort_flag, p.err);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+            // Pass 1: TMEM -> registers.  Either the finished epilogue (no split)
+            // or the raw partial to scratch (split K).
+            float *part = nullptr;
+            if (p.splits > 1)
+                part = p.ws + (static_cast<size_t>(c.tile) * p.splits + c.split) * (kBM * BN);
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + ch * 32, r);
+                tmem_wait_ld();
+                if (p.splits > 1) {
+                    // scratch layout per unit: [chunk][column j][row 0..127] -> coalesced
+                    float *dst = part + ch * 32 * kBM + row_in_tile;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dst[j * kBM] = __uint_as_float(r[j]);
+                    continue;
+                }
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if constexpr (!SWAP) {
+                    const int grow = c.m0 + row_in_tile;
+                    const int col0 = c.n0 + ch * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int gc = col0 + j;
+                        const bool in = gc < p.N;
+                        const float b = (p.bias && in) ? __ldg(p.bias + gc) : 0.f;
+                        const float cold =
+                            (p.beta != 0.f && in && grow < p.M) ? p.C[static_cast<size_t>(grow) * p.N + gc] : 0.f;
+                        v[j] = epi_value(v[j], p, cold, b);
+                    }
+                    // stage the 32x32 block (128-byte swizzle) and TMA-store it
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        *reinterpret_cast<float4 *>(stage_c + lane * 32 + ((c4 ^ (lane & 7)) << 2)) =
+                            make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && c.m0 + q * 32 < p.M && col0 < p.N) {
+                        tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
+                        bulk_commit();
+                    }
+                } else {
+                    // transposed: this thread owns column n of C, registers walk rows m
+                    const int gn = c.n0 + row_in_tile;
+                    if (gn < p.N) {
+                        const float b = p.bias ? __ldg(p.bias + gn) : 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int gm = ch * 32 + j;
+                            if (gm < p.M) {
+                                float *cp = p.C + static_cast<size_t>(gm) * p.N + gn;
+                                const float cold = p.beta != 0.f ? *cp : 0.f;
+                                *cp = epi_value(v[j], p, cold, b);
+                            }
+                        }
+                    }
+                }
+            }
+            // Accumulator buffer free for the MMA warp.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+
+            if (p.splits > 1) {
+                // Last of the splits for this 32-row slice adds them in split order.
+                __threadfence();
+                __syncwarp();
+                unsigned last = 0;
+                if (lane == 0)
+                    last = atomicAdd(&p.counters[c.tile * 4 + q], 1u) == static_cast<unsigned>(p.splits - 1);
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    const float *all = p.ws + static_cast<size_t>(c.tile) * p.splits * (kBM * BN);
+#pragma unroll 1
+                    for (int ch = 0; ch < BN / 32; ++ch) {
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __ldcg(all + ch * 32 * kBM + j * kBM + row_in_tile);
+                        for (int s = 1; s < p.splits; ++s) {
+                            const float *src = all + static_cast<size_t>(s) * (kBM * BN) + ch * 32 * kBM + row_in_tile;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] += __ldcg(src + j * kBM);
+                        }
+                        if constexpr (!SWAP) {
+                            const int grow = c.m0 + row_in_tile;
+                            const int col0 = c.n0 + ch * 32;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int gc = col0 + j;
+                                const bool in = gc < p.N;
+                                const float b = (p.bias && in) ? __ldg(p.bias + gc) : 0.f;
+                                const float cold = (p.beta != 0.f && in && grow < p.M)
+                                                       ? p.C[static_cast<size_t>(grow) * p.N + gc]
+                                                       : 0.f;
+                                v[j] = epi_value(v[j], p, cold, b);
+                            }
+                            if (lane == 0) bulk_wait_read_all();
+                            __syncwarp();
+#pragma unroll
+                            for (int c4 = 0; c4 < 8; ++c4)
+                                *reinterpret_cast<float4 *>(stage_c + lane * 32 + ((c4 ^ (lane & 7)) << 2)) =
+                                    make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0 && c.m0 + q * 32 < p.M && col0 < p.N) {
+                                tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
+                                bulk_commit();
+                            }
+                        } else {
+                            const int gn = c.n0 + row_in_tile;
+                            if (gn < p.N) {
+                                const float b = p.bias ? __ldg(p.bias + gn) : 0.f;
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    const int gm = ch * 32 + j;
+                                    if (gm < p.M) {
+                                        float *cp = p.C + static_cast<size_t>(gm) * p.N + gn;
+                                        const float cold = p.beta != 0.f ? *cp : 0.f;
+                                        *cp = epi_value(v[j], p, cold, b);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    if (lane == 0) p.counters[c.tile * 4 + q] = 0u;
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------- drain and unwind
+    if (warp == 0 && lane == 0) {
+        // every TMA copy this CTA issued must have landed before it exits
+        for (int s = 0; s < STAGES; ++s)
+            if (armed & (1u << s))
+                if (!mbar_wait(&full[s], (armed_parity >> s) & 1u)) flag_timeout(abort_flag, p.err);
+    }
+    if (warp == 1 && lane == 0) {
+        umma_commit(mma_done);  // completes when all MMAs issued above have finished
+        if (!mbar_wait(mma_done, 0)) flag_timeout(abort_flag, p.err);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem_bytes, const void *base, uint64_t inner,
+               uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_elems * static_cast<uint64_t>(elem_bytes)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool SWAP>
+cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const HgemmArgs &a,
+                         int grid, cudaStream_t stream) {
+    using Cfg = HgemmCfg<BN, STAGES, SWAP>;
+    auto kern = hgemm_tc_kernel<BN, STAGES, SWAP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, tc, a);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
+                         const float *bias, int act, cudaStream_t stream, CallInfo *info) {
+    const int sms = device_sm_count();
+    HgemmArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.bias = bias;
+    a.act = act;
+    a.C = C;
+    a.kb_total = (K + kBK - 1) / kBK;
+    a.err = watchdog_word();
+
+    // Tile table.  M <= 64: transposed product with MMA N = M rounded up to
+    // 32 or 64.  Otherwise 128 x 256 tiles (128 x 128 when N <= 128).  K is
+    // split when the tiles alone leave SMs idle.
+    const bool swap = M <= 64;
+    int bn;
+    if (swap)
+        bn = M <= 32 ? 32 : 64;
+    else
+        bn = N > 128 ? 256 : 128;
+    const int bn_tile = swap ? kBM : bn;
+    a.tiles_m = swap ? 1 : (M + kBM - 1) / kBM;
+    a.tiles_n = (N + bn_tile - 1) / bn_tile;
+    const int tiles = a.tiles_m * a.tiles_n;
+    int splits = 1;
+    if (tiles < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
+    splits = std::min(splits, 32);
+    a.splits = splits;
+    a.units = tiles * splits;
+    if (splits > 1) {
+        Scratch sc;
+        cudaError_t e =
+            acquire_scratch(stream, static_cast<size_t>(tiles) * splits * kBM * bn, static_cast<size_t>(tiles) * 4, &sc);
+        if (e != cudaSuccess) return e;
+        a.ws = sc.partials;
+        a.counters = sc.counters;
+    }
+
+    CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    bool ok = true;
+    if (!swap) {
+        ok = ok && encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, kBM);
+        ok = ok && encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK);
+        ok = ok && encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32);
+    } else {
+        ok = ok && encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, bn);
+        ok = ok && encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK);
+        tc = tb;  // unused by the transposed variant
+    }
+    if (!ok) return cudaErrorNotSupported;
+
+    const int grid = std::min(a.units, sms);
+    cudaError_t e;
+    if (!swap) {
+        if (bn == 256) {
+            e = launch_hgemm<256, 4, false>(ta, tb, tc, a, grid, stream);
+            info->plan = splits > 1 ? "tc_128x256_splitk" : "tc_128x256";
+        } else {
+            e = launch_hgemm<128, 6, false>(ta, tb, tc, a, grid, stream);
+            info->plan = splits > 1 ? "tc_128x128_splitk" : "tc_128x128";
+        }
+    } else {
+        if (bn == 32) {
+            e = launch_hgemm<32, 8, true>(ta, tb, tc, a, grid, stream);
+            info->plan = splits > 1 ? "tc_swap_n32_splitk" : "tc_swap_n32";
+        } else {
+            e = launch_hgemm<64, 8, true>(ta, tb, tc, a, grid, stream);
+            info->plan = splits > 1 ? "tc_swap_n64_splitk" : "tc_swap_n64";
+        }
+    }
+    info->launches = 1;
+    return e;
+}
+
+}  // namespace gemm11

@@ -1,0 +1,47 @@
+// internal.h -- host-side interfaces shared by the translation units of
+// libgemm11.so (not installed, not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace gemm11 {
+
+// Scratch for split-K partial tiles and their arrival counters, owned by the
+// library, one per (device, stream), grown on demand.  Counters are zero
+// between calls: every kernel that increments one resets it.
+struct Scratch {
+    float *partials = nullptr;
+    unsigned *counters = nullptr;
+};
+// Returns cudaSuccess and fills `out` with at least `partial_floats` floats and
+// `ncounters` zeroed counters usable on `stream` (current device).
+cudaError_t acquire_scratch(cudaStream_t stream, size_t partial_floats, size_t ncounters, Scratch *out);
+
+// Device address of the current device's watchdog word.
+unsigned *watchdog_word();
+
+int device_sm_count();  // multiprocessors of the current device
+
+struct CallInfo {
+    const char *plan = "none";
+    int launches = 0;
+};
+
+// ---- FP32 path (sgemm.cu) ----
+cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                         float beta, float *C, int ldc, cudaStream_t stream, CallInfo *info);
+
+// ---- FP16 tensor-core path (hgemm.cu) ----
+// Returns cudaSuccess, or cudaErrorNotSupported when the tensor-map encoder
+// is unavailable.
+cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
+                         const float *bias, int act, cudaStream_t stream, CallInfo *info);
+
+// C = beta * C over an M x N window (alpha == 0 or K == 0), with the epilogue
+// bias/act applied when given (the FP16 path), in sgemm.cu.
+cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float *bias, int act,
+                        cudaStream_t stream, CallInfo *info);
+
+}  // namespace gemm11

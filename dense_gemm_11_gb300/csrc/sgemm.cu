@@ -1,0 +1,534 @@
+// sgemm.cu -- true-FP32 GEMM on the CUDA cores (FFMA), sm_103a.
+//
+//   C = alpha * A x B + beta * C, row-major, any shape, any leading dimension
+//   ("SGEMM优化，从naive到warptiling", section 项目概况 / 问题与估算).
+//
+// Design (GB300-first; the pages' RTX 3090 / A100 kernels are prior art):
+//  * block -> warp -> thread tiling: a CTA owns a BM x BN tile of C, each warp
+//    a 64 x (4*TN) sub-tile, each thread TM x TN = 8 x 16 accumulators, the
+//    three-level hierarchy of the warptiling kernel (section k10) sized so
+//    that 6 shared-memory vector loads feed 128 FFMAs per k step;
+//  * A stays K-major in shared memory (the layout the global rows already
+//    have) and the inner loop reads 4 consecutive k of a row with one 128-bit
+//    load ("第 11 章 Tiled GEMM", section 11.6, k unrolled by four); the
+//    16-byte chunks of each 128-byte A row are XOR-swizzled by (row mod 8)
+//    so that the 8 rows a warp reads at once hit 8 different bank groups
+//    (section 11.5.2 derives the same XOR map for its tile);
+//  * STAGES-deep cp.async ring, one __syncthreads per 32-wide k slice, so
+//    global loads overlap the FFMA work (section 11.4, double buffer + async
+//    copy, generalised to more stages);
+//  * loads past M, N or K are zero-filled by cp.async's source size, the
+//    grid is rounded up and the store is guarded (section 11.3's edge rule),
+//    so no shape needs padding; 16-byte copies when A and B rows are 16-byte
+//    aligned, 4-byte copies otherwise (lda = 4099 and the like);
+//  * small grids split K across CTAs; partial tiles go to a library-owned
+//    scratch buffer and the last CTA to finish a tile (atomic arrival count)
+//    adds them in split order -- deterministic, and no CTA ever waits for
+//    another;
+//  * M == 1 and N == 1 are matrix-vector products bound by HBM; they use
+//    their own streaming kernels ("第24讲 ... GEMM 分块与 Tensor Core 思维",
+//    section 8.3 question 2 discusses these GEMV-like shapes).
+#include <algorithm>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gemm11 {
+namespace {
+
+constexpr int kBK = 32;  // k slice per pipeline stage (one 128-byte A row)
+
+struct SgemmArgs {
+    int M, N, K;
+    float alpha, beta;
+    const float *A;
+    const float *B;
+    float *C;
+    int lda, ldb, ldc;
+    int tiles_m, tiles_n;
+    int splits;
+    int c_vec;  // C rows 16-byte aligned
+    float *ws;
+    unsigned *counters;
+};
+
+__device__ __forceinline__ float f4get(const float4 &v, int q) {
+    return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
+}
+
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC>
+struct SgemmTile {
+    static constexpr int kThreads = WARPS_M * WARPS_N * 32;
+    static constexpr int kWM = 8 * TM;  // 8 lanes down M, TM rows each (8 apart)
+    static constexpr int kWN = 4 * TN;  // 4 lanes across N, TN/4 float4 each (16 apart)
+    static constexpr int kAStage = BM * kBK;
+    static constexpr int kBStage = kBK * BN;
+    static constexpr int kSmemBytes = STAGES * (kAStage + kBStage) * 4;
+    static_assert(BM == WARPS_M * kWM && BN == WARPS_N * kWN, "tile does not match warp layout");
+    static_assert(TN % 4 == 0, "TN must be a multiple of 4");
+    static_assert((BM * kBK / 4) % kThreads == 0 && (kBK * BN / 4) % kThreads == 0, "load split");
+};
+
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC>
+__global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32 <= 128) ? 2 : 1)
+    sgemm_tiled_kernel(const SgemmArgs p) {
+    using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
+    constexpr int kThreads = T::kThreads;
+    extern __shared__ __align__(128) float smem[];
+    float *As = smem;
+    float *Bs = smem + STAGES * T::kAStage;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int wm = warp / WARPS_N, wn = warp % WARPS_N;
+    const int lm = lane & 7, ln = lane >> 3;
+
+    // Grouped raster: 8 M-tiles share each sweep over N so that concurrently
+    // resident CTAs reuse the same A and B panels from L2.
+    const int t = blockIdx.x;
+    const int group_tiles = 8 * p.tiles_n;
+    const int first_m = (t / group_tiles) * 8;
+    const int gsz = min(p.tiles_m - first_m, 8);
+    const int tm = first_m + (t % group_tiles) % gsz;
+    const int tn = (t % group_tiles) / gsz;
+    const int m0 = tm * BM, n0 = tn * BN;
+
+    const int M = p.M, N = p.N, K = p.K;
+    const int KT = (K + kBK - 1) / kBK;
+    const int split = blockIdx.y;
+    const int kt0 = static_cast<int>(static_cast<long long>(KT) * split / p.splits);
+    const int kt1 = static_cast<int>(static_cast<long long>(KT) * (split + 1) / p.splits);
+    const int nkt = kt1 - kt0;
+
+    auto load_stage = [&](int stage, int kt) {
+        const int k0 = kt * kBK;
+        float *as = As + stage * T::kAStage;
+        float *bs = Bs + stage * T::kBStage;
+        if constexpr (VEC) {
+#pragma unroll
+            for (int it = 0; it < BM * kBK / 4 / kThreads; ++it) {
+                const int c = tid + it * kThreads;
+                const int row = c >> 3, kc = c & 7;
+                const int gm = m0 + row, gk = k0 + kc * 4;
+                int bytes = 0;
+                const float *src = p.A;
+                if (gm < M && gk < K) {
+                    bytes = min(K - gk, 4) * 4;
+                    src = p.A + static_cast<size_t>(gm) * p.lda + gk;
+                }
+                cp_async_16(as + row * kBK + ((kc ^ (row & 7)) << 2), src, bytes);
+            }
+#pragma unroll
+            for (int it = 0; it < kBK * BN / 4 / kThreads; ++it) {
+                const int c = tid + it * kThreads;
+                const int kr = c / (BN / 4), nc = c % (BN / 4);
+                const int gk = k0 + kr, gn = n0 + nc * 4;
+                int bytes = 0;
+                const float *src = p.B;
+                if (gk < K && gn < N) {
+                    bytes = min(N - gn, 4) * 4;
+                    src = p.B + static_cast<size_t>(gk) * p.ldb + gn;
+                }
+                cp_async_16(bs + kr * BN + nc * 4, src, bytes);
+            }
+        } else {
+#pragma unroll 4
+            for (int it = 0; it < BM * kBK / kThreads; ++it) {
+                const int e = tid + it * kThreads;
+                const int row = e >> 5, k = e & 31;
+                const int gm = m0 + row, gk = k0 + k;
+                const bool ok = gm < M && gk < K;
+                const float *src = ok ? p.A + static_cast<size_t>(gm) * p.lda + gk : p.A;
+                cp_async_4(as + row * kBK + ((((k >> 2) ^ (row & 7))) << 2) + (k & 3), src, ok ? 4 : 0);
+            }
+#pragma unroll 4
+            for (int it = 0; it < kBK * BN / kThreads; ++it) {
+                const int e = tid + it * kThreads;
+                const int kr = e / BN, n = e % BN;
+                const int gk = k0 + kr, gn = n0 + n;
+                const bool ok = gk < K && gn < N;
+                const float *src = ok ? p.B + static_cast<size_t>(gk) * p.ldb + gn : p.B;
+                cp_async_4(bs + kr * BN + n, src, ok ? 4 : 0);
+            }
+        }
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < nkt) load_stage(s, kt0 + s);
+        cp_async_commit();
+    }
+
+    for (int it = 0; it < nkt; ++it) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        const int nxt = it + STAGES - 1;
+        if (nxt < nkt) load_stage(nxt % STAGES, kt0 + nxt);
+        cp_async_commit();
+
+        const int s = it % STAGES;
+        const float *as = As + s * T::kAStage + (wm * T::kWM + lm) * kBK;
+        const float *bs = Bs + s * T::kBStage + wn * T::kWN + ln * 4;
+#pragma unroll
+        for (int kg = 0; kg < kBK / 4; ++kg) {
+            float4 a[TM];
+            const int sw = (kg ^ lm) << 2;  // row & 7 == lm for every row this thread reads
+#pragma unroll
+            for (int i = 0; i < TM; ++i) a[i] = *reinterpret_cast<const float4 *>(as + i * 8 * kBK + sw);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 b[TN / 4];
+#pragma unroll
+                for (int jj = 0; jj < TN / 4; ++jj)
+                    b[jj] = *reinterpret_cast<const float4 *>(bs + (kg * 4 + q) * BN + jj * 16);
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const float av = f4get(a[i], q);
+#pragma unroll
+                    for (int jj = 0; jj < TN / 4; ++jj) {
+                        acc[i][jj * 4 + 0] = fmaf(av, b[jj].x, acc[i][jj * 4 + 0]);
+                        acc[i][jj * 4 + 1] = fmaf(av, b[jj].y, acc[i][jj * 4 + 1]);
+                        acc[i][jj * 4 + 2] = fmaf(av, b[jj].z, acc[i][jj * 4 + 2]);
+                        acc[i][jj * 4 + 3] = fmaf(av, b[jj].w, acc[i][jj * 4 + 3]);
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    const int r_base = wm * T::kWM + lm;  // tile-local row of acc[0][*]
+    const int c_base = wn * T::kWN + ln * 4;
+
+    if (p.splits > 1) {
+        // Partial tile -> scratch (tile-local [BM][BN]); the last arriving CTA
+        // of this tile sums all splits in split order.
+        const int tile = blockIdx.x;
+        float *mine = p.ws + (static_cast<size_t>(tile) * p.splits + split) * (BM * BN);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int jj = 0; jj < TN / 4; ++jj)
+                *reinterpret_cast<float4 *>(mine + (r_base + 8 * i) * BN + c_base + 16 * jj) =
+                    make_float4(acc[i][jj * 4], acc[i][jj * 4 + 1], acc[i][jj * 4 + 2], acc[i][jj * 4 + 3]);
+        __threadfence();
+        __syncthreads();
+        __shared__ int s_last;
+        if (tid == 0) s_last = (atomicAdd(&p.counters[tile], 1u) == static_cast<unsigned>(p.splits - 1));
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        const float *base = p.ws + static_cast<size_t>(tile) * p.splits * (BM * BN);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int jj = 0; jj < TN / 4; ++jj) {
+                const size_t off = static_cast<size_t>(r_base + 8 * i) * BN + c_base + 16 * jj;
+                float4 s = __ldcg(reinterpret_cast<const float4 *>(base + off));
+                for (int sp = 1; sp < p.splits; ++sp) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + sp * (BM * BN) + off));
+                    s.x += v.x;
+                    s.y += v.y;
+                    s.z += v.z;
+                    s.w += v.w;
+                }
+                acc[i][jj * 4] = s.x;
+                acc[i][jj * 4 + 1] = s.y;
+                acc[i][jj * 4 + 2] = s.z;
+                acc[i][jj * 4 + 3] = s.w;
+            }
+        if (tid == 0) p.counters[tile] = 0u;  // ready for the next call on this stream
+    }
+
+    // Epilogue: C = alpha * acc + beta * C (C not read when beta == 0).
+    const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int gr = m0 + r_base + 8 * i;
+        if (gr >= M) continue;
+        float *crow = p.C + static_cast<size_t>(gr) * p.ldc;
+#pragma unroll
+        for (int jj = 0; jj < TN / 4; ++jj) {
+            const int gc = n0 + c_base + 16 * jj;
+            if (p.c_vec && gc + 3 < N) {
+                float4 v = make_float4(alpha * acc[i][jj * 4], alpha * acc[i][jj * 4 + 1],
+                                       alpha * acc[i][jj * 4 + 2], alpha * acc[i][jj * 4 + 3]);
+                if (beta != 0.f) {
+                    const float4 o = *reinterpret_cast<const float4 *>(crow + gc);
+                    v.x = fmaf(beta, o.x, v.x);
+                    v.y = fmaf(beta, o.y, v.y);
+                    v.z = fmaf(beta, o.z, v.z);
+                    v.w = fmaf(beta, o.w, v.w);
+                }
+                *reinterpret_cast<float4 *>(crow + gc) = v;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (gc + e < N) {
+                        float v = alpha * acc[i][jj * 4 + e];
+                        if (beta != 0.f) v = fmaf(beta, crow[gc + e], v);
+                        crow[gc + e] = v;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ GEMV
+// N == 1: y_i = alpha * sum_k A[i, k] * x_k + beta * y_i, one warp per row,
+// x_k = B[k * incx], y_i = C[i * incy].  A streams once from HBM.
+__global__ void __launch_bounds__(256) sgemv_rows_kernel(int M, int K, float alpha, const float *__restrict__ A,
+                                                         int lda, const float *__restrict__ x, int incx,
+                                                         float beta, float *y, int incy, int vec) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;
+    const float *a = A + static_cast<size_t>(row) * lda;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int kdone = 0;
+    if (vec) {
+        const int K4 = K >> 2;
+        const float4 *a4 = reinterpret_cast<const float4 *>(a);
+        const float4 *x4 = reinterpret_cast<const float4 *>(x);
+#pragma unroll 8
+        for (int c = lane; c < K4; c += 32) {
+            const float4 av = __ldcs(a4 + c);
+            const float4 xv = __ldg(x4 + c);
+            s0 = fmaf(av.x, xv.x, s0);
+            s1 = fmaf(av.y, xv.y, s1);
+            s2 = fmaf(av.z, xv.z, s2);
+            s3 = fmaf(av.w, xv.w, s3);
+        }
+        kdone = K4 << 2;
+    }
+#pragma unroll 4
+    for (int k = kdone + lane; k < K; k += 32) s0 = fmaf(a[k], x[static_cast<size_t>(k) * incx], s0);
+    float s = (s0 + s1) + (s2 + s3);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) {
+        float v = alpha * s;
+        float *yp = y + static_cast<size_t>(row) * incy;
+        if (beta != 0.f) v = fmaf(beta, *yp, v);
+        *yp = v;
+    }
+}
+
+// M == 1: y_j = alpha * sum_k x_k * B[k, j] + beta * y_j with x = A's row,
+// y = C's row.  A CTA owns 128 columns (4 per lane) and one K chunk (blockIdx.y);
+// its 8 warps take interleaved rows of B and are combined in warp order.
+// With several K chunks the partial rows go to scratch and the last CTA of a
+// column block adds them in chunk order.
+__global__ void __launch_bounds__(256) sgemv_cols_kernel(int N, int K, float alpha, const float *__restrict__ x,
+                                                         const float *__restrict__ B, int ldb, float beta,
+                                                         float *y, int vec, int splits, float *ws,
+                                                         unsigned *counters) {
+    __shared__ float4 red[8][32];
+    __shared__ int s_last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int col = blockIdx.x * 128 + lane * 4;
+    const int chunk = blockIdx.y;
+    const int k0 = static_cast<int>(static_cast<long long>(K) * chunk / splits);
+    const int k1 = static_cast<int>(static_cast<long long>(K) * (chunk + 1) / splits);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (vec && col + 3 < N) {
+#pragma unroll 8
+        for (int k = k0 + warp; k < k1; k += 8) {
+            const float xv = __ldg(x + k);
+            const float4 bv = __ldcs(reinterpret_cast<const float4 *>(B + static_cast<size_t>(k) * ldb + col));
+            s.x = fmaf(xv, bv.x, s.x);
+            s.y = fmaf(xv, bv.y, s.y);
+            s.z = fmaf(xv, bv.z, s.z);
+            s.w = fmaf(xv, bv.w, s.w);
+        }
+    } else if (col < N) {
+        for (int k = k0 + warp; k < k1; k += 8) {
+            const float xv = __ldg(x + k);
+            const float *br = B + static_cast<size_t>(k) * ldb + col;
+            s.x = fmaf(xv, br[0], s.x);
+            if (col + 1 < N) s.y = fmaf(xv, br[1], s.y);
+            if (col + 2 < N) s.z = fmaf(xv, br[2], s.z);
+            if (col + 3 < N) s.w = fmaf(xv, br[3], s.w);
+        }
+    }
+    red[warp][lane] = s;
+    __syncthreads();
+    if (warp != 0) return;
+    float4 t = red[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+        const float4 v = red[w][lane];
+        t.x += v.x;
+        t.y += v.y;
+        t.z += v.z;
+        t.w += v.w;
+    }
+    if (splits > 1) {
+        float4 *mine = reinterpret_cast<float4 *>(ws + (static_cast<size_t>(blockIdx.x) * splits + chunk) * 128);
+        mine[lane] = t;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) s_last = (atomicAdd(&counters[blockIdx.x], 1u) == static_cast<unsigned>(splits - 1));
+        __syncwarp();
+        if (!s_last) return;
+        __threadfence();
+        const float4 *all = reinterpret_cast<const float4 *>(ws + static_cast<size_t>(blockIdx.x) * splits * 128);
+        t = __ldcg(all + lane);
+        for (int c = 1; c < splits; ++c) {
+            const float4 v = __ldcg(all + c * 32 + lane);
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        if (lane == 0) counters[blockIdx.x] = 0u;
+    }
+    const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if (col + e < N) {
+            float v = alpha * tv[e];
+            if (beta != 0.f) v = fmaf(beta, y[col + e], v);
+            y[col + e] = v;
+        }
+    }
+}
+
+// alpha == 0 or K == 0: C = act(beta * C + bias) (beta == 0 writes without reading).
+__global__ void scale_c_kernel(int M, int N, float beta, float *C, int ldc, const float *bias, int act) {
+    const long long total = static_cast<long long>(M) * N;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(e / N), j = static_cast<int>(e % N);
+        float *c = C + static_cast<size_t>(i) * ldc + j;
+        float v = beta != 0.f ? beta * *c : 0.f;
+        if (bias) v += bias[j];
+        if (act == 1) v = 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+        *c = v;
+    }
+}
+
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC>
+cudaError_t launch_tiled(const SgemmArgs &a, cudaStream_t stream) {
+    using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
+    auto kern = sgemm_tiled_kernel<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.tiles_m * a.tiles_n, a.splits);
+    kern<<<grid, T::kThreads, T::kSmemBytes, stream>>>(a);
+    return cudaPeekAtLastError();
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float *bias, int act,
+                        cudaStream_t stream, CallInfo *info) {
+    if (beta == 1.f && !bias && act == 0) {
+        info->plan = "noop_beta1";
+        info->launches = 0;
+        return cudaSuccess;
+    }
+    const long long total = static_cast<long long>(M) * N;
+    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4LL * device_sm_count()));
+    scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc, bias, act);
+    info->plan = "scale_c";
+    info->launches = 1;
+    return cudaPeekAtLastError();
+}
+
+cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                         float beta, float *C, int ldc, cudaStream_t stream, CallInfo *info) {
+    const int sms = device_sm_count();
+    if (N == 1) {
+        const int vec = aligned16(A) && (lda % 4 == 0) && ldb == 1 && aligned16(B);
+        const int blocks = (M + 7) / 8;
+        sgemv_rows_kernel<<<blocks, 256, 0, stream>>>(M, K, alpha, A, lda, B, ldb, beta, C, ldc, vec);
+        info->plan = vec ? "sgemv_rows_vec" : "sgemv_rows";
+        info->launches = 1;
+        return cudaPeekAtLastError();
+    }
+    if (M == 1) {
+        const int vec = aligned16(B) && (ldb % 4 == 0);
+        const int col_blocks = (N + 127) / 128;
+        // enough CTAs for every SM to stream B: about 4 per SM, each K chunk >= 64 rows
+        int splits = std::max(1, std::min((4 * sms + col_blocks - 1) / col_blocks, K / 64));
+        splits = std::min(splits, 64);
+        Scratch sc;
+        if (splits > 1) {
+            cudaError_t e = acquire_scratch(stream, static_cast<size_t>(col_blocks) * splits * 128, col_blocks, &sc);
+            if (e != cudaSuccess) return e;
+        }
+        dim3 grid(col_blocks, splits);
+        sgemv_cols_kernel<<<grid, 256, 0, stream>>>(N, K, alpha, A, B, ldb, beta, C, vec, splits, sc.partials,
+                                                    sc.counters);
+        info->plan = splits > 1 ? "sgemv_cols_splitk" : "sgemv_cols";
+        info->launches = 1;
+        return cudaPeekAtLastError();
+    }
+
+    SgemmArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.lda = lda;
+    a.ldb = ldb;
+    a.ldc = ldc;
+    a.c_vec = aligned16(C) && (ldc % 4 == 0);
+    const bool vec = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
+    const int KT = (K + kBK - 1) / kBK;
+
+    // Tile table: 128x256 CTAs (8 warps, one per SM) when there are at least
+    // two waves of them, otherwise 128x128 CTAs (4 warps, two per SM); split K
+    // when even those leave SMs idle.
+    const int tiles_big = ((M + 127) / 128) * ((N + 255) / 256);
+    const bool big = tiles_big >= 2 * sms;
+    const int BMv = 128, BNv = big ? 256 : 128;
+    a.tiles_m = (M + BMv - 1) / BMv;
+    a.tiles_n = (N + BNv - 1) / BNv;
+    const int tiles = a.tiles_m * a.tiles_n;
+    const int slots = big ? sms : 2 * sms;
+    int splits = 1;
+    if (tiles < slots) splits = std::max(1, std::min(slots / tiles, KT / 4));
+    splits = std::min(splits, 16);
+    a.splits = splits;
+    if (splits > 1) {
+        Scratch sc;
+        cudaError_t e = acquire_scratch(stream, static_cast<size_t>(tiles) * splits * BMv * BNv, tiles, &sc);
+        if (e != cudaSuccess) return e;
+        a.ws = sc.partials;
+        a.counters = sc.counters;
+    }
+    cudaError_t e;
+    if (big) {
+        e = vec ? launch_tiled<128, 256, 2, 4, 8, 16, 3, true>(a, stream)
+                : launch_tiled<128, 256, 2, 4, 8, 16, 3, false>(a, stream);
+        info->plan = vec ? "sgemm_128x256_vec16" : "sgemm_128x256_vec4b";
+    } else {
+        e = vec ? launch_tiled<128, 128, 2, 2, 8, 16, 3, true>(a, stream)
+                : launch_tiled<128, 128, 2, 2, 8, 16, 3, false>(a, stream);
+        if (splits > 1)
+            info->plan = vec ? "sgemm_128x128_vec16_splitk" : "sgemm_128x128_vec4b_splitk";
+        else
+            info->plan = vec ? "sgemm_128x128_vec16" : "sgemm_128x128_vec4b";
+    }
+    info->launches = 1;
+    return e;
+}
+
+}  // namespace gemm11

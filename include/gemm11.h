@@ -1,0 +1,130 @@
+/*
+ * gemm11.h -- C ABI of the GB300 (sm_103a) dense GEMM library libgemm11.so.
+ *
+ * The operation is the dense matrix product
+ *
+ *     C = alpha * A x B + beta * C
+ *
+ * on row-major operands, as defined in "SGEMM优化，从naive到warptiling"
+ * (section 项目概况 / 问题与估算: A is MxK, B is KxN, C is MxN, all row-major
+ * float).  The FP16-input variant accumulates in FP32 and folds bias, scale
+ * and an activation into the epilogue, as the DeepGEMM essay
+ * "企业官网建设流程全解析" describes (sections 1.3 "定制点" and 3.2, where the
+ * epilogue applies bias, scale and activation to the accumulator before the
+ * single store).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers A, B, C, bias are DEVICE pointers (CUDA global memory of the
+ *     current device).  The caller owns them; the library keeps no pointer
+ *     after the call returns, apart from the work it has enqueued.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous and stream-ordered: they return once the work is enqueued.
+ *   - A, B and bias are read only.  C is read (only when beta != 0) and written
+ *     in place.  A, B and C must not overlap.
+ *   - Degenerate shapes follow BLAS: M == 0 or N == 0 is a no-op; K == 0 or
+ *     alpha == 0 gives C = beta * C without reading A or B; beta == 0 makes C
+ *     write-only (NaN or Inf already in C do not propagate).
+ *   - Argument errors are detected on the host before anything is launched
+ *     and return GEMM_ERR_INVALID_ARG or GEMM_ERR_UNSUPPORTED.
+ *   - A CUDA error while enqueueing returns GEMM_ERR_CUDA;
+ *     gemm_last_cuda_error() gives the cudaError_t.  Faults during execution
+ *     show up at the caller's next synchronisation, as for any CUDA kernel.
+ *   - Every wait inside a kernel is bounded.  If one runs out (a pipeline that
+ *     stopped making progress) the kernel records it in a device-side status
+ *     word and returns early; gemm_check() reports it as GEMM_ERR_TIMEOUT.
+ *   - Split-K shapes use a library-owned workspace, allocated lazily once per
+ *     (device, stream) and reused; calls on one stream are serialised by the
+ *     stream, calls on different streams use different workspaces.
+ */
+#ifndef GEMM11_H
+#define GEMM11_H
+
+#if defined(__GNUC__)
+#define GEMM11_API __attribute__((visibility("default")))
+#else
+#define GEMM11_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1, /* bad dimension, leading dimension, pointer or enum */
+    GEMM_ERR_UNSUPPORTED = -2, /* valid arguments this path cannot take (alignment) */
+    GEMM_ERR_CUDA = -3,        /* a CUDA runtime call failed; see gemm_last_cuda_error() */
+    GEMM_ERR_TIMEOUT = -4      /* a bounded in-kernel wait ran out (from gemm_check) */
+} gemm_status;
+
+typedef enum {
+    GEMM_ACT_NONE = 0, /* identity */
+    GEMM_ACT_GELU = 1  /* exact GELU: x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))) */
+} gemm_act;
+
+/*
+ * gemm_f32 -- true-FP32 SGEMM on the CUDA cores (FFMA, round-to-nearest).
+ *   C[i*ldc + j] = alpha * sum_k A[i*lda + k] * B[k*ldb + j] + beta * C[i*ldc + j]
+ * for 0 <= i < M, 0 <= j < N.  Definition: "SGEMM优化，从naive到warptiling",
+ * section 项目概况 / 问题与估算 (and the naive kernel of section k1, which is
+ * the same sum written as one thread per C element).
+ *   M, N, K  >= 0.
+ *   A        M x K, row-major, leading dimension lda >= max(1, K) (elements).
+ *   B        K x N, row-major, ldb >= max(1, N).
+ *   C        M x N, row-major, ldc >= max(1, N).
+ * Any alignment and any leading dimension are accepted; 16-byte aligned
+ * operands with leading dimensions that are multiples of 4 take the
+ * vector-load path, others a 4-byte path with the same results.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (negative size, short leading
+ * dimension, NULL pointer with a non-empty extent) or GEMM_ERR_CUDA.
+ */
+GEMM11_API int gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+             float beta, float *C, int ldc, void *stream);
+
+/*
+ * gemm_f16_f32acc_epilogue -- FP16 inputs, FP32 accumulation on the tcgen05
+ * tensor cores, fused epilogue:
+ *   C[i*N + j] = act( alpha * sum_k A[i*K + k] * B[k*N + j] + beta * C[i*N + j] + bias[j] )
+ * Definition: the DeepGEMM essay "企业官网建设流程全解析", sections 1.2
+ * (FP16 input, FP32 accumulate), 1.3 and 3.2 (bias, scale and activation in
+ * the epilogue); alpha is the scale.
+ *   A     __half, M x K, row-major, lda = K.
+ *   B     __half, K x N, row-major, ldb = N.
+ *   C     float,  M x N, row-major, ldc = N.
+ *   bias  float, length N, or NULL for no bias.
+ *   act   GEMM_ACT_NONE or GEMM_ACT_GELU.
+ * The tensor-memory-access path needs K % 8 == 0, N % 8 == 0 and A, B, C
+ * 16-byte aligned ("第24讲 ... GEMM 分块与 Tensor Core 思维", section 7.2 item 7:
+ * pad tensor-core operands to aligned sizes); anything else returns
+ * GEMM_ERR_UNSUPPORTED.  M is unrestricted.
+ */
+GEMM11_API int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B,
+                             float beta, float *C, const float *bias, int act, void *stream);
+
+/* Text for a gemm_status value (static storage, never NULL). */
+GEMM11_API const char *gemm_status_string(int status);
+
+/* cudaError_t of the last CUDA failure seen by this thread's calls (0 if none). */
+GEMM11_API int gemm_last_cuda_error(void);
+
+/*
+ * gemm_check -- synchronise `stream`, then read and clear the current
+ * device's watchdog word.  Returns GEMM_ERR_TIMEOUT if a bounded wait ran out
+ * in any kernel since the previous check, GEMM_ERR_CUDA if the synchronisation
+ * failed, GEMM_OK otherwise.
+ */
+GEMM11_API int gemm_check(void *stream);
+
+/*
+ * Introspection for tests and benchmarks: the name of the kernel plan the
+ * calling thread's last successful call used (static storage), and how many
+ * kernels that call launched.
+ */
+GEMM11_API const char *gemm_last_plan(void);
+GEMM11_API int gemm_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM11_H */

@@ -1,0 +1,89 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_11_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm11.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(g.LIB_PATH):
+        g.build()
+    return g.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GEMM11_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_binding_symbols():
+    names = declared_functions()
+    assert set(names) == set(g.EXPORTED_SYMBOLS), names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails on the host first
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, 4, 4, 4),        # negative M
+    (4, -1, 4, 4, 4, 4),        # negative N
+    (4, 4, -1, 4, 4, 4),        # negative K
+    (4, 4, 8, 7, 4, 4),         # lda < K
+    (4, 8, 4, 4, 7, 8),         # ldb < N
+    (4, 8, 4, 4, 8, 7),         # ldc < N
+])
+def test_f32_rejects_bad_dims(L, args):
+    M, N, K, lda, ldb, ldc = args
+    st = g.gemm_f32_raw(M, N, K, 1.0, FAKE, lda, FAKE, ldb, 0.0, FAKE, ldc)
+    assert st == g.GEMM_ERR_INVALID_ARG
+
+
+def test_f32_rejects_null_pointers(L):
+    assert g.gemm_f32_raw(4, 4, 4, 1.0, 0, 4, FAKE, 4, 0.0, FAKE, 4) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f32_raw(4, 4, 4, 1.0, FAKE, 4, 0, 4, 0.0, FAKE, 4) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f32_raw(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, 0, 4) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_empty_shapes_are_noops_without_cuda(L):
+    assert g.gemm_f32_raw(0, 5, 3, 1.0, 0, 3, 0, 5, 0.0, 0, 5) == g.GEMM_OK
+    assert g.last_launch_count() == 0
+    assert g.gemm_f32_raw(5, 0, 3, 1.0, 0, 3, 0, 1, 0.0, 0, 1) == g.GEMM_OK
+    assert g.gemm_f16_raw(0, 8, 8, 1.0, 0, 0, 0.0, 0) == g.GEMM_OK
+
+
+def test_f16_rejects_bad_args(L):
+    assert g.gemm_f16_raw(-1, 8, 8, 1.0, FAKE, FAKE, 0.0, FAKE) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f16_raw(8, 8, 8, 1.0, FAKE, FAKE, 0.0, FAKE, act=7) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f16_raw(8, 8, 8, 1.0, 0, FAKE, 0.0, FAKE) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f16_raw(8, 8, 8, 1.0, FAKE, FAKE, 0.0, 0) == g.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M,N,K,a,b,c", [
+    (8, 8, 12, FAKE, FAKE, FAKE),          # K % 8 != 0
+    (8, 12, 8, FAKE, FAKE, FAKE),          # N % 8 != 0
+    (8, 8, 8, FAKE + 2, FAKE, FAKE),       # A not 16-byte aligned
+    (8, 8, 8, FAKE, FAKE + 8, FAKE),       # B not 16-byte aligned
+    (8, 8, 8, FAKE, FAKE, FAKE + 4),       # C not 16-byte aligned
+])
+def test_f16_unsupported_layouts(L, M, N, K, a, b, c):
+    assert g.gemm_f16_raw(M, N, K, 1.0, a, b, 0.0, c) == g.GEMM_ERR_UNSUPPORTED
+
+
+def test_status_strings(L):
+    for st in (g.GEMM_OK, g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_UNSUPPORTED, g.GEMM_ERR_CUDA, g.GEMM_ERR_TIMEOUT):
+        assert g.status_string(st).startswith("GEMM_")
+    assert "unknown" in g.status_string(12345)

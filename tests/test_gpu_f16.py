@@ -1,0 +1,121 @@
+"""FP16-input / FP32-accumulate GEMM (tcgen05) parity against the CPU oracle,
+elementwise within |C - C_ref| <= 2e-3 * S + 1e-6, exact for small integers.
+Called through the C ABI (ctypes binding)."""
+import numpy as np
+import pytest
+
+import oracle
+from dense_gemm_11_gb300 import inputs
+from tests.helpers import TOL_F16, assert_within, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import dense_gemm_11_gb300 as g  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+def run_f16(d, alpha, beta, bias=None, act=0):
+    A = torch.from_numpy(d["A"]).to(DEV)
+    B = torch.from_numpy(d["B"]).to(DEV)
+    C = torch.from_numpy(d["C"]).to(DEV)
+    b = torch.from_numpy(bias).to(DEV) if bias is not None else None
+    g.gemm_f16_f32acc_epilogue(A, B, C, alpha=alpha, beta=beta, bias=b, act=act)
+    st = g.check()
+    assert st == g.GEMM_OK, g.status_string(st)
+    return C.cpu().numpy(), g.last_plan()
+
+
+def check_workload(name, rows=None, exact=False):
+    w = inputs.WORKLOADS[name]
+    d = inputs.make_workload(w)
+    bias = d.get("bias")
+    got, plan = run_f16(d, w.alpha, w.beta, bias, w.act)
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=w.alpha, beta=w.beta, bias=bias, act=w.act, rows=rows)
+    sel = got if rows is None else got[rows]
+    if exact:
+        np.testing.assert_array_equal(sel.astype(np.float64), ref, err_msg=f"{name} [{plan}]")
+        return plan
+    assert_within(sel, ref, S, TOL_F16, f"{name} [{plan}]")
+    return plan
+
+
+def test_f16_4096_sampled():
+    check_workload("f16_4096", rows=sample_rows(4096, seed=3))
+
+
+def test_f16_4096_small_integers_exact():
+    check_workload("f16_4096_int", rows=sample_rows(4096, seed=4), exact=True)
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3])
+def test_f16_epilogue_shapes(i):
+    w = inputs.WORKLOADS[f"f16_epi{i}"]
+    rows = None if w.M <= 128 else sample_rows(w.M, seed=5 + i)
+    check_workload(f"f16_epi{i}", rows=rows)
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 17, 32, 33, 64, 65, 127, 128, 129, 200, 300])
+@pytest.mark.parametrize("N,K", [(8, 8), (136, 72), (264, 136), (520, 1032)])
+def test_f16_ragged_shapes(M, N, K):
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=M * 131 + N + K, beta=0.0, bias=True)
+    got, plan = run_f16(d, 1.5, 0.0, d["bias"], 0)
+    ref, S = oracle.gemm(d["A"], d["B"], None, alpha=1.5, beta=0.0, bias=d["bias"])
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 1024), (128, 1024, 4096), (384, 512, 640), (5, 64, 4096)])
+def test_f16_small_integers_exact_paths(M, N, K):
+    d = inputs.make(M, N, K, kind="f16", dist="smallint", seed=6, beta=2.0)
+    got, plan = run_f16(d, 1.0, 2.0)
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=2.0, with_scale=False)
+    np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (16, 1024, 2048)])
+@pytest.mark.parametrize("act", [0, 1])
+def test_f16_beta_and_bias_epilogue(M, N, K, act):
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=7, beta=-0.5, bias=True)
+    got, plan = run_f16(d, 0.5, -0.5, d["bias"], act)
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=0.5, beta=-0.5, bias=d["bias"], act=act)
+    assert_within(got, ref, S, TOL_F16, f"beta/bias act={act} [{plan}]")
+
+
+def test_f16_beta_zero_does_not_read_c():
+    d = inputs.make(300, 264, 128, kind="f16", dist="normal_k", seed=8, beta=0.0)
+    got, plan = run_f16(d, 1.0, 0.0)
+    assert np.isfinite(got).all(), plan
+
+
+def test_f16_alpha_zero_epilogue_only():
+    rng = np.random.default_rng(9)
+    C0 = rng.uniform(-1, 1, (33, 24)).astype(np.float32)
+    bias = rng.normal(0, 0.1, 24).astype(np.float32)
+    A = torch.full((33, 16), float("nan"), dtype=torch.float16, device=DEV)
+    B = torch.full((16, 24), float("nan"), dtype=torch.float16, device=DEV)
+    C = torch.from_numpy(C0).to(DEV)
+    g.gemm_f16_f32acc_epilogue(A, B, C, alpha=0.0, beta=2.0, bias=torch.from_numpy(bias).to(DEV), act=1)
+    torch.cuda.synchronize()
+    ref, S = oracle.gemm(np.zeros((33, 16)), np.zeros((16, 24)), C0, alpha=0.0, beta=2.0, bias=bias, act=1)
+    assert_within(C.cpu().numpy(), ref, S, 1e-6, "alpha=0")
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (16, 4096, 4096), (128, 11008, 4096)])
+def test_f16_deterministic(M, N, K):
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=10, beta=0.0)
+    a, plan = run_f16(d, 1.0, 0.0)
+    b, _ = run_f16(d, 1.0, 0.0)
+    np.testing.assert_array_equal(a, b, err_msg=plan)
+
+
+def test_f16_unsupported_is_reported():
+    A = torch.zeros(8, 12, dtype=torch.float16, device=DEV)
+    B = torch.zeros(12, 8, dtype=torch.float16, device=DEV)
+    C = torch.zeros(8, 8, device=DEV)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_f32acc_epilogue(A, B, C)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED
