@@ -1,0 +1,356 @@
+"""Benchmark of the dense GEMM library at M = N = K = 4096.
+
+One step is one pass of the whole path: an FP32 SGEMM (alpha 1, beta 3, C
+reset to its seeded values first) followed by an FP16-input / FP32-accumulate
+GEMM (alpha 1, beta 0), both 4096^3, inputs resident in HBM.  L2 is flushed
+(a 256 MB write) before each GEMM; resets and flushes are outside the
+per-GEMM CUDA-event intervals that give ms_per_step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64 triple loop) on the host cores,
+on a bounded row sample of the same workload.  Under torchrun (N > 1) every
+rank runs the same workload on its own GPU (replicas: the product shards by
+output rows with no exchange), rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TFLOPS at 4096³ (FP32 SGEMM; FP16-in/FP32-acc) and % of GB300 roofline"
+SIZE = 4096
+FLOPS_ONE = 2 * SIZE ** 3
+FLOPS_STEP = 2 * FLOPS_ONE
+WORKLOAD = ("square 4096^3 x2 per step: FP32 SGEMM (alpha 1, beta 3, C reset to seeded U[-1,1] before each "
+            "run, A/B U[-1,1]) then FP16-in/FP32-acc GEMM (alpha 1, beta 0, A/B N(0,1/sqrt(K)) in fp16)")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"gemm11_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        try:
+            for line in open(self.out):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def cpu_oracle_sample(target_s: float = 12.0):
+    """Time the oracle (as it stands) on rows of both 4096^3 GEMMs; about target_s seconds."""
+    import numpy as np
+
+    import oracle
+    from dense_gemm_11_gb300 import inputs
+    threads = oracle.default_threads()
+    w32, w16 = inputs.WORKLOADS["f32_sq4096"], inputs.WORKLOADS["f16_4096"]
+    d32, d16 = inputs.make_workload(w32), inputs.make_workload(w16)
+    # calibrate on a few rows, then size the sample
+    rows = np.arange(threads, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows, threads=threads)
+    per_row = (time.perf_counter() - t0) / len(rows)
+    n = int(max(threads, min(SIZE, target_s / 2 / max(per_row, 1e-6))))
+    n = max(threads, (n // threads) * threads)
+    rows = np.linspace(0, SIZE - 1, n).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows, threads=threads)
+    t1 = time.perf_counter()
+    oracle.gemm(d16["A"], d16["B"], None, alpha=1.0, beta=0.0, rows=rows, threads=threads)
+    t2 = time.perf_counter()
+    flops = 2 * (2 * n * SIZE * SIZE)
+    secs = t2 - t0
+    return {
+        "value": flops / secs / 1e12,
+        "unit": "TFLOPS",
+        "cores": threads,
+        "kind": "oracle",
+        "sample": f"{n} of 4096 output rows of each 4096^3 GEMM (fp32 and fp16-in), fp64 accumulation; "
+                  f"{secs:.1f} s on {threads} host threads ({t1 - t0:.1f} s fp32 + {t2 - t1:.1f} s fp16)",
+    }
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on bounded row samples."""
+    if rank != 0:
+        return
+    samples = []
+    for _ in range(max(1, args.steps)):
+        samples.append(cpu_oracle_sample(target_s=8.0))
+    value = statistics.mean(s["value"] for s in samples)
+    ms = FLOPS_STEP / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE},
+        "cpu_baseline": {**samples[-1], "value": value},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import dense_gemm_11_gb300 as g
+    from dense_gemm_11_gb300 import inputs, roofline
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    hbm_gbs, tc_peak, tc_sustained, peak_src = _peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+
+    w32, w16 = inputs.WORKLOADS["f32_sq4096"], inputs.WORKLOADS["f16_4096"]
+    d32, d16 = inputs.make_workload(w32), inputs.make_workload(w16)
+    A32 = torch.from_numpy(d32["A"]).to(dev)
+    B32 = torch.from_numpy(d32["B"]).to(dev)
+    C32_0 = torch.from_numpy(d32["C"]).to(dev)
+    C32 = C32_0.clone()
+    A16 = torch.from_numpy(d16["A"]).to(dev)
+    B16 = torch.from_numpy(d16["B"]).to(dev)
+    C16 = torch.empty(SIZE, SIZE, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    launches = [0]
+    plans = {}
+
+    def gemm32():
+        g.gemm_f32(A32, B32, C32, alpha=1.0, beta=3.0, stream=stream)
+        launches[0] += g.last_launch_count()
+        plans["sgemm_f32"] = g.last_plan()
+
+    def gemm16():
+        g.gemm_f16_f32acc_epilogue(A16, B16, C16, alpha=1.0, beta=0.0, stream=stream)
+        launches[0] += g.last_launch_count()
+        plans["gemm_f16"] = g.last_plan()
+
+    def step(ev):
+        C32.copy_(C32_0)
+        flush.fill_(1.0)
+        ev[0].record(stream)
+        gemm32()
+        ev[1].record(stream)
+        flush.fill_(2.0)
+        ev[2].record(stream)
+        gemm16()
+        ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    torch.cuda.synchronize(dev)
+    assert g.check(stream) == g.GEMM_OK
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    launches[0] = 0
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_wall0 = time.perf_counter()
+        for s in range(args.steps):
+            step(events[s])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if dist:
+        dist.barrier()
+    st = g.check(stream)
+    if st != g.GEMM_OK:
+        raise RuntimeError(f"watchdog: {g.status_string(st)}")
+    t32 = [e[0].elapsed_time(e[1]) for e in events]
+    t16 = [e[2].elapsed_time(e[3]) for e in events]
+    ms_step = statistics.mean(a + b for a, b in zip(t32, t16))
+    gpu_launches = launches[0]
+
+    # e2e through the public API: pinned host inputs -> device, both GEMMs, results -> host
+    hA32 = torch.from_numpy(d32["A"]).pin_memory()
+    hB32 = torch.from_numpy(d32["B"]).pin_memory()
+    hC32 = torch.from_numpy(d32["C"]).pin_memory()
+    hA16 = torch.from_numpy(d16["A"]).pin_memory()
+    hB16 = torch.from_numpy(d16["B"]).pin_memory()
+    oC32 = torch.empty(SIZE, SIZE).pin_memory()
+    oC16 = torch.empty(SIZE, SIZE).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hA32, hB32, hC32, hA16, hB16))
+    d2h = sum(t.numel() * t.element_size() for t in (oC32, oC16))
+
+    def e2e_step():
+        A32.copy_(hA32, non_blocking=True)
+        B32.copy_(hB32, non_blocking=True)
+        C32.copy_(hC32, non_blocking=True)
+        A16.copy_(hA16, non_blocking=True)
+        B16.copy_(hB16, non_blocking=True)
+        gemm32()
+        gemm16()
+        oC32.copy_(C32, non_blocking=True)
+        oC16.copy_(C16, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, args.steps)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+
+    # max over ranks
+    times = torch.tensor([ms_step, e2e_ms, statistics.mean(t32), statistics.mean(t16)], device=dev)
+    if dist:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_step, e2e_ms, ms32, ms16 = (float(x) for x in times.tolist())
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    clocks = clk.summary()
+    f32_peak_max = roofline.fp32_fma_peak_tflops(sms, clocks.get("sm_max_mhz") or 2070.0)
+    f32_peak_obs = roofline.fp32_fma_peak_tflops(sms, clocks["sm_mhz"]) if clocks.get("sm_mhz") else None
+    ach32 = FLOPS_ONE / (ms32 * 1e-3) / 1e12
+    ach16 = FLOPS_ONE / (ms16 * 1e-3) / 1e12
+    traffic = _traffic_from_profiles()
+    value = world * FLOPS_STEP / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "dtypes": {"sgemm": "f32 (FFMA)", "tensor_core": "f16 in, f32 accumulate"},
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
+                   "l2": "flushed (256 MB write) before every GEMM, outside the timed intervals",
+                   "parallelism": f"replicas x{world}", "plans": plans},
+        "paths": {
+            "sgemm_f32": {"ms": ms32, "tflops": ach32, "frac_of_fp32_peak_at_max_clock": ach32 / f32_peak_max,
+                          "frac_of_fp32_peak_at_observed_clock": (ach32 / f32_peak_obs) if f32_peak_obs else None},
+            "gemm_f16_f32acc": {"ms": ms16, "tflops": ach16, "frac_of_measured_bf16_peak": ach16 / tc_peak},
+        },
+        "roofline": {"bound": "alu", "achieved": ach32, "peak": f32_peak_max, "unit": "TFLOP/s",
+                     "frac": ach32 / f32_peak_max, "traffic": traffic.get("sgemm"),
+                     "kernel": "sgemm_tiled_kernel (FP32 FFMA)",
+                     "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 x {clocks.get('sm_max_mhz') or 2070.0} MHz"},
+        "roofline_tensor": {"bound": "tensor", "achieved": ach16, "peak": tc_peak, "unit": "TFLOP/s",
+                            "frac": ach16 / tc_peak, "traffic": traffic.get("hgemm"),
+                            "kernel": "hgemm_tc_kernel (tcgen05 f16)",
+                            "peak_source": f"{peak_src} bf16 burst (fp16 runs at the bf16 rate)"},
+        "e2e": {"value": world * FLOPS_STEP / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample()
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def _traffic_from_profiles():
+    """DRAM bytes per launch from the committed ncu summaries, if present and current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()
