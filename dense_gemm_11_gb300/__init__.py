@@ -25,11 +25,13 @@ GEMM_ERR_INVALID_ARG = -1
 GEMM_ERR_UNSUPPORTED = -2
 GEMM_ERR_CUDA = -3
 GEMM_ERR_TIMEOUT = -4
+GEMM_ERR_SCRATCH_LIMIT = -5
 GEMM_ACT_NONE = 0
 GEMM_ACT_GELU = 1
 
-EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_status_string", "gemm_last_cuda_error",
-                    "gemm_check", "gemm_last_plan", "gemm_last_launch_count")
+EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_f16_f32acc_epilogue_noalloc",
+                    "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_last_plan",
+                    "gemm_last_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +61,8 @@ def lib():
             L.gemm_f16_f32acc_epilogue.restype = c_int
             L.gemm_f16_f32acc_epilogue.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_float,
                                                    c_void_p, c_void_p, c_int, c_void_p]
+            L.gemm_f16_f32acc_epilogue_noalloc.restype = c_int
+            L.gemm_f16_f32acc_epilogue_noalloc.argtypes = L.gemm_f16_f32acc_epilogue.argtypes
             L.gemm_status_string.restype = ctypes.c_char_p
             L.gemm_status_string.argtypes = [c_int]
             L.gemm_last_cuda_error.restype = c_int
@@ -117,6 +121,19 @@ def gemm_f16_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, s
     return lib().gemm_f16_f32acc_epilogue(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr),
                                           ctypes.c_void_p(B_ptr), float(beta), ctypes.c_void_p(C_ptr),
                                           ctypes.c_void_p(bias_ptr or None), int(act), ctypes.c_void_p(stream_ptr))
+
+
+def gemm_f16_noalloc_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, stream_ptr=0) -> int:
+    """C-ABI call of the no-allocation variant (M <= 64); returns the status code.
+
+    For callers that cannot let the library allocate device memory: the
+    split-K scratch is a fixed array inside the library.  Calls that overlap
+    on the GPU share that array and race; issue them on one stream.
+    """
+    return lib().gemm_f16_f32acc_epilogue_noalloc(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr),
+                                                  ctypes.c_void_p(B_ptr), float(beta), ctypes.c_void_p(C_ptr),
+                                                  ctypes.c_void_p(bias_ptr or None), int(act),
+                                                  ctypes.c_void_p(stream_ptr))
 
 
 def gemm_f32(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, stream=None) -> None:

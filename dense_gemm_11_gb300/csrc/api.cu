@@ -180,6 +180,45 @@ int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, co
     return GEMM_OK;
 }
 
+int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const void *A, const void *B, float beta,
+                                     float *C, const float *bias, int act, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (act != GEMM_ACT_NONE && act != GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) {
+        t_last_plan = "noop_empty";
+        t_last_launches = 0;
+        return GEMM_OK;
+    }
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    const bool product = (K > 0) && (alpha != 0.f);
+    if (product && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    if (product) {
+        const bool ok = (K % 8 == 0) && (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) &&
+                        ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) &&
+                        ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+        if (!ok || M > 64) return GEMM_ERR_UNSUPPORTED;
+    }
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CallInfo info;
+    cudaError_t e;
+    if (!product) {
+        e = run_scale_c(M, N, beta, C, N, bias, act, s, &info);
+    } else {
+        int reject = 0;
+        e = run_gemm_f16_small_m_noalloc(M, N, K, alpha, A, B, beta, C, bias, act, s, &info, &reject);
+        if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
+        if (e == cudaSuccess && reject == 1) return GEMM_ERR_UNSUPPORTED;
+        if (e == cudaSuccess && reject == 2) return GEMM_ERR_SCRATCH_LIMIT;
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_plan = info.plan;
+    t_last_launches = info.launches;
+    return GEMM_OK;
+}
+
 const char *gemm_status_string(int status) {
     switch (status) {
         case GEMM_OK: return "GEMM_OK";
@@ -187,6 +226,9 @@ const char *gemm_status_string(int status) {
         case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: arguments outside this path's constraints";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime call failed";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "GEMM_ERR_SCRATCH_LIMIT: the shape needs more split-K scratch than the fixed no-allocation "
+                   "buffer holds (4 MiB of partial tiles, 4096 counters)";
         default: return "unknown gemm status";
     }
 }

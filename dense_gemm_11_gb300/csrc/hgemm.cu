@@ -545,4 +545,100 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     return e;
 }
 
+// ------------------------------------------------------------------ no-allocation variant
+// The small-M (M <= 64) transposed split-K plan of run_gemm_f16, with its
+// split-K scratch taken from a fixed array in device memory instead of the
+// library's lazily allocated per-stream buffer, for callers that cannot let
+// the library call cudaMalloc.  The array below is part of the module image:
+// every GPU that loads the library holds it until the process exits.
+namespace {
+
+constexpr size_t kNoAllocCounters = 4096;                   // arrival counters (4 per tile)
+constexpr size_t kNoAllocPartialFloats = size_t(1) << 20;   // fp32 partial tiles: 4 MiB
+constexpr size_t kNoAllocBytes = kNoAllocCounters * sizeof(unsigned) + kNoAllocPartialFloats * sizeof(float);
+
+// Counters first (16 KiB), partial tiles after them.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocSlot {
+    std::once_flag once;
+    unsigned char *base = nullptr;  // device address of g_noalloc_scratch on that device
+    cudaError_t err = cudaSuccess;
+};
+NoAllocSlot g_noalloc_slot[64];
+
+}  // namespace
+
+cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const void *A, const void *B, float beta,
+                                         float *C, const float *bias, int act, cudaStream_t stream, CallInfo *info,
+                                         int *reject) {
+    *reject = 0;
+    if (M > 64) {
+        *reject = 1;
+        return cudaSuccess;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // Set-up, once per device, with that device current: host code cannot use
+    // the array's name as a device address, so look the address up.
+    NoAllocSlot &slot = g_noalloc_slot[dev];
+    std::call_once(slot.once, [&slot] {
+        slot.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&slot.base), g_noalloc_scratch);
+    });
+    if (slot.err != cudaSuccess) return slot.err;
+    unsigned *counters = reinterpret_cast<unsigned *>(slot.base);
+    float *partials = reinterpret_cast<float *>(slot.base + kNoAllocCounters * sizeof(unsigned));
+
+    const int sms = device_sm_count();
+    HgemmArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.bias = bias;
+    a.act = act;
+    a.C = C;
+    a.kb_total = (K + kBK - 1) / kBK;
+    a.err = watchdog_word();
+    const int bn = M <= 32 ? 32 : 64;
+    a.tiles_m = 1;
+    a.tiles_n = (N + kBM - 1) / kBM;
+    const int tiles = a.tiles_n;
+    int splits = 1;
+    if (tiles < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
+    splits = std::min(splits, 32);
+    a.splits = splits;
+    a.units = tiles * splits;
+    if (splits > 1) {
+        const size_t need_floats = static_cast<size_t>(tiles) * splits * kBM * bn;
+        const size_t need_counters = static_cast<size_t>(tiles) * 4;
+        if (need_floats > kNoAllocPartialFloats || need_counters > kNoAllocCounters) {
+            *reject = 2;
+            return cudaSuccess;
+        }
+        // The array keeps the previous call's contents: the counters must start at zero.
+        e = cudaMemsetAsync(counters, 0, need_counters * sizeof(unsigned), stream);
+        if (e != cudaSuccess) return e;
+        a.ws = partials;
+        a.counters = counters;
+    }
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, bn) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK))
+        return cudaErrorNotSupported;
+    const int grid = std::min(a.units, sms);
+    if (bn == 32) {
+        e = launch_hgemm<32, 8, true>(ta, tb, tb, a, grid, stream);
+        info->plan = splits > 1 ? "tc_swap_n32_splitk_static" : "tc_swap_n32_static";
+    } else {
+        e = launch_hgemm<64, 8, true>(ta, tb, tb, a, grid, stream);
+        info->plan = splits > 1 ? "tc_swap_n64_splitk_static" : "tc_swap_n64_static";
+    }
+    info->launches = splits > 1 ? 2 : 1;  // counter clear + GEMM
+    return e;
+}
+
 }  // namespace gemm11

@@ -39,6 +39,13 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
 cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
                          const float *bias, int act, cudaStream_t stream, CallInfo *info);
 
+// The same small-M (M <= 64) transposed split-K plan with its scratch in a
+// fixed device array (no allocation).  *reject = 1 if M > 64, 2 if the plan's
+// scratch exceeds the array; nothing is launched then.
+cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const void *A, const void *B, float beta,
+                                         float *C, const float *bias, int act, cudaStream_t stream, CallInfo *info,
+                                         int *reject);
+
 // C = beta * C over an M x N window (alpha == 0 or K == 0), with the epilogue
 // bias/act applied when given (the FP16 path), in sgemm.cu.
 cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float *bias, int act,

@@ -54,7 +54,8 @@ typedef enum {
     GEMM_ERR_INVALID_ARG = -1, /* bad dimension, leading dimension, pointer or enum */
     GEMM_ERR_UNSUPPORTED = -2, /* valid arguments this path cannot take (alignment) */
     GEMM_ERR_CUDA = -3,        /* a CUDA runtime call failed; see gemm_last_cuda_error() */
-    GEMM_ERR_TIMEOUT = -4      /* a bounded in-kernel wait ran out (from gemm_check) */
+    GEMM_ERR_TIMEOUT = -4,     /* a bounded in-kernel wait ran out (from gemm_check) */
+    GEMM_ERR_SCRATCH_LIMIT = -5 /* the no-allocation entry point's fixed scratch is too small */
 } gemm_status;
 
 typedef enum {
@@ -100,6 +101,34 @@ GEMM11_API int gemm_f32(int M, int N, int K, float alpha, const float *A, int ld
  */
 GEMM11_API int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B,
                              float beta, float *C, const float *bias, int act, void *stream);
+
+/*
+ * gemm_f16_f32acc_epilogue_noalloc -- the same operation and arguments as
+ * gemm_f16_f32acc_epilogue, restricted to M <= 64, and guaranteed not to
+ * allocate: no cudaMalloc, cudaFree or allocating library routine is called.
+ * The pages have no counterpart; this entry point exists for callers that
+ * cannot let a library allocate device memory on their behalf, for example a
+ * serving loop that reserved all of its memory up front and runs under a
+ * fixed budget (a cudaMalloc there can fail under memory pressure, and
+ * cudaMalloc/cudaFree may synchronise the whole device and stall the
+ * caller's other streams).
+ *   Scratch: the split-K partial tiles of the small-M plan live in one
+ *   file-scope device array of this library (4 MiB of fp32 partials plus
+ *   4096 arrival counters, 4 MiB + 16 KiB); every GPU that loads the library
+ *   holds it until the process exits.  A shape whose split-K plan needs more
+ *   than that returns GEMM_ERR_SCRATCH_LIMIT without launching anything;
+ *   M > 64 or the alignment rules of gemm_f16_f32acc_epilogue return
+ *   GEMM_ERR_UNSUPPORTED.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.  Every call zeroes the counters it uses (an async memset
+ *   on `stream`) before its kernel.
+ *   All calls share the one array: calls whose execution overlaps on the GPU
+ *   (for example on two streams at once) race on it and give wrong results.
+ *   Serialise them, e.g. by issuing them on one stream.
+ */
+GEMM11_API int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const void *A, const void *B,
+                                                float beta, float *C, const float *bias, int act, void *stream);
 
 /* Text for a gemm_status value (static storage, never NULL). */
 GEMM11_API const char *gemm_status_string(int status);
