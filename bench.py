@@ -324,13 +324,47 @@ def run_ours(args, rank, world, local_rank):
 
 
 def _traffic_from_profiles():
-    """DRAM bytes per launch from the committed ncu summaries, if present and current."""
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) from
+    profiles/traffic.json; an entry counts only while its kernel source is unchanged."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    out = {}
     try:
         with open(path) as f:
-            return json.load(f)
+            rec = json.load(f)
     except Exception:
-        return {}
+        return out
+    for key, r in rec.items():
+        try:
+            with open(os.path.join(ROOT, r["source"]), "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()[:16]
+            out[key] = r["bytes"] if sha == r["sha"] else None
+        except Exception:
+            out[key] = None
+    return out
+
+
+def run_profile_case(case: str, repeats: int):
+    """One GEMM of the bench workload, launched `repeats` times, for ncu captures."""
+    import torch
+
+    import dense_gemm_11_gb300 as g
+    from dense_gemm_11_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    if case == "sgemm":
+        d = inputs.make_workload(inputs.WORKLOADS["f32_sq4096"])
+        A, B, C = (torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C"))
+        for _ in range(repeats):
+            g.gemm_f32(A, B, C, alpha=1.0, beta=3.0)
+    else:
+        d = inputs.make_workload(inputs.WORKLOADS["f16_4096"])
+        A, B = (torch.from_numpy(d[k]).to(dev) for k in ("A", "B"))
+        C = torch.empty(SIZE, SIZE, device=dev)
+        for _ in range(repeats):
+            g.gemm_f16_f32acc_epilogue(A, B, C, alpha=1.0, beta=0.0)
+    torch.cuda.synchronize()
+    assert g.check() == g.GEMM_OK
+    print(f"{case}: {repeats} launches of plan {g.last_plan()}")
 
 
 def main():
@@ -340,7 +374,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["sgemm", "hgemm"], default=None,
+                    help="launch one 4096^3 GEMM of the workload a few times (for ncu) and exit")
+    ap.add_argument("--repeats", type=int, default=2)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.repeats)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))
