@@ -21,10 +21,15 @@
 //    grid is rounded up and the store is guarded (section 11.3's edge rule),
 //    so no shape needs padding; 16-byte copies when A and B rows are 16-byte
 //    aligned, 4-byte copies otherwise (lda = 4099 and the like);
-//  * small grids split K across CTAs; partial tiles go to a library-owned
-//    scratch buffer and the last CTA to finish a tile (atomic arrival count)
-//    adds them in split order -- deterministic, and no CTA ever waits for
-//    another;
+//  * the inner product step uses packed FP32 FMAs (__ffma2_rn: two
+//    independent fmaf, one rounding each, so results are bit-identical to
+//    scalar FFMA) -- half the issue slots for the same FP32 work;
+//  * large problems run one persistent CTA per SM: whole tiles round-robin,
+//    and the tiles of the last partial wave are shared out by k slices
+//    (stream-K) so that all SMs finish together; small problems split K
+//    across CTAs.  Either way partial tiles go to a library-owned scratch
+//    buffer and the last CTA to finish a tile (atomic arrival count) adds
+//    them in k order -- deterministic, and no CTA ever waits for another;
 //  * M == 1 and N == 1 are matrix-vector products bound by HBM; they use
 //    their own streaming kernels ("第24讲 ... GEMM 分块与 Tensor Core 思维",
 //    section 8.3 question 2 discusses these GEMV-like shapes).
@@ -47,11 +52,26 @@ struct SgemmArgs {
     float *C;
     int lda, ldb, ldc;
     int tiles_m, tiles_n;
-    int splits;
-    int c_vec;  // C rows 16-byte aligned
+    int splits;      // K splits (grid mode: blockIdx.y)
+    int persistent;  // 1: one CTA per SM, stream-K tail + data-parallel tiles
+    int dp_tiles;    // persistent: tiles done whole, round-robin
+    int sk_tiles;    // persistent: tiles shared out by k slices
+    int grid_ctas;   // persistent: CTAs launched
+    int c_vec;       // C rows 16-byte aligned
     float *ws;
     unsigned *counters;
 };
+
+__device__ __forceinline__ int ctaid_x() {
+    int v;
+    asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(v));
+    return v;
+}
+__device__ __forceinline__ int ctaid_y() {
+    int v;
+    asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(v));
+    return v;
+}
 
 __device__ __forceinline__ float f4get(const float4 &v, int q) {
     return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
@@ -70,12 +90,13 @@ struct SgemmTile {
     static_assert((BM * kBK / 4) % kThreads == 0 && (kBK * BN / 4) % kThreads == 0, "load split");
 };
 
-template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC>
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC, bool PERSIST>
 __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32 <= 128) ? 2 : 1)
     sgemm_tiled_kernel(const SgemmArgs p) {
     using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
     constexpr int kThreads = T::kThreads;
     extern __shared__ __align__(128) float smem[];
+    __shared__ int s_last;
     float *As = smem;
     float *Bs = smem + STAGES * T::kAStage;
 
@@ -84,200 +105,367 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32
     const int warp = tid >> 5;
     const int wm = warp / WARPS_N, wn = warp % WARPS_N;
     const int lm = lane & 7, ln = lane >> 3;
+    const int M = p.M, N = p.N, K = p.K;
+    const int KT = (K + kBK - 1) / kBK;
+
+    // Per-thread copy coordinates.  A: 8 threads per 128-byte row, rows
+    // kARowStep apart; B: BN/4 threads per row, rows kBRowStep apart.
+    constexpr int kARowStep = kThreads / 8;
+    constexpr int kBChunks = BN / 4;
+    constexpr int kBRowStep = kThreads / kBChunks;
+    const int a_row = tid >> 3, a_kc = tid & 7;
+    const int b_kr = tid / kBChunks, b_nc = tid % kBChunks;
+    const uint32_t a_dst0 = smem_u32(As) + (a_row * kBK + ((a_kc ^ (a_row & 7)) << 2)) * 4;
+    const uint32_t b_dst0 = smem_u32(Bs) + (b_kr * BN + b_nc * 4) * 4;
+
+    float acc[TM][TN];
 
     // Grouped raster: 8 M-tiles share each sweep over N so that concurrently
     // resident CTAs reuse the same A and B panels from L2.
-    const int t = blockIdx.x;
-    const int group_tiles = 8 * p.tiles_n;
-    const int first_m = (t / group_tiles) * 8;
-    const int gsz = min(p.tiles_m - first_m, 8);
-    const int tm = first_m + (t % group_tiles) % gsz;
-    const int tn = (t % group_tiles) / gsz;
-    const int m0 = tm * BM, n0 = tn * BN;
-
-    const int M = p.M, N = p.N, K = p.K;
-    const int KT = (K + kBK - 1) / kBK;
-    const int split = blockIdx.y;
-    const int kt0 = static_cast<int>(static_cast<long long>(KT) * split / p.splits);
-    const int kt1 = static_cast<int>(static_cast<long long>(KT) * (split + 1) / p.splits);
-    const int nkt = kt1 - kt0;
-
-    auto load_stage = [&](int stage, int kt) {
-        const int k0 = kt * kBK;
-        float *as = As + stage * T::kAStage;
-        float *bs = Bs + stage * T::kBStage;
-        if constexpr (VEC) {
-#pragma unroll
-            for (int it = 0; it < BM * kBK / 4 / kThreads; ++it) {
-                const int c = tid + it * kThreads;
-                const int row = c >> 3, kc = c & 7;
-                const int gm = m0 + row, gk = k0 + kc * 4;
-                int bytes = 0;
-                const float *src = p.A;
-                if (gm < M && gk < K) {
-                    bytes = min(K - gk, 4) * 4;
-                    src = p.A + static_cast<size_t>(gm) * p.lda + gk;
-                }
-                cp_async_16(as + row * kBK + ((kc ^ (row & 7)) << 2), src, bytes);
-            }
-#pragma unroll
-            for (int it = 0; it < kBK * BN / 4 / kThreads; ++it) {
-                const int c = tid + it * kThreads;
-                const int kr = c / (BN / 4), nc = c % (BN / 4);
-                const int gk = k0 + kr, gn = n0 + nc * 4;
-                int bytes = 0;
-                const float *src = p.B;
-                if (gk < K && gn < N) {
-                    bytes = min(N - gn, 4) * 4;
-                    src = p.B + static_cast<size_t>(gk) * p.ldb + gn;
-                }
-                cp_async_16(bs + kr * BN + nc * 4, src, bytes);
-            }
-        } else {
-#pragma unroll 4
-            for (int it = 0; it < BM * kBK / kThreads; ++it) {
-                const int e = tid + it * kThreads;
-                const int row = e >> 5, k = e & 31;
-                const int gm = m0 + row, gk = k0 + k;
-                const bool ok = gm < M && gk < K;
-                const float *src = ok ? p.A + static_cast<size_t>(gm) * p.lda + gk : p.A;
-                cp_async_4(as + row * kBK + ((((k >> 2) ^ (row & 7))) << 2) + (k & 3), src, ok ? 4 : 0);
-            }
-#pragma unroll 4
-            for (int it = 0; it < kBK * BN / kThreads; ++it) {
-                const int e = tid + it * kThreads;
-                const int kr = e / BN, n = e % BN;
-                const int gk = k0 + kr, gn = n0 + n;
-                const bool ok = gk < K && gn < N;
-                const float *src = ok ? p.B + static_cast<size_t>(gk) * p.ldb + gn : p.B;
-                cp_async_4(bs + kr * BN + n, src, ok ? 4 : 0);
-            }
-        }
+    auto tile_origin = [&](int t, int &m0, int &n0) {
+        const int group_tiles = 8 * p.tiles_n;
+        const int first_m = (t / group_tiles) * 8;
+        const int gsz = min(p.tiles_m - first_m, 8);
+        m0 = (first_m + (t % group_tiles) % gsz) * BM;
+        n0 = ((t % group_tiles) / gsz) * BN;
     };
 
-    float acc[TM][TN];
+    // acc = sum over k slices [kt0, kt1) of the tile at (m0, n0).
+    auto mainloop = [&](int m0, int n0, int kt0, int kt1) {
+        const int nkt = kt1 - kt0;
+        const bool full_mn = (m0 + BM <= M) && (n0 + BN <= N);
+        const float *a_src = p.A + static_cast<size_t>(m0 + a_row) * p.lda + a_kc * 4;
+        const float *b_src = p.B + static_cast<size_t>(b_kr) * p.ldb + n0 + b_nc * 4;
+
+        auto load_stage = [&](int stage, int kt) {
+            const int k0 = kt * kBK;
+            if constexpr (VEC) {
+                if (full_mn && k0 + kBK <= K) {
+                    // interior slice: every copy is a full, in-bounds 16-byte chunk
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
+                    for (int it = 0; it < BM * kBK / 4 / kThreads; ++it)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                                         a_dst0 + (stage * T::kAStage + it * kARowStep * kBK) * 4),
+                                     "l"(a_src + static_cast<size_t>(it) * kARowStep * p.lda + k0)
+                                     : "memory");
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+                    for (int it = 0; it < kBK * BN / 4 / kThreads; ++it)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                                         b_dst0 + (stage * T::kBStage + it * kBRowStep * BN) * 4),
+                                     "l"(b_src + static_cast<size_t>(k0 + it * kBRowStep) * p.ldb)
+                                     : "memory");
+                    return;
+                }
+            }
+            float *as = As + stage * T::kAStage;
+            float *bs = Bs + stage * T::kBStage;
+            if constexpr (VEC) {
+#pragma unroll
+                for (int it = 0; it < BM * kBK / 4 / kThreads; ++it) {
+                    const int c = tid + it * kThreads;
+                    const int row = c >> 3, kc = c & 7;
+                    const int gm = m0 + row, gk = k0 + kc * 4;
+                    int bytes = 0;
+                    const float *src = p.A;
+                    if (gm < M && gk < K) {
+                        bytes = min(K - gk, 4) * 4;
+                        src = p.A + static_cast<size_t>(gm) * p.lda + gk;
+                    }
+                    cp_async_16(as + row * kBK + ((kc ^ (row & 7)) << 2), src, bytes);
+                }
+#pragma unroll
+                for (int it = 0; it < kBK * BN / 4 / kThreads; ++it) {
+                    const int c = tid + it * kThreads;
+                    const int kr = c / (BN / 4), nc = c % (BN / 4);
+                    const int gk = k0 + kr, gn = n0 + nc * 4;
+                    int bytes = 0;
+                    const float *src = p.B;
+                    if (gk < K && gn < N) {
+                        bytes = min(N - gn, 4) * 4;
+                        src = p.B + static_cast<size_t>(gk) * p.ldb + gn;
+                    }
+                    cp_async_16(bs + kr * BN + nc * 4, src, bytes);
+                }
+            } else {
+#pragma unroll 4
+                for (int it = 0; it < BM * kBK / kThreads; ++it) {
+                    const int e = tid + it * kThreads;
+                    const int row = e >> 5, k = e & 31;
+                    const int gm = m0 + row, gk = k0 + k;
+                    const bool ok = gm < M && gk < K;
+                    const float *src = ok ? p.A + static_cast<size_t>(gm) * p.lda + gk : p.A;
+                    cp_async_4(as + row * kBK + ((((k >> 2) ^ (row & 7))) << 2) + (k & 3), src, ok ? 4 : 0);
+                }
+#pragma unroll 4
+                for (int it = 0; it < kBK * BN / kThreads; ++it) {
+                    const int e = tid + it * kThreads;
+                    const int kr = e / BN, n = e % BN;
+                    const int gk = k0 + kr, gn = n0 + n;
+                    const bool ok = gk < K && gn < N;
+                    const float *src = ok ? p.B + static_cast<size_t>(gk) * p.ldb + gn : p.B;
+                    cp_async_4(bs + kr * BN + n, src, ok ? 4 : 0);
+                }
+            }
+        };
 
 #pragma unroll
-    for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < nkt) load_stage(s, kt0 + s);
-        cp_async_commit();
-    }
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-    for (int it = 0; it < nkt; ++it) {
-        cp_async_wait<STAGES - 2>();
-        __syncthreads();
-        const int nxt = it + STAGES - 1;
-        if (nxt < nkt) load_stage(nxt % STAGES, kt0 + nxt);
-        cp_async_commit();
+        __syncthreads();  // the previous work item may still be reading the ring
+#pragma unroll
+        for (int s = 0; s < STAGES - 1; ++s) {
+            if (s < nkt) load_stage(s, kt0 + s);
+            cp_async_commit();
+        }
+        for (int it = 0; it < nkt; ++it) {
+            cp_async_wait<STAGES - 2>();
+            __syncthreads();
+            const int nxt = it + STAGES - 1;
+            if (nxt < nkt) load_stage(nxt % STAGES, kt0 + nxt);
+            cp_async_commit();
 
-        const int s = it % STAGES;
-        const float *as = As + s * T::kAStage + (wm * T::kWM + lm) * kBK;
-        const float *bs = Bs + s * T::kBStage + wn * T::kWN + ln * 4;
+            const int s = it % STAGES;
+            const float *as = As + s * T::kAStage + (wm * T::kWM + lm) * kBK;
+            const float *bs = Bs + s * T::kBStage + wn * T::kWN + ln * 4;
 #pragma unroll
-        for (int kg = 0; kg < kBK / 4; ++kg) {
-            float4 a[TM];
-            const int sw = (kg ^ lm) << 2;  // row & 7 == lm for every row this thread reads
+            for (int kg = 0; kg < kBK / 4; ++kg) {
+                float4 a[TM];
+                const int sw = (kg ^ lm) << 2;  // row & 7 == lm for every row this thread reads
 #pragma unroll
-            for (int i = 0; i < TM; ++i) a[i] = *reinterpret_cast<const float4 *>(as + i * 8 * kBK + sw);
+                for (int i = 0; i < TM; ++i) a[i] = *reinterpret_cast<const float4 *>(as + i * 8 * kBK + sw);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float4 b[TN / 4];
+                for (int q = 0; q < 4; ++q) {
+                    float4 b[TN / 4];
 #pragma unroll
-                for (int jj = 0; jj < TN / 4; ++jj)
-                    b[jj] = *reinterpret_cast<const float4 *>(bs + (kg * 4 + q) * BN + jj * 16);
+                    for (int jj = 0; jj < TN / 4; ++jj)
+                        b[jj] = *reinterpret_cast<const float4 *>(bs + (kg * 4 + q) * BN + jj * 16);
+                    // Outer product with packed FP32 FMAs: each __ffma2_rn is two
+                    // independent fmaf (one rounding each), acc[i][j] += a_i * b_j.
 #pragma unroll
-                for (int i = 0; i < TM; ++i) {
-                    const float av = f4get(a[i], q);
+                    for (int i = 0; i < TM; ++i) {
+                        const float av = f4get(a[i], q);
+                        const float2 a2 = make_float2(av, av);
 #pragma unroll
-                    for (int jj = 0; jj < TN / 4; ++jj) {
-                        acc[i][jj * 4 + 0] = fmaf(av, b[jj].x, acc[i][jj * 4 + 0]);
-                        acc[i][jj * 4 + 1] = fmaf(av, b[jj].y, acc[i][jj * 4 + 1]);
-                        acc[i][jj * 4 + 2] = fmaf(av, b[jj].z, acc[i][jj * 4 + 2]);
-                        acc[i][jj * 4 + 3] = fmaf(av, b[jj].w, acc[i][jj * 4 + 3]);
+                        for (int jj = 0; jj < TN / 4; ++jj) {
+                            float2 c0 = make_float2(acc[i][jj * 4], acc[i][jj * 4 + 1]);
+                            float2 c1 = make_float2(acc[i][jj * 4 + 2], acc[i][jj * 4 + 3]);
+                            c0 = __ffma2_rn(a2, make_float2(b[jj].x, b[jj].y), c0);
+                            c1 = __ffma2_rn(a2, make_float2(b[jj].z, b[jj].w), c1);
+                            acc[i][jj * 4] = c0.x;
+                            acc[i][jj * 4 + 1] = c0.y;
+                            acc[i][jj * 4 + 2] = c1.x;
+                            acc[i][jj * 4 + 3] = c1.y;
+                        }
                     }
                 }
             }
         }
-    }
-    cp_async_wait<0>();
+        cp_async_wait<0>();
+    };
 
     const int r_base = wm * T::kWM + lm;  // tile-local row of acc[0][*]
     const int c_base = wn * T::kWN + ln * 4;
 
-    if (p.splits > 1) {
-        // Partial tile -> scratch (tile-local [BM][BN]); the last arriving CTA
-        // of this tile sums all splits in split order.
-        const int tile = blockIdx.x;
-        float *mine = p.ws + (static_cast<size_t>(tile) * p.splits + split) * (BM * BN);
+    // Epilogue: C = alpha * acc + beta * C (C not read when beta == 0).
+    auto epilogue = [&](int m0, int n0) {
+        const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int gr = m0 + r_base + 8 * i;
+            if (gr >= M) continue;
+            float *crow = p.C + static_cast<size_t>(gr) * p.ldc;
+#pragma unroll
+            for (int jj = 0; jj < TN / 4; ++jj) {
+                const int gc = n0 + c_base + 16 * jj;
+                if (p.c_vec && gc + 3 < N) {
+                    float4 v = make_float4(alpha * acc[i][jj * 4], alpha * acc[i][jj * 4 + 1],
+                                           alpha * acc[i][jj * 4 + 2], alpha * acc[i][jj * 4 + 3]);
+                    if (beta != 0.f) {
+                        const float4 o = *reinterpret_cast<const float4 *>(crow + gc);
+                        v.x = fmaf(beta, o.x, v.x);
+                        v.y = fmaf(beta, o.y, v.y);
+                        v.z = fmaf(beta, o.z, v.z);
+                        v.w = fmaf(beta, o.w, v.w);
+                    }
+                    *reinterpret_cast<float4 *>(crow + gc) = v;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (gc + e < N) {
+                            float v = alpha * acc[i][jj * 4 + e];
+                            if (beta != 0.f) v = fmaf(beta, crow[gc + e], v);
+                            crow[gc + e] = v;
+                        }
+                    }
+                }
+            }
+        }
+    };
+
+    // Raw partial tile -> scratch slot (tile-local [BM][BN], row-major).
+    auto store_partial = [&](float *slot) {
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int jj = 0; jj < TN / 4; ++jj)
-                *reinterpret_cast<float4 *>(mine + (r_base + 8 * i) * BN + c_base + 16 * jj) =
+                *reinterpret_cast<float4 *>(slot + (r_base + 8 * i) * BN + c_base + 16 * jj) =
                     make_float4(acc[i][jj * 4], acc[i][jj * 4 + 1], acc[i][jj * 4 + 2], acc[i][jj * 4 + 3]);
-        __threadfence();
-        __syncthreads();
-        __shared__ int s_last;
-        if (tid == 0) s_last = (atomicAdd(&p.counters[tile], 1u) == static_cast<unsigned>(p.splits - 1));
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();
-        const float *base = p.ws + static_cast<size_t>(tile) * p.splits * (BM * BN);
+    };
+    // acc += slot (L2 reads: the slot was written by another CTA).
+    auto add_partial = [&](const float *slot, bool first) {
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int jj = 0; jj < TN / 4; ++jj) {
-                const size_t off = static_cast<size_t>(r_base + 8 * i) * BN + c_base + 16 * jj;
-                float4 s = __ldcg(reinterpret_cast<const float4 *>(base + off));
-                for (int sp = 1; sp < p.splits; ++sp) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + sp * (BM * BN) + off));
-                    s.x += v.x;
-                    s.y += v.y;
-                    s.z += v.z;
-                    s.w += v.w;
+                const float4 v =
+                    __ldcg(reinterpret_cast<const float4 *>(slot + (r_base + 8 * i) * BN + c_base + 16 * jj));
+                if (first) {
+                    acc[i][jj * 4] = v.x;
+                    acc[i][jj * 4 + 1] = v.y;
+                    acc[i][jj * 4 + 2] = v.z;
+                    acc[i][jj * 4 + 3] = v.w;
+                } else {
+                    acc[i][jj * 4] += v.x;
+                    acc[i][jj * 4 + 1] += v.y;
+                    acc[i][jj * 4 + 2] += v.z;
+                    acc[i][jj * 4 + 3] += v.w;
                 }
-                acc[i][jj * 4] = s.x;
-                acc[i][jj * 4 + 1] = s.y;
-                acc[i][jj * 4 + 2] = s.z;
-                acc[i][jj * 4 + 3] = s.w;
             }
-        if (tid == 0) p.counters[tile] = 0u;  // ready for the next call on this stream
-    }
+    };
+    // Arrival on a tile's counter; true for the CTA that completes the tile.
+    auto arrive_last = [&](unsigned *counter, unsigned arrivals) -> bool {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = (atomicAdd(counter, 1u) == arrivals - 1u);
+        __syncthreads();
+        const bool last = s_last != 0;
+        if (last) __threadfence();
+        return last;
+    };
 
-    // Epilogue: C = alpha * acc + beta * C (C not read when beta == 0).
-    const float alpha = p.alpha, beta = p.beta;
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int gr = m0 + r_base + 8 * i;
-        if (gr >= M) continue;
-        float *crow = p.C + static_cast<size_t>(gr) * p.ldc;
-#pragma unroll
-        for (int jj = 0; jj < TN / 4; ++jj) {
-            const int gc = n0 + c_base + 16 * jj;
-            if (p.c_vec && gc + 3 < N) {
-                float4 v = make_float4(alpha * acc[i][jj * 4], alpha * acc[i][jj * 4 + 1],
-                                       alpha * acc[i][jj * 4 + 2], alpha * acc[i][jj * 4 + 3]);
-                if (beta != 0.f) {
-                    const float4 o = *reinterpret_cast<const float4 *>(crow + gc);
-                    v.x = fmaf(beta, o.x, v.x);
-                    v.y = fmaf(beta, o.y, v.y);
-                    v.z = fmaf(beta, o.z, v.z);
-                    v.w = fmaf(beta, o.w, v.w);
+    if constexpr (!PERSIST) {
+        // One tile per CTA (blockIdx.x), K split blockIdx.y ways.
+        const int tile = blockIdx.x;
+        int m0, n0;
+        tile_origin(tile, m0, n0);
+        const int split = blockIdx.y;
+        const int kt0 = static_cast<int>(static_cast<long long>(KT) * split / p.splits);
+        const int kt1 = static_cast<int>(static_cast<long long>(KT) * (split + 1) / p.splits);
+        mainloop(m0, n0, kt0, kt1);
+        if (p.splits > 1) {
+            // re-read the CTA coordinates here so they are not held across the main loop
+            const int tile2 = ctaid_x(), split2 = ctaid_y();
+            float *base = p.ws + static_cast<size_t>(tile2) * p.splits * (BM * BN);
+            store_partial(base + static_cast<size_t>(split2) * (BM * BN));
+            if (!arrive_last(&p.counters[tile2], static_cast<unsigned>(p.splits))) return;
+            for (int sp = 0; sp < p.splits; ++sp) add_partial(base + static_cast<size_t>(sp) * (BM * BN), sp == 0);
+            if (tid == 0) p.counters[tile2] = 0u;  // ready for the next call on this stream
+        }
+        tile_origin(ctaid_x(), m0, n0);
+        epilogue(m0, n0);
+    } else {
+        // Persistent CTAs (one per SM).  Stream-K part first: the last
+        // sk_tiles tiles of the raster are cut into G contiguous ranges of k
+        // slices, one per CTA (each range at most one tile long, so it
+        // touches at most two tiles).  A CTA that covers a whole tile
+        // finishes it; otherwise it writes its partial tile to its slot
+        // (2 * cta + segment) and sgemm_streamk_fixup_kernel, launched next on
+        // the same stream, adds the slots of each tile in k order.  The
+        // segment list lives in shared memory so that it is not held in
+        // registers across the main loop.
+        __shared__ int s_seg[2][3];  // sk-local tile, first and end k slice
+        __shared__ int s_nseg;
+        const int G = gridDim.x;
+        const int cta = blockIdx.x;
+        if (tid == 0) {
+            int n = 0;
+            if (p.sk_tiles > 0) {
+                const long long I = static_cast<long long>(p.sk_tiles) * KT;
+                const long long b = cta * I / G, e = (cta + 1) * I / G;
+                for (long long i0 = b; i0 < e && n < 2; ++n) {
+                    const int ts = static_cast<int>(i0 / KT);
+                    s_seg[n][0] = ts;
+                    s_seg[n][1] = static_cast<int>(i0 - static_cast<long long>(ts) * KT);
+                    s_seg[n][2] = static_cast<int>(min(static_cast<long long>(KT), e - static_cast<long long>(ts) * KT));
+                    i0 = static_cast<long long>(ts + 1) * KT;
                 }
-                *reinterpret_cast<float4 *>(crow + gc) = v;
+            }
+            s_nseg = n;
+        }
+        __syncthreads();
+        const volatile int *vseg = &s_seg[0][0];
+        const int n_sk = s_nseg;
+        const int n_dp = cta < p.dp_tiles ? (p.dp_tiles - cta + G - 1) / G : 0;
+        for (int w = 0; w < n_sk + n_dp; ++w) {
+            int m0, n0;
+            if (w < n_sk) {
+                tile_origin(p.dp_tiles + vseg[w * 3], m0, n0);
+                mainloop(m0, n0, vseg[w * 3 + 1], vseg[w * 3 + 2]);
+                if (!(vseg[w * 3 + 1] == 0 && vseg[w * 3 + 2] == KT)) {
+                    store_partial(p.ws + static_cast<size_t>(2 * ctaid_x() + (vseg[w * 3] - vseg[0])) * (BM * BN));
+                    continue;
+                }
+                tile_origin(p.dp_tiles + vseg[w * 3], m0, n0);
             } else {
+                tile_origin(cta + (w - n_sk) * G, m0, n0);
+                mainloop(m0, n0, 0, KT);
+                tile_origin(ctaid_x() + (w - n_sk) * G, m0, n0);
+            }
+            epilogue(m0, n0);
+        }
+    }
+}
+
+// Stream-K fixup: for stream-K tile blockIdx.x, add the partial tiles of the
+// CTAs that covered it in k order (owner(i) = ((i+1)G - 1) / I is the CTA
+// whose range holds k slice i) and apply the epilogue.  Tiles covered whole
+// by one CTA were finished by the main kernel.  blockIdx.y picks 8 rows.
+template <int BM, int BN>
+__global__ void __launch_bounds__(256) sgemm_streamk_fixup_kernel(const SgemmArgs p) {
+    const int KT = (p.K + kBK - 1) / kBK;
+    const int G = p.grid_ctas;
+    const int ts = blockIdx.x;
+    const long long I = static_cast<long long>(p.sk_tiles) * KT;
+    const long long f = static_cast<long long>(ts) * KT;
+    const int c0 = static_cast<int>(((f + 1) * G - 1) / I);
+    const int c1 = static_cast<int>(((f + KT) * G - 1) / I);
+    if (c0 == c1) return;
+    const int tile = p.dp_tiles + ts;
+    const int group_tiles = 8 * p.tiles_n;
+    const int first_m = (tile / group_tiles) * 8;
+    const int gsz = min(p.tiles_m - first_m, 8);
+    const int m0 = (first_m + (tile % group_tiles) % gsz) * BM;
+    const int n0 = ((tile % group_tiles) / gsz) * BN;
+    constexpr int kVecPerRow = BN / 4;
+    for (int v = threadIdx.x; v < 8 * kVecPerRow; v += blockDim.x) {
+        const int r = blockIdx.y * 8 + v / kVecPerRow;
+        const int c = (v % kVecPerRow) * 4;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int cc = c0; cc <= c1; ++cc) {
+            const int tf = static_cast<int>((static_cast<long long>(cc) * I / G) / KT);
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(
+                p.ws + static_cast<size_t>(2 * cc + (ts - tf)) * (BM * BN) + r * BN + c));
+            if (cc == c0) {
+                s = x;
+            } else {
+                s.x += x.x;
+                s.y += x.y;
+                s.z += x.z;
+                s.w += x.w;
+            }
+        }
+        const int gr = m0 + r, gc = n0 + c;
+        if (gr >= p.M) continue;
+        float *crow = p.C + static_cast<size_t>(gr) * p.ldc;
+        const float sv[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (gc + e < N) {
-                        float v = alpha * acc[i][jj * 4 + e];
-                        if (beta != 0.f) v = fmaf(beta, crow[gc + e], v);
-                        crow[gc + e] = v;
-                    }
-                }
+        for (int e = 0; e < 4; ++e) {
+            if (gc + e < p.N) {
+                float val = p.alpha * sv[e];
+                if (p.beta != 0.f) val = fmaf(p.beta, crow[gc + e], val);
+                crow[gc + e] = val;
             }
         }
     }
@@ -417,13 +605,13 @@ __global__ void scale_c_kernel(int M, int N, float beta, float *C, int ldc, cons
     }
 }
 
-template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC>
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC, bool PERSIST>
 cudaError_t launch_tiled(const SgemmArgs &a, cudaStream_t stream) {
     using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
-    auto kern = sgemm_tiled_kernel<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
+    auto kern = sgemm_tiled_kernel<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC, PERSIST>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.tiles_m * a.tiles_n, a.splits);
+    dim3 grid = PERSIST ? dim3(a.grid_ctas, 1) : dim3(a.tiles_m * a.tiles_n, a.splits);
     kern<<<grid, T::kThreads, T::kSmemBytes, stream>>>(a);
     return cudaPeekAtLastError();
 }
@@ -493,41 +681,69 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
     const bool vec = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
     const int KT = (K + kBK - 1) / kBK;
 
-    // Tile table: 128x256 CTAs (8 warps, one per SM) when there are at least
-    // two waves of them, otherwise 128x128 CTAs (4 warps, two per SM); split K
-    // when even those leave SMs idle.
+    // Tile table.  128x256 CTAs (8 warps, one per SM) run persistently when
+    // there is enough work for every SM: whole tiles round-robin, and the
+    // tiles of the last partial wave shared out by k slices (stream-K), so
+    // every SM gets the same number of k slices.  Smaller problems use
+    // 128x128 CTAs (4 warps, two per SM) with K split across CTAs.
     const int tiles_big = ((M + 127) / 128) * ((N + 255) / 256);
-    const bool big = tiles_big >= 2 * sms;
-    const int BMv = 128, BNv = big ? 256 : 128;
-    a.tiles_m = (M + BMv - 1) / BMv;
-    a.tiles_n = (N + BNv - 1) / BNv;
-    const int tiles = a.tiles_m * a.tiles_n;
-    const int slots = big ? sms : 2 * sms;
-    int splits = 1;
-    if (tiles < slots) splits = std::max(1, std::min(slots / tiles, KT / 4));
-    splits = std::min(splits, 16);
-    a.splits = splits;
-    if (splits > 1) {
-        Scratch sc;
-        cudaError_t e = acquire_scratch(stream, static_cast<size_t>(tiles) * splits * BMv * BNv, tiles, &sc);
-        if (e != cudaSuccess) return e;
-        a.ws = sc.partials;
-        a.counters = sc.counters;
-    }
+    const bool big = tiles_big >= sms || static_cast<long long>(tiles_big) * KT >= 4LL * sms;
     cudaError_t e;
     if (big) {
-        e = vec ? launch_tiled<128, 256, 2, 4, 8, 16, 3, true>(a, stream)
-                : launch_tiled<128, 256, 2, 4, 8, 16, 3, false>(a, stream);
-        info->plan = vec ? "sgemm_128x256_vec16" : "sgemm_128x256_vec4b";
+        a.tiles_m = (M + 127) / 128;
+        a.tiles_n = (N + 255) / 256;
+        a.splits = 1;
+        a.persistent = 1;
+        const int rem = tiles_big % sms;
+        a.dp_tiles = tiles_big - rem;
+        a.sk_tiles = rem;
+        if (rem != 0 && static_cast<long long>(rem) * KT < 2LL * sms) {
+            a.dp_tiles = tiles_big;  // too few k slices to share out: whole tiles only
+            a.sk_tiles = 0;
+        }
+        a.grid_ctas = a.sk_tiles > 0 ? sms : std::min(sms, tiles_big);
+        if (a.sk_tiles > 0) {
+            Scratch sc;
+            e = acquire_scratch(stream, static_cast<size_t>(2) * a.grid_ctas * 128 * 256, 0, &sc);
+            if (e != cudaSuccess) return e;
+            a.ws = sc.partials;
+            a.counters = sc.counters;
+        }
+        e = vec ? launch_tiled<128, 256, 2, 4, 8, 16, 3, true, true>(a, stream)
+                : launch_tiled<128, 256, 2, 4, 8, 16, 3, false, true>(a, stream);
+        if (e != cudaSuccess) return e;
+        if (a.sk_tiles > 0) {
+            sgemm_streamk_fixup_kernel<128, 256><<<dim3(a.sk_tiles, 128 / 8), 256, 0, stream>>>(a);
+            e = cudaPeekAtLastError();
+        }
+        info->launches = a.sk_tiles > 0 ? 2 : 1;
+        if (a.sk_tiles > 0)
+            info->plan = vec ? "sgemm_128x256_vec16_streamk" : "sgemm_128x256_vec4b_streamk";
+        else
+            info->plan = vec ? "sgemm_128x256_vec16" : "sgemm_128x256_vec4b";
     } else {
-        e = vec ? launch_tiled<128, 128, 2, 2, 8, 16, 3, true>(a, stream)
-                : launch_tiled<128, 128, 2, 2, 8, 16, 3, false>(a, stream);
+        a.tiles_m = (M + 127) / 128;
+        a.tiles_n = (N + 127) / 128;
+        const int tiles = a.tiles_m * a.tiles_n;
+        int splits = 1;
+        if (tiles < 2 * sms) splits = std::max(1, std::min(2 * sms / tiles, KT / 4));
+        splits = std::min(splits, 16);
+        a.splits = splits;
+        if (splits > 1) {
+            Scratch sc;
+            e = acquire_scratch(stream, static_cast<size_t>(tiles) * splits * 128 * 128, tiles, &sc);
+            if (e != cudaSuccess) return e;
+            a.ws = sc.partials;
+            a.counters = sc.counters;
+        }
+        e = vec ? launch_tiled<128, 128, 2, 2, 8, 16, 3, true, false>(a, stream)
+                : launch_tiled<128, 128, 2, 2, 8, 16, 3, false, false>(a, stream);
         if (splits > 1)
             info->plan = vec ? "sgemm_128x128_vec16_splitk" : "sgemm_128x128_vec4b_splitk";
         else
             info->plan = vec ? "sgemm_128x128_vec16" : "sgemm_128x128_vec4b";
+        info->launches = 1;
     }
-    info->launches = 1;
     return e;
 }
 
