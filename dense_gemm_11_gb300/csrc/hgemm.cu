@@ -59,6 +59,10 @@ struct HgemmArgs {
     float *ws;
     unsigned *counters;
     unsigned *err;
+    // stream-K schedule (non-transposed, splits == 1): the first dp_tiles
+    // tiles of the raster are whole units, the last sk_tiles are shared out
+    // by k blocks over the grid; partial tiles go to 2 slots per CTA.
+    int streamk, dp_tiles, sk_tiles;
 };
 
 __host__ __device__ constexpr int tmem_cols_for(int bn) {
@@ -83,6 +87,7 @@ __device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.f + erff
 
 struct UnitCoord {
     int tile, split, m0, n0, kb0, kb1;
+    int slot;  // stream-K partial slot, -1 when the unit finishes its tile
 };
 
 __device__ __forceinline__ UnitCoord decode_unit(const HgemmArgs &p, int u, int bn_tile, bool swap) {
@@ -102,7 +107,50 @@ __device__ __forceinline__ UnitCoord decode_unit(const HgemmArgs &p, int u, int 
     }
     c.kb0 = static_cast<int>(static_cast<long long>(p.kb_total) * c.split / p.splits);
     c.kb1 = static_cast<int>(static_cast<long long>(p.kb_total) * (c.split + 1) / p.splits);
+    c.slot = -1;
     return c;
+}
+
+// The idx-th unit of this CTA; false past the last one.  All three warp
+// roles walk the same sequence.  Stream-K: CTA c owns k blocks
+// [c*I/G, (c+1)*I/G) of the I = sk_tiles * kb_total blocks of the stream-K
+// tiles (at most two tiles, since sk_tiles < G), then data-parallel tiles
+// c, c + G, ...
+__device__ __forceinline__ bool next_unit(const HgemmArgs &p, int idx, int bn_tile, bool swap, UnitCoord &c) {
+    if (!p.streamk) {
+        const int u = blockIdx.x + idx * gridDim.x;
+        if (u >= p.units) return false;
+        c = decode_unit(p, u, bn_tile, swap);
+        return true;
+    }
+    const int G = gridDim.x, cta = blockIdx.x;
+    const long long KB = p.kb_total;
+    const long long I = static_cast<long long>(p.sk_tiles) * KB;
+    const long long b = cta * I / G, e = (cta + 1) * I / G;
+    const int nsk = (p.sk_tiles > 0 && b < e) ? static_cast<int>((e - 1) / KB - b / KB + 1) : 0;
+    int tile;
+    if (idx < nsk) {
+        const int ts = static_cast<int>(b / KB) + idx;
+        const long long t0 = static_cast<long long>(ts) * KB;
+        tile = p.dp_tiles + ts;
+        c.kb0 = static_cast<int>(max(b, t0) - t0);
+        c.kb1 = static_cast<int>(min(e, t0 + KB) - t0);
+        c.slot = (c.kb0 == 0 && c.kb1 == p.kb_total) ? -1 : 2 * cta + idx;
+    } else {
+        tile = cta + (idx - nsk) * G;
+        if (tile >= p.dp_tiles) return false;
+        c.kb0 = 0;
+        c.kb1 = p.kb_total;
+        c.slot = -1;
+    }
+    c.tile = tile;
+    c.split = 0;
+    const int group_tiles = 8 * p.tiles_n;
+    const int first_m = (tile / group_tiles) * 8;
+    const int gsz = min(p.tiles_m - first_m, 8);
+    c.m0 = (first_m + (tile % group_tiles) % gsz) * kBM;
+    c.n0 = ((tile % group_tiles) / gsz) * bn_tile;
+    return true;
 }
 
 __device__ __forceinline__ void flag_timeout(volatile int *abort_flag, unsigned *err) {
@@ -176,8 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ TMA producer
         int stage = 0;
         uint32_t phase = 0;
-        for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
-            const UnitCoord c = decode_unit(p, u, kBnTile, SWAP);
+        for (int idx = 0; !*abort_flag; ++idx) {
+            UnitCoord c;
+            if (!next_unit(p, idx, kBnTile, SWAP, c)) break;
             for (int kb = c.kb0; kb < c.kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u)) {
                     flag_timeout(abort_flag, p.err);
@@ -210,8 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         int local = 0;
-        for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x, ++local) {
-            const UnitCoord c = decode_unit(p, u, kBnTile, SWAP);
+        for (int idx = 0; !*abort_flag; ++idx, ++local) {
+            UnitCoord c;
+            if (!next_unit(p, idx, kBnTile, SWAP, c)) break;
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait(&tempty[buf], acc_phase ^ 1u)) {
@@ -257,8 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_tile = q * 32 + lane;
         float *stage_c = reinterpret_cast<float *>(sC + (warp - 2) * 4096);
         int local = 0;
-        for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x, ++local) {
-            const UnitCoord c = decode_unit(p, u, kBnTile, SWAP);
+        for (int idx = 0; !*abort_flag; ++idx, ++local) {
+            UnitCoord c;
+            if (!next_unit(p, idx, kBnTile, SWAP, c)) break;
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait(&tfull[buf], acc_phase)) {
@@ -269,15 +320,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
             // Pass 1: TMEM -> registers.  Either the finished epilogue (no split)
             // or the raw partial to scratch (split K).
+            // A unit leaves a partial tile when K is split evenly (splits > 1) or
+            // when it covers only part of a stream-K tile (slot >= 0).
+            const bool partial = (p.splits > 1) || (c.slot >= 0);
             float *part = nullptr;
-            if (p.splits > 1)
-                part = p.ws + (static_cast<size_t>(c.tile) * p.splits + c.split) * (kBM * BN);
+            if (partial)
+                part = p.ws + (c.slot >= 0 ? static_cast<size_t>(c.slot)
+                                           : static_cast<size_t>(c.tile) * p.splits + c.split) * (kBM * BN);
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_row + ch * 32, r);
                 tmem_wait_ld();
-                if (p.splits > 1) {
+                if (partial) {
                     // scratch layout per unit: [chunk][column j][row 0..127] -> coalesced
                     float *dst = part + ch * 32 * kBM + row_in_tile;
 #pragma unroll
@@ -334,24 +389,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
 
-            if (p.splits > 1) {
-                // Last of the splits for this 32-row slice adds them in split order.
+            if (partial) {
+                // The last contributor to arrive on this 32-row slice of the
+                // tile adds all contributions in k order (even splits: split
+                // index; stream-K: the owning CTAs c0..c1 in order).
+                int n_contrib, c0 = 0, cnt_idx;
+                long long I = 0;
+                if (c.slot >= 0) {
+                    const long long KB = p.kb_total;
+                    I = static_cast<long long>(p.sk_tiles) * KB;
+                    const long long f = static_cast<long long>(c.tile - p.dp_tiles) * KB;
+                    c0 = static_cast<int>(((f + 1) * gridDim.x - 1) / I);
+                    n_contrib = static_cast<int>(((f + KB) * gridDim.x - 1) / I) - c0 + 1;
+                    cnt_idx = (c.tile - p.dp_tiles) * 4 + q;
+                } else {
+                    n_contrib = p.splits;
+                    cnt_idx = c.tile * 4 + q;
+                }
                 __threadfence();
                 __syncwarp();
                 unsigned last = 0;
-                if (lane == 0)
-                    last = atomicAdd(&p.counters[c.tile * 4 + q], 1u) == static_cast<unsigned>(p.splits - 1);
+                if (lane == 0) last = atomicAdd(&p.counters[cnt_idx], 1u) == static_cast<unsigned>(n_contrib - 1);
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    const float *all = p.ws + static_cast<size_t>(c.tile) * p.splits * (kBM * BN);
+                    auto contrib = [&](int i) -> const float * {
+                        size_t slot;
+                        if (c.slot >= 0) {
+                            const int cc = c0 + i;
+                            const int ts = c.tile - p.dp_tiles;
+                            slot = 2 * static_cast<size_t>(cc) +
+                                   static_cast<size_t>(ts - static_cast<int>((cc * I / gridDim.x) / p.kb_total));
+                        } else {
+                            slot = static_cast<size_t>(c.tile) * p.splits + i;
+                        }
+                        return p.ws + slot * (kBM * BN);
+                    };
 #pragma unroll 1
                     for (int ch = 0; ch < BN / 32; ++ch) {
                         float v[32];
+                        const float *src0 = contrib(0) + ch * 32 * kBM + row_in_tile;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __ldcg(all + ch * 32 * kBM + j * kBM + row_in_tile);
-                        for (int s = 1; s < p.splits; ++s) {
-                            const float *src = all + static_cast<size_t>(s) * (kBM * BN) + ch * 32 * kBM + row_in_tile;
+                        for (int j = 0; j < 32; ++j) v[j] = __ldcg(src0 + j * kBM);
+                        for (int s = 1; s < n_contrib; ++s) {
+                            const float *src = contrib(s) + ch * 32 * kBM + row_in_tile;
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] += __ldcg(src + j * kBM);
                         }
@@ -396,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    if (lane == 0) p.counters[c.tile * 4 + q] = 0u;
+                    if (lane == 0) p.counters[cnt_idx] = 0u;
                 }
             }
         }
@@ -482,8 +563,12 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     a.err = watchdog_word();
 
     // Tile table.  M <= 64: transposed product with MMA N = M rounded up to
-    // 32 or 64.  Otherwise 128 x 256 tiles (128 x 128 when N <= 128).  K is
-    // split when the tiles alone leave SMs idle.
+    // 32 or 64.  Otherwise 128 x 256 tiles (128 x 128 when N <= 128).  With
+    // at least a wave of tiles, one persistent CTA per SM takes whole tiles
+    // round-robin and the tiles of the last partial wave are shared out by
+    // k blocks (stream-K); with fewer tiles than
+    // SMs, K is split evenly.  Partial tiles are reduced in k order by the
+    // last contributor to arrive (per 32-row slice), inside the kernel.
     const bool swap = M <= 64;
     int bn;
     if (swap)
@@ -499,10 +584,33 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     splits = std::min(splits, 32);
     a.splits = splits;
     a.units = tiles * splits;
+    // Stream-K for the partial last wave is implemented (next_unit) but off:
+    // on GB300 at 4096^3 it measured slower (126 us vs 110 us) than whole
+    // tiles, because the last arriver's reduction of ~2.7 partial tiles is
+    // latency-bound inside one CTA.
+    constexpr bool kUseStreamK = false;
+    if (kUseStreamK && !swap && tiles >= sms) {
+        const int rem = tiles % sms;
+        const long long share = static_cast<long long>(rem) * a.kb_total / sms;  // k blocks per CTA
+        if (rem != 0 && share >= 2 && a.kb_total / share + 2 <= 64) {
+            a.streamk = 1;
+            a.dp_tiles = tiles - rem;
+            a.sk_tiles = rem;
+        }
+    }
     if (splits > 1) {
         Scratch sc;
         cudaError_t e =
             acquire_scratch(stream, static_cast<size_t>(tiles) * splits * kBM * bn, static_cast<size_t>(tiles) * 4, &sc);
+        if (e != cudaSuccess) return e;
+        a.ws = sc.partials;
+        a.counters = sc.counters;
+    }
+    const int grid = a.streamk ? sms : std::min(a.units, sms);
+    if (a.streamk) {
+        Scratch sc;
+        cudaError_t e = acquire_scratch(stream, static_cast<size_t>(2) * grid * kBM * bn,
+                                        static_cast<size_t>(a.sk_tiles) * 4, &sc);
         if (e != cudaSuccess) return e;
         a.ws = sc.partials;
         a.counters = sc.counters;
@@ -522,15 +630,14 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     }
     if (!ok) return cudaErrorNotSupported;
 
-    const int grid = std::min(a.units, sms);
     cudaError_t e;
     if (!swap) {
         if (bn == 256) {
             e = launch_hgemm<256, 4, false>(ta, tb, tc, a, grid, stream);
-            info->plan = splits > 1 ? "tc_128x256_splitk" : "tc_128x256";
+            info->plan = a.streamk ? "tc_128x256_streamk" : (splits > 1 ? "tc_128x256_splitk" : "tc_128x256");
         } else {
             e = launch_hgemm<128, 6, false>(ta, tb, tc, a, grid, stream);
-            info->plan = splits > 1 ? "tc_128x128_splitk" : "tc_128x128";
+            info->plan = a.streamk ? "tc_128x128_streamk" : (splits > 1 ? "tc_128x128_splitk" : "tc_128x128");
         }
     } else {
         if (bn == 32) {

@@ -438,16 +438,24 @@ __global__ void __launch_bounds__(256) sgemm_streamk_fixup_kernel(const SgemmArg
     const int gsz = min(p.tiles_m - first_m, 8);
     const int m0 = (first_m + (tile % group_tiles) % gsz) * BM;
     const int n0 = ((tile % group_tiles) / gsz) * BN;
+    // slot of each contributing CTA, in k order (a tile has few contributors)
+    constexpr int kMaxOwners = 64;
+    __shared__ int s_slot[kMaxOwners];
+    const int n_own = min(c1 - c0 + 1, kMaxOwners);
+    for (int i = threadIdx.x; i < n_own; i += blockDim.x) {
+        const int cc = c0 + i;
+        s_slot[i] = 2 * cc + (ts - static_cast<int>((static_cast<long long>(cc) * I / G) / KT));
+    }
+    __syncthreads();
     constexpr int kVecPerRow = BN / 4;
     for (int v = threadIdx.x; v < 8 * kVecPerRow; v += blockDim.x) {
         const int r = blockIdx.y * 8 + v / kVecPerRow;
         const int c = (v % kVecPerRow) * 4;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc = c0; cc <= c1; ++cc) {
-            const int tf = static_cast<int>((static_cast<long long>(cc) * I / G) / KT);
+        for (int i = 0; i < n_own; ++i) {
             const float4 x = __ldcg(reinterpret_cast<const float4 *>(
-                p.ws + static_cast<size_t>(2 * cc + (ts - tf)) * (BM * BN) + r * BN + c));
-            if (cc == c0) {
+                p.ws + static_cast<size_t>(s_slot[i]) * (BM * BN) + r * BN + c));
+            if (i == 0) {
                 s = x;
             } else {
                 s.x += x.x;
@@ -697,8 +705,11 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         const int rem = tiles_big % sms;
         a.dp_tiles = tiles_big - rem;
         a.sk_tiles = rem;
-        if (rem != 0 && static_cast<long long>(rem) * KT < 2LL * sms) {
-            a.dp_tiles = tiles_big;  // too few k slices to share out: whole tiles only
+        const long long share = static_cast<long long>(rem) * KT / sms;  // k slices per CTA
+        // too few k slices to share out (or too many CTAs per tile for the
+        // fixup's owner list): whole tiles only
+        if (rem != 0 && (share < 2 || KT / share + 2 > 64)) {
+            a.dp_tiles = tiles_big;
             a.sk_tiles = 0;
         }
         a.grid_ctas = a.sk_tiles > 0 ? sms : std::min(sms, tiles_big);

@@ -68,7 +68,8 @@ def test_f16_ragged_shapes(M, N, K):
     assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 4096, 1024), (128, 1024, 4096), (384, 512, 640), (5, 64, 4096)])
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 1024), (128, 1024, 4096), (384, 512, 640), (5, 64, 4096),
+                                   (2048, 4096, 512), (2000, 4000, 1032)])
 def test_f16_small_integers_exact_paths(M, N, K):
     d = inputs.make(M, N, K, kind="f16", dist="smallint", seed=6, beta=2.0)
     got, plan = run_f16(d, 1.0, 2.0)
@@ -76,7 +77,7 @@ def test_f16_small_integers_exact_paths(M, N, K):
     np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (16, 1024, 2048)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (16, 1024, 2048), (2048, 4096, 1024)])
 @pytest.mark.parametrize("act", [0, 1])
 def test_f16_beta_and_bias_epilogue(M, N, K, act):
     d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=7, beta=-0.5, bias=True)
