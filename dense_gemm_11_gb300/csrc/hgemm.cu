@@ -505,6 +505,249 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+// Same roles as hgemm_tc_kernel, on a cluster of two CTAs on neighbouring
+// SMs that compute one 256 x BN tile together with tcgen05.mma.cta_group::2:
+// CTA r stages A rows [m0 + 128r, +128) and B columns [n0 + r*BN/2, +BN/2)
+// in its own shared memory; the even CTA's MMA thread multiplies the pair
+// (each SM's tensor core reads its own A rows and both halves of B) and the
+// accumulator rows land in each CTA's own tensor memory.  Per SM this moves
+// half the B bytes of the single-CTA 128 x BN tile for the same MMA work.
+// Barriers: each CTA's TMA loads count on the even CTA's "full" barrier;
+// the MMA thread's commits arrive on both CTAs' "empty" and "accumulator
+// full" barriers (multicast); both CTAs' epilogue warps arrive on the even
+// CTA's "accumulator empty" barrier.
+template <int BN, int STAGES>
+struct HgemmPairCfg {
+    static constexpr int kABytes = kBM * kBK * 2;  // this CTA's 128 rows
+    static constexpr int kBHalf = BN / 2;          // this CTA's columns of B
+    static constexpr int kBBoxes = (kBHalf + 63) / 64;
+    static constexpr int kBBytes = kBBoxes * 64 * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kCStageBytes = kEpiWarps * 32 * 32 * 4;
+    static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
+    static constexpr int kTmemCols = tmem_cols_for(BN);
+    static_assert(BN % 32 == 0 && BN <= 256 && kBHalf % 16 == 0, "pair MMA N");
+    static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
+};
+
+// Pair tile t -> (first row of the pair, first column), grouped raster of 4
+// pair rows per sweep over N.
+__device__ __forceinline__ void pair_tile_origin(const HgemmArgs &p, int t, int bn, int &m0, int &n0) {
+    const int group_tiles = 4 * p.tiles_n;
+    const int first_m = (t / group_tiles) * 4;
+    const int gsz = min(p.tiles_m - first_m, 4);
+    m0 = (first_m + (t % group_tiles) % gsz) * (2 * kBM);
+    n0 = ((t % group_tiles) / gsz) * bn;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    hgemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                         const __grid_constant__ CUtensorMap tm_c, const HgemmArgs p) {
+    using Cfg = HgemmPairCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * Cfg::kABytes;
+    uint8_t *sC = sB + STAGES * Cfg::kBBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + Cfg::kCStageBytes);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = bars + 2 * STAGES + 2;
+    uint64_t *mma_done = bars + 2 * STAGES + 4;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cid = blockIdx.x >> 1;
+    const int ncl = gridDim.x >> 1;
+    constexpr uint32_t kIdesc = umma_idesc_f16_f32(2 * kBM, BN, 0, 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 2 * kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_c);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, Cfg::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    uint32_t armed = 0, armed_parity = 0;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int t = cid; t < p.units && !*abort_flag; t += ncl) {
+            int m0, n0;
+            pair_tile_origin(p, t, BN, m0, n0);
+            const int my_m = m0 + static_cast<int>(rank) * kBM;
+            const int my_n = n0 + static_cast<int>(rank) * Cfg::kBHalf;
+            bool ok = true;
+            for (int kb = 0; kb < p.kb_total; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+                    flag_timeout(abort_flag, p.err);
+                    ok = false;
+                    break;
+                }
+                if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
+                const uint32_t full_even = mapa_shared(smem_u32(&full[stage]), 0);
+                const int k0 = kb * kBK;
+                tma_load_2d_pair(&tm_a, full_even, sA + stage * Cfg::kABytes, k0, my_m);
+#pragma unroll
+                for (int j = 0; j < Cfg::kBBoxes; ++j)
+                    tma_load_2d_pair(&tm_b, full_even, sB + stage * Cfg::kBBytes + j * 8192, my_n + 64 * j, k0);
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        for (int t = cid; t < p.units && !*abort_flag; t += ncl, ++local) {
+            const int buf = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(&tempty[buf], acc_phase ^ 1u)) {
+                flag_timeout(abort_flag, p.err);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+            bool ok = true;
+            for (int kb = 0; kb < p.kb_total; ++kb) {
+                if (!mbar_wait(&full[stage], phase)) {
+                    flag_timeout(abort_flag, p.err);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + stage * Cfg::kABytes);
+                const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+                    umma_f16_pair(d_tmem, umma_desc_sw128(a_addr + kk * 32, 16, 1024),
+                                  umma_desc_sw128(b_addr + kk * 2048, 8192, 1024), kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                umma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit_pair_mc(&tfull[buf], 0x3);  // both halves of the accumulator complete
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue warps (both CTAs)
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        float *stage_c = reinterpret_cast<float *>(sC + (warp - 2) * 4096);
+        int local = 0;
+        for (int t = cid; t < p.units && !*abort_flag; t += ncl, ++local) {
+            int m0, n0;
+            pair_tile_origin(p, t, BN, m0, n0);
+            const int my_m = m0 + static_cast<int>(rank) * kBM;
+            const int buf = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(&tfull[buf], acc_phase)) {
+                flag_timeout(abort_flag, p.err);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+            const int grow = my_m + row_in_tile;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + ch * 32, r);
+                tmem_wait_ld();
+                const int col0 = n0 + ch * 32;
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int gc = col0 + j;
+                    const bool in = gc < p.N;
+                    const float b = (p.bias && in) ? __ldg(p.bias + gc) : 0.f;
+                    const float cold =
+                        (p.beta != 0.f && in && grow < p.M) ? p.C[static_cast<size_t>(grow) * p.N + gc] : 0.f;
+                    v[j] = epi_value(__uint_as_float(r[j]), p, cold, b);
+                }
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    *reinterpret_cast<float4 *>(stage_c + lane * 32 + ((c4 ^ (lane & 7)) << 2)) =
+                        make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && my_m + q * 32 < p.M && col0 < p.N) {
+                    tma_store_2d(&tm_c, stage_c, col0, my_m + q * 32);
+                    bulk_commit();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(&tempty[buf]);
+                else
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------- drain and unwind
+    if (warp == 0 && lane == 0 && leader) {
+        // the even CTA's full barriers count the copies of both CTAs
+        for (int s = 0; s < STAGES; ++s)
+            if (armed & (1u << s))
+                if (!mbar_wait(&full[s], (armed_parity >> s) & 1u)) flag_timeout(abort_flag, p.err);
+    }
+    if (warp == 1 && lane == 0 && leader) {
+        umma_commit_pair_mc(mma_done, 0x1);
+        if (!mbar_wait(mma_done, 0)) flag_timeout(abort_flag, p.err);
+    }
+    tc_fence_before();
+    cluster_sync();  // neither CTA leaves while the pair's MMAs or copies may touch it
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -542,6 +785,41 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, tc, a);
+    return cudaPeekAtLastError();
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const HgemmArgs &a,
+                              cudaStream_t stream, int *clusters_used) {
+    using Cfg = HgemmPairCfg<BN, STAGES>;
+    auto kern = hgemm_tc_pair_kernel<BN, STAGES>;
+    static int max_clusters = -1;  // per instantiation; one device type per process
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters < 0) {
+        cfg.gridDim = dim3(2 * device_sm_count(), 1, 1);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        max_clusters = n;
+    }
+    if (max_clusters < 1) return cudaErrorNotSupported;
+    const int clusters = std::min(a.units, max_clusters);
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    *clusters_used = clusters;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, a);
+    if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
 
@@ -596,6 +874,50 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
             a.streamk = 1;
             a.dp_tiles = tiles - rem;
             a.sk_tiles = rem;
+        }
+    }
+    // CTA pairs: M > 128 with enough 256-row pair tiles for the SMs.  The
+    // tile width is picked from {256, 224, 192} by waves x time per tile,
+    // time per tile ~ (BN + 64): 4096 columns split 19 x 224 give exactly
+    // four pair tiles per SM pair on 152 SMs where 256 gives 3.4.
+    if (!swap && M > kBM && sms >= 2) {
+        const int pairs = sms / 2;
+        const int rows2 = (M + 2 * kBM - 1) / (2 * kBM);
+        int best_bn = 0;
+        double best_cost = 0.0;
+        for (int cand : {256, 224, 192}) {
+            const int t2 = rows2 * ((N + cand - 1) / cand);
+            const double cost = static_cast<double>((t2 + pairs - 1) / pairs) * (cand + 64);
+            if (best_bn == 0 || cost < best_cost - 1e-9) {
+                best_bn = cand;
+                best_cost = cost;
+            }
+        }
+        const int t2 = rows2 * ((N + best_bn - 1) / best_bn);
+        if (t2 * 2 >= pairs) {
+            a.tiles_m = rows2;
+            a.tiles_n = (N + best_bn - 1) / best_bn;
+            a.splits = 1;
+            a.units = t2;
+            CUtensorMap ta, tb, tc;
+            if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, kBM) ||
+                !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK) ||
+                !encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32))
+                return cudaErrorNotSupported;
+            int used = 0;
+            cudaError_t e;
+            if (best_bn == 256) {
+                e = launch_hgemm_pair<256, 6>(ta, tb, tc, a, stream, &used);
+                info->plan = "tc_pair_256x256";
+            } else if (best_bn == 224) {
+                e = launch_hgemm_pair<224, 6>(ta, tb, tc, a, stream, &used);
+                info->plan = "tc_pair_256x224";
+            } else {
+                e = launch_hgemm_pair<192, 6>(ta, tb, tc, a, stream, &used);
+                info->plan = "tc_pair_256x192";
+            }
+            info->launches = 1;
+            return e;
         }
     }
     if (splits > 1) {

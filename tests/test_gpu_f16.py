@@ -86,6 +86,15 @@ def test_f16_beta_and_bias_epilogue(M, N, K, act):
     assert_within(got, ref, S, TOL_F16, f"beta/bias act={act} [{plan}]")
 
 
+@pytest.mark.parametrize("M,N,K", [(129, 9728, 128), (300, 8448, 200), (1000, 4000, 520), (4100, 4104, 64)])
+def test_f16_cta_pair_ragged(M, N, K):
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=M + N + K, beta=0.25, bias=True)
+    got, plan = run_f16(d, -0.75, 0.25, d["bias"], 1)
+    assert "pair" in plan
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=-0.75, beta=0.25, bias=d["bias"], act=1)
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+
+
 def test_f16_beta_zero_does_not_read_c():
     d = inputs.make(300, 264, 128, kind="f16", dist="normal_k", seed=8, beta=0.0)
     got, plan = run_f16(d, 1.0, 0.0)
