@@ -46,7 +46,7 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -61,7 +61,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
@@ -104,8 +104,9 @@ def cpu_oracle_sample(target_s: float = 12.0):
     threads = oracle.default_threads()
     w32, w16 = inputs.WORKLOADS["f32_sq4096"], inputs.WORKLOADS["f16_4096"]
     d32, d16 = inputs.make_workload(w32), inputs.make_workload(w16)
-    # calibrate on a few rows, then size the sample
-    rows = np.arange(threads, dtype=np.int64)
+    # calibrate on a warm sample of rows, then size the sample to the target time
+    rows = np.arange(4 * threads, dtype=np.int64)
+    oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows[:threads], threads=threads)
     t0 = time.perf_counter()
     oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows, threads=threads)
     per_row = (time.perf_counter() - t0) / len(rows)
@@ -203,24 +204,24 @@ def run_ours(args, rank, world, local_rank):
         gemm16()
         ev[3].record(stream)
 
-    for _ in range(args.warmup):
-        step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
-    torch.cuda.synchronize(dev)
-    assert g.check(stream) == g.GEMM_OK
-
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    launches[0] = 0
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
+    # Clocks are sampled from the warm-up through the end of the timed region.
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for _ in range(args.warmup):
+            step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+        torch.cuda.synchronize(dev)
+        assert g.check(stream) == g.GEMM_OK
+        launches[0] = 0
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         t_wall0 = time.perf_counter()
         for s in range(args.steps):
             step(events[s])
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
-    if dist:
-        dist.barrier()
+        if dist:
+            dist.barrier()
     st = g.check(stream)
     if st != g.GEMM_OK:
         raise RuntimeError(f"watchdog: {g.status_string(st)}")
@@ -370,7 +371,7 @@ def run_profile_case(case: str, repeats: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
