@@ -368,6 +368,104 @@ def run_profile_case(case: str, repeats: int):
     print(f"{case}: {repeats} launches of plan {g.last_plan()}")
 
 
+def run_sweep(reps: int):
+    """Time every named workload (one JSON line each).
+
+    Two figures per workload: `ms` is the median of single calls, each after
+    a C reset and an L2 flush (cold L2, GPU briefly idle before the call);
+    `ms_steady` is the mean over back-to-back calls that cycle through enough
+    copies of A, B and C (> 2x L2) that no call finds its inputs in L2 --
+    the steady-state throughput of a stream of such GEMMs.  `frac` uses the
+    steady figure against min(compute peak, HBM bandwidth x intensity)."""
+    import torch
+
+    import dense_gemm_11_gb300 as g
+    from dense_gemm_11_gb300 import inputs, roofline
+    dev = torch.device("cuda", 0)
+    hbm_gbs, tc_peak, _, _ = _peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    f32_peak = roofline.fp32_fma_peak_tflops(sms, 2070.0)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2_bytes = 129 * 1024 * 1024
+    for name, w in inputs.WORKLOADS.items():
+        d = inputs.make_workload(w)
+        set_bytes = sum(d[k].nbytes for k in ("A", "B", "C"))
+        nbuf = max(1, min(16, -(-3 * l2_bytes // set_bytes)))
+        sets = []
+        for _ in range(nbuf):
+            sets.append({k: torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")})
+        C0 = sets[0]["C"].clone()
+        bias = torch.from_numpy(d["bias"]).to(dev) if "bias" in d else None
+
+        def call(t, st=None):
+            st = torch.cuda.current_stream(dev) if st is None else st
+            if w.kind == "f32":
+                g.gemm_f32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
+            else:
+                g.gemm_f16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
+                                           act=w.act, stream=st)
+
+        times = []
+        for r in range(reps + 3):
+            sets[0]["C"].copy_(C0)
+            flush.fill_(float(r))
+            torch.cuda._sleep(2_000_000)  # GPU busy while the host enqueues the call
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(sets[0])
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if r >= 3:
+                times.append(e0.elapsed_time(e1))
+        plan = g.last_plan()
+        # steady state: back-to-back calls over rotating input sets (C is
+        # overwritten with beta = 0 or keeps growing with beta != 0: same work),
+        # captured in a CUDA graph so that host-side argument handling is not
+        # between the kernels
+        n_steady = max(2 * nbuf, 20)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for i in range(nbuf):
+                call(sets[i])  # split-K scratch is per stream: allocate it outside the capture
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(n_steady):
+                t = sets[i % nbuf]
+                if w.kind == "f32":
+                    g.gemm_f32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=cap)
+                else:
+                    g.gemm_f16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
+                                               act=w.act, stream=cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        assert g.check(stream) == g.GEMM_OK
+        ms_steady = e0.elapsed_time(e1) / n_steady
+        del graph
+        ms = statistics.median(times)
+        flops = roofline.gemm_flops(w.M, w.N, w.K)
+        nbytes = roofline.gemm_bytes(w.M, w.N, w.K, in_bytes=4 if w.kind == "f32" else 2,
+                                     beta_nonzero=w.beta != 0.0, bias=w.bias)
+        peak = f32_peak if w.kind == "f32" else tc_peak
+        roof, bound = roofline.roofline_tflops(flops, nbytes, peak, hbm_gbs)
+        tflops = flops / (ms_steady * 1e-3) / 1e12
+        print(json.dumps({"workload": name, "M": w.M, "N": w.N, "K": w.K, "plan": plan, "ms": ms,
+                          "ms_steady": ms_steady, "input_sets": nbuf, "tflops": tflops,
+                          "gbs": nbytes / (ms_steady * 1e-3) / 1e9, "bound": bound, "roofline_tflops": roof,
+                          "frac": tflops / roof,
+                          "peak_note": "fp32 FFMA at 2070 MHz" if w.kind == "f32" else "measured bf16 burst"}),
+              flush=True)
+        del sets
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -378,7 +476,11 @@ def main():
     ap.add_argument("--profile-case", choices=["sgemm", "hgemm"], default=None,
                     help="launch one 4096^3 GEMM of the workload a few times (for ncu) and exit")
     ap.add_argument("--repeats", type=int, default=2)
+    ap.add_argument("--sweep", action="store_true", help="time every named workload, one JSON line each")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(max(3, args.steps // 10))
+        return
     if args.profile_case:
         run_profile_case(args.profile_case, args.repeats)
         return

@@ -67,6 +67,8 @@ int fail_cuda(cudaError_t e) {
 
 }  // namespace
 
+int current_device_id() { return current_device(); }
+
 int device_sm_count() {
     DeviceState *s = device_state();
     return (s && s->sm_count > 0) ? s->sm_count : 1;

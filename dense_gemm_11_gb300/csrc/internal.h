@@ -23,6 +23,21 @@ cudaError_t acquire_scratch(cudaStream_t stream, size_t partial_floats, size_t n
 unsigned *watchdog_word();
 
 int device_sm_count();  // multiprocessors of the current device
+int current_device_id();  // -1 if none
+
+// Opt `kern` in to `bytes` of dynamic shared memory on the current device,
+// once per (kernel, device): `done_mask` is a static owned by the caller's
+// launcher instantiation (one per kernel), bit d set once device d is done.
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(Kernel kern, int bytes, unsigned long long &done_mask) {
+    const int d = current_device_id();
+    if (d < 0) return cudaErrorInvalidDevice;
+    const unsigned long long bit = d < 64 ? (1ull << d) : 0ull;
+    if (bit && (__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) __atomic_fetch_or(&done_mask, bit, __ATOMIC_RELEASE);
+    return e;
+}
 
 struct CallInfo {
     const char *plan = "none";

@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(256) sgemv_rows_kernel(int M, int K, float alp
         const int K4 = K >> 2;
         const float4 *a4 = reinterpret_cast<const float4 *>(a);
         const float4 *x4 = reinterpret_cast<const float4 *>(x);
-#pragma unroll 8
+#pragma unroll 16
         for (int c = lane; c < K4; c += 32) {
             const float4 av = __ldcs(a4 + c);
             const float4 xv = __ldg(x4 + c);
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(256) sgemv_cols_kernel(int N, int K, float alp
     const int k1 = static_cast<int>(static_cast<long long>(K) * (chunk + 1) / splits);
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (vec && col + 3 < N) {
-#pragma unroll 8
+#pragma unroll 16
         for (int k = k0 + warp; k < k1; k += 8) {
             const float xv = __ldg(x + k);
             const float4 bv = __ldcs(reinterpret_cast<const float4 *>(B + static_cast<size_t>(k) * ldb + col));
@@ -617,7 +617,8 @@ template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, 
 cudaError_t launch_tiled(const SgemmArgs &a, cudaStream_t stream) {
     using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
     auto kern = sgemm_tiled_kernel<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC, PERSIST>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+    static unsigned long long smem_set = 0;
+    cudaError_t e = ensure_dynamic_smem(kern, T::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     dim3 grid = PERSIST ? dim3(a.grid_ctas, 1) : dim3(a.tiles_m * a.tiles_n, a.splits);
     kern<<<grid, T::kThreads, T::kSmemBytes, stream>>>(a);
@@ -692,8 +693,7 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
     // Tile table.  128x256 CTAs (8 warps, one per SM) run persistently when
     // there is enough work for every SM: whole tiles round-robin, and the
     // tiles of the last partial wave shared out by k slices (stream-K), so
-    // every SM gets the same number of k slices.  Smaller problems use
-    // 128x128 CTAs (4 warps, two per SM) with K split across CTAs.
+    // every SM gets the same number of k slices.
     const int tiles_big = ((M + 127) / 128) * ((N + 255) / 256);
     const bool big = tiles_big >= sms || static_cast<long long>(tiles_big) * KT >= 4LL * sms;
     cudaError_t e;
@@ -733,26 +733,29 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         else
             info->plan = vec ? "sgemm_128x256_vec16" : "sgemm_128x256_vec4b";
     } else {
-        a.tiles_m = (M + 127) / 128;
-        a.tiles_n = (N + 127) / 128;
+        // Small problems: 64x64 CTAs (4 warps of 32x32, 4x8 per thread), several
+        // per SM, with K split so that there are about four CTAs per SM, each
+        // split at least two 32-wide k slices.
+        a.tiles_m = (M + 63) / 64;
+        a.tiles_n = (N + 63) / 64;
         const int tiles = a.tiles_m * a.tiles_n;
         int splits = 1;
-        if (tiles < 2 * sms) splits = std::max(1, std::min(2 * sms / tiles, KT / 4));
+        if (tiles < 4 * sms) splits = std::max(1, std::min((4 * sms + tiles - 1) / tiles, KT / 2));
         splits = std::min(splits, 16);
         a.splits = splits;
         if (splits > 1) {
             Scratch sc;
-            e = acquire_scratch(stream, static_cast<size_t>(tiles) * splits * 128 * 128, tiles, &sc);
+            e = acquire_scratch(stream, static_cast<size_t>(tiles) * splits * 64 * 64, tiles, &sc);
             if (e != cudaSuccess) return e;
             a.ws = sc.partials;
             a.counters = sc.counters;
         }
-        e = vec ? launch_tiled<128, 128, 2, 2, 8, 16, 3, true, false>(a, stream)
-                : launch_tiled<128, 128, 2, 2, 8, 16, 3, false, false>(a, stream);
+        e = vec ? launch_tiled<64, 64, 2, 2, 4, 8, 3, true, false>(a, stream)
+                : launch_tiled<64, 64, 2, 2, 4, 8, 3, false, false>(a, stream);
         if (splits > 1)
-            info->plan = vec ? "sgemm_128x128_vec16_splitk" : "sgemm_128x128_vec4b_splitk";
+            info->plan = vec ? "sgemm_64x64_vec16_splitk" : "sgemm_64x64_vec4b_splitk";
         else
-            info->plan = vec ? "sgemm_128x128_vec16" : "sgemm_128x128_vec4b";
+            info->plan = vec ? "sgemm_64x64_vec16" : "sgemm_64x64_vec4b";
         info->launches = 1;
     }
     return e;
