@@ -95,6 +95,20 @@ class ClockSampler:
                 "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise max of per-rank timings (every rank gets the result)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def replica_throughput(flops_per_rank_step: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job TFLOP/s of `world` independent replicas timed by the slowest rank."""
+    return world * flops_per_rank_step / (ms_per_step_max * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(target_s: float = 12.0):
     """Time the oracle (as it stands) on rows of both 4096^3 GEMMs; about target_s seconds."""
     import numpy as np
@@ -265,10 +279,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / n_e2e
 
     # max over ranks
-    times = torch.tensor([ms_step, e2e_ms, statistics.mean(t32), statistics.mean(t16)], device=dev)
-    if dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_step, e2e_ms, ms32, ms16 = (float(x) for x in times.tolist())
+    ms_step, e2e_ms, ms32, ms16 = max_over_ranks(
+        [ms_step, e2e_ms, statistics.mean(t32), statistics.mean(t16)], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -280,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
     ach32 = FLOPS_ONE / (ms32 * 1e-3) / 1e12
     ach16 = FLOPS_ONE / (ms16 * 1e-3) / 1e12
     traffic = _traffic_from_profiles()
-    value = world * FLOPS_STEP / (ms_step * 1e-3) / 1e12
+    value = replica_throughput(FLOPS_STEP, world, ms_step)
     line = {
         "metric": METRIC,
         "value": value,
@@ -311,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
                             "frac": ach16 / tc_peak, "traffic": traffic.get("hgemm"),
                             "kernel": "hgemm_tc_kernel (tcgen05 f16)",
                             "peak_source": f"{peak_src} bf16 burst (fp16 runs at the bf16 rate)"},
-        "e2e": {"value": world * FLOPS_STEP / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+        "e2e": {"value": replica_throughput(FLOPS_STEP, world, e2e_ms), "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": gpu_launches,
         "clocks": clocks,

@@ -30,8 +30,8 @@ GEMM_ACT_NONE = 0
 GEMM_ACT_GELU = 1
 
 EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_f16_f32acc_epilogue_noalloc",
-                    "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_last_plan",
-                    "gemm_last_launch_count")
+                    "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
+                    "gemm_last_plan", "gemm_last_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +69,8 @@ def lib():
             L.gemm_last_cuda_error.argtypes = []
             L.gemm_check.restype = c_int
             L.gemm_check.argtypes = [c_void_p]
+            L.gemm_watchdog_selftest.restype = c_int
+            L.gemm_watchdog_selftest.argtypes = [c_int, c_void_p]
             L.gemm_last_plan.restype = ctypes.c_char_p
             L.gemm_last_plan.argtypes = []
             L.gemm_last_launch_count.restype = c_int
@@ -175,6 +177,11 @@ def gemm_f16_f32acc_epilogue(A, B, C, alpha: float = 1.0, beta: float = 0.0, bia
                                         ctypes.c_void_p(bias_ptr), int(act), _stream_handle(stream))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16_f32acc_epilogue")
+
+
+def watchdog_selftest(wait_ms: int = 20, stream=None) -> int:
+    """Enqueue the watchdog probe (a wait that must time out after wait_ms); returns the status."""
+    return int(lib().gemm_watchdog_selftest(int(wait_ms), _stream_handle(stream)))
 
 
 def check(stream=None) -> int:

@@ -19,6 +19,17 @@ __device__ unsigned g_watchdog_word;
 
 namespace {
 
+// One thread waits on an mbarrier that nothing ever arrives on, with the
+// same bounded wait the GEMM pipelines use; when it gives up it records the
+// timeout in the watchdog word exactly as they do.
+__global__ void watchdog_probe_kernel(unsigned *err, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    if (!mbar_wait(&bar, 0, limit_ns)) atomicOr(err, kWatchdogTimeout);
+}
+
 thread_local int t_last_cuda_error = 0;
 thread_local const char *t_last_plan = "none";
 thread_local int t_last_launches = 0;
@@ -262,6 +273,20 @@ int gemm_check(void *stream) {
         if (e != cudaSuccess) return fail_cuda(e);
         return GEMM_ERR_TIMEOUT;
     }
+    return GEMM_OK;
+}
+
+int gemm_watchdog_selftest(int wait_ms, void *stream) {
+    if (wait_ms < 1 || wait_ms > 2000) return GEMM_ERR_INVALID_ARG;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    watchdog_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        ds->watchdog, static_cast<unsigned long long>(wait_ms) * 1000000ull);
+    const cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_plan = "watchdog_probe";
+    t_last_launches = 1;
     return GEMM_OK;
 }
 

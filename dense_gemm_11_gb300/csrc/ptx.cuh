@@ -72,14 +72,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
     return ok != 0;
 }
 // Wait until the phase with the given parity has completed.  Bounded: gives
-// up after kWaitLimitNs and returns false (the caller records the timeout).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// up after limit_ns and returns false (the caller records the timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 255u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 255u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

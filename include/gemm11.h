@@ -145,6 +145,18 @@ GEMM11_API int gemm_last_cuda_error(void);
 GEMM11_API int gemm_check(void *stream);
 
 /*
+ * gemm_watchdog_selftest -- diagnostic: enqueue on `stream` a one-thread
+ * kernel whose bounded wait (the same wait every GEMM pipeline uses) can
+ * never be satisfied, with a limit of wait_ms milliseconds (1..2000).  The
+ * kernel returns normally after the limit and records the timeout in the
+ * device watchdog word, so the next gemm_check(stream) returns
+ * GEMM_ERR_TIMEOUT (and clears it).  This exercises the timeout path without
+ * faulting, trapping or hanging the GPU; the context stays usable.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG or GEMM_ERR_CUDA.
+ */
+GEMM11_API int gemm_watchdog_selftest(int wait_ms, void *stream);
+
+/*
  * Introspection for tests and benchmarks: the name of the kernel plan the
  * calling thread's last successful call used (static storage), and how many
  * kernels that call launched.

@@ -87,3 +87,8 @@ def test_status_strings(L):
     for st in (g.GEMM_OK, g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_UNSUPPORTED, g.GEMM_ERR_CUDA, g.GEMM_ERR_TIMEOUT):
         assert g.status_string(st).startswith("GEMM_")
     assert "unknown" in g.status_string(12345)
+
+
+def test_watchdog_selftest_rejects_bad_limits_on_host(L):
+    assert L.gemm_watchdog_selftest(0, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.gemm_watchdog_selftest(2001, None) == g.GEMM_ERR_INVALID_ARG
