@@ -74,7 +74,7 @@ struct HgemmCfg {
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows of 128 B
     static constexpr int kBBytes = BN * kBK * 2;   // BN rows (or k-rows) of 128 B
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kCStageBytes = SWAP ? 0 : kEpiWarps * 32 * 32 * 4;
+    static constexpr int kCStageBytes = SWAP ? 0 : kEpiWarps * 2 * 32 * 32 * 4;  // 2 x 4 KB per warp
     static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
     static constexpr int kTmemCols = tmem_cols_for(BN);
@@ -159,6 +159,54 @@ __device__ __forceinline__ void flag_timeout(volatile int *abort_flag, unsigned 
 }
 
 // Epilogue value for one element.
+// Epilogue of one row chunk: v[j] holds the accumulator of C[grow][col0 + j],
+// j < 32.  Each optional term is one uniform pass over the chunk (the flags
+// are kernel arguments), so the common alpha-only case is 32 multiplies:
+// v = act(alpha * acc + beta * C + bias).  N % 8 == 0 and 16-byte aligned
+// C rows let in-range groups of 4 columns use 128-bit loads (bias too when
+// it is 16-byte aligned).
+__device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmArgs &p, int grow, int col0) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+    if (p.beta != 0.f && grow < p.M) {
+        const float *crow = p.C + static_cast<size_t>(grow) * p.N;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int gc = col0 + 4 * q;
+            if (gc < p.N) {  // N % 8 == 0: the whole group of 4 is in range
+                const float4 c4 = *reinterpret_cast<const float4 *>(crow + gc);
+                v[4 * q] = fmaf(p.beta, c4.x, v[4 * q]);
+                v[4 * q + 1] = fmaf(p.beta, c4.y, v[4 * q + 1]);
+                v[4 * q + 2] = fmaf(p.beta, c4.z, v[4 * q + 2]);
+                v[4 * q + 3] = fmaf(p.beta, c4.w, v[4 * q + 3]);
+            }
+        }
+    }
+    if (p.bias) {
+        if ((reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int gc = col0 + 4 * q;
+                if (gc < p.N) {
+                    const float4 b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + gc));
+                    v[4 * q] += b4.x;
+                    v[4 * q + 1] += b4.y;
+                    v[4 * q + 2] += b4.z;
+                    v[4 * q + 3] += b4.w;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
+        }
+    }
+    if (p.act == 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
+    }
+}
+
 __device__ __forceinline__ float epi_value(float acc, const HgemmArgs &p, float cold, float b) {
     float v = p.alpha * acc;
     if (p.beta != 0.f) v = fmaf(p.beta, cold, v);
@@ -305,7 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue warps
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
-        float *stage_c = reinterpret_cast<float *>(sC + (warp - 2) * 4096);
+        // Two 4 KB staging buffers per warp used alternately (running chunk
+        // count), so a chunk's shared-memory writes only wait for the TMA
+        // store issued two chunks earlier.
+        float *const stage_base = reinterpret_cast<float *>(sC + (warp - 2) * 8192);
+        uint32_t n_staged = 0;
         int local = 0;
         for (int idx = 0; !*abort_flag; ++idx, ++local) {
             UnitCoord c;
@@ -345,17 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (!SWAP) {
                     const int grow = c.m0 + row_in_tile;
                     const int col0 = c.n0 + ch * 32;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int gc = col0 + j;
-                        const bool in = gc < p.N;
-                        const float b = (p.bias && in) ? __ldg(p.bias + gc) : 0.f;
-                        const float cold =
-                            (p.beta != 0.f && in && grow < p.M) ? p.C[static_cast<size_t>(grow) * p.N + gc] : 0.f;
-                        v[j] = epi_value(v[j], p, cold, b);
-                    }
+                    epilogue_row_chunk(v, p, grow, col0);
                     // stage the 32x32 block (128-byte swizzle) and TMA-store it
-                    if (lane == 0) bulk_wait_read_all();
+                    float *stage_c = stage_base + (n_staged & 1u) * 1024;
+                    ++n_staged;
+                    if (lane == 0) bulk_wait_read_all_but_one();
                     __syncwarp();
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4)
@@ -363,9 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0 && c.m0 + q * 32 < p.M && col0 < p.N) {
-                        tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
-                        bulk_commit();
+                    if (lane == 0) {
+                        if (c.m0 + q * 32 < p.M && col0 < p.N) tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
+                        bulk_commit();  // one group per chunk, possibly empty
                     }
                 } else {
                     // transposed: this thread owns column n of C, registers walk rows m
@@ -466,17 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (!SWAP) {
                             const int grow = c.m0 + row_in_tile;
                             const int col0 = c.n0 + ch * 32;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int gc = col0 + j;
-                                const bool in = gc < p.N;
-                                const float b = (p.bias && in) ? __ldg(p.bias + gc) : 0.f;
-                                const float cold = (p.beta != 0.f && in && grow < p.M)
-                                                       ? p.C[static_cast<size_t>(grow) * p.N + gc]
-                                                       : 0.f;
-                                v[j] = epi_value(v[j], p, cold, b);
-                            }
-                            if (lane == 0) bulk_wait_read_all();
+                            epilogue_row_chunk(v, p, grow, col0);
+                            float *stage_c = stage_base + (n_staged & 1u) * 1024;
+                            ++n_staged;
+                            if (lane == 0) bulk_wait_read_all_but_one();
                             __syncwarp();
 #pragma unroll
                             for (int c4 = 0; c4 < 8; ++c4)
@@ -484,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
                             fence_proxy_async_smem();
                             __syncwarp();
-                            if (lane == 0 && c.m0 + q * 32 < p.M && col0 < p.N) {
-                                tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
-                                bulk_commit();
+                            if (lane == 0) {
+                                if (c.m0 + q * 32 < p.M && col0 < p.N) tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
+                                bulk_commit();  // one group per chunk, possibly empty
                             }
                         } else {
                             const int gn = c.n0 + row_in_tile;
@@ -551,7 +590,7 @@ struct HgemmPairCfg {
     static constexpr int kBBoxes = (kBHalf + 63) / 64;
     static constexpr int kBBytes = kBBoxes * 64 * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kCStageBytes = kEpiWarps * 32 * 32 * 4;
+    static constexpr int kCStageBytes = kEpiWarps * 2 * 32 * 32 * 4;  // 2 x 4 KB per warp
     static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
     static constexpr int kTmemCols = tmem_cols_for(BN);
@@ -698,7 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue warps (both CTAs)
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
-        float *stage_c = reinterpret_cast<float *>(sC + (warp - 2) * 4096);
+        // Two 4 KB staging buffers per warp used alternately (running chunk
+        // count), so a chunk's shared-memory writes only wait for the TMA
+        // store issued two chunks earlier.
+        float *const stage_base = reinterpret_cast<float *>(sC + (warp - 2) * 8192);
+        uint32_t n_staged = 0;
         int local = 0;
         for (int t = cid; t < p.units && !*abort_flag; t += ncl, ++local) {
             int m0, n0;
@@ -721,15 +764,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col0 = n0 + ch * 32;
                 float v[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int gc = col0 + j;
-                    const bool in = gc < p.N;
-                    const float b = (p.bias && in) ? __ldg(p.bias + gc) : 0.f;
-                    const float cold =
-                        (p.beta != 0.f && in && grow < p.M) ? p.C[static_cast<size_t>(grow) * p.N + gc] : 0.f;
-                    v[j] = epi_value(__uint_as_float(r[j]), p, cold, b);
-                }
-                if (lane == 0) bulk_wait_read_all();
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                epilogue_row_chunk(v, p, grow, col0);
+                float *stage_c = stage_base + (n_staged & 1u) * 1024;
+                ++n_staged;
+                if (lane == 0) bulk_wait_read_all_but_one();
                 __syncwarp();
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4)
@@ -737,9 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && my_m + q * 32 < p.M && col0 < p.N) {
-                    tma_store_2d(&tm_c, stage_c, col0, my_m + q * 32);
-                    bulk_commit();
+                if (lane == 0) {
+                    if (my_m + q * 32 < p.M && col0 < p.N) tma_store_2d(&tm_c, stage_c, col0, my_m + q * 32);
+                    bulk_commit();  // one group per chunk, possibly empty
                 }
             }
             tc_fence_before();

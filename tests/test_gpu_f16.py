@@ -129,3 +129,19 @@ def test_f16_unsupported_is_reported():
     with pytest.raises(g.GemmError) as e:
         g.gemm_f16_f32acc_epilogue(A, B, C)
     assert e.value.status == g.GEMM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 520, 128), (2048, 4096, 256), (40, 264, 64)])
+def test_f16_unaligned_bias_pointer(M, N, K):
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=31, beta=0.0, bias=True)
+    A = torch.from_numpy(d["A"]).to(DEV)
+    B = torch.from_numpy(d["B"]).to(DEV)
+    C = torch.from_numpy(d["C"]).to(DEV)
+    buf = torch.zeros(N + 1, device=DEV)
+    buf[1:] = torch.from_numpy(d["bias"]).to(DEV)
+    bias = buf[1:]  # 4-byte aligned only
+    assert bias.data_ptr() % 16 != 0
+    g.gemm_f16_f32acc_epilogue(A, B, C, alpha=0.5, beta=0.0, bias=bias, act=1)
+    assert g.check() == g.GEMM_OK
+    ref, S = oracle.gemm(d["A"], d["B"], None, alpha=0.5, beta=0.0, bias=d["bias"], act=1)
+    assert_within(C.cpu().numpy(), ref, S, TOL_F16, f"unaligned bias [{g.last_plan()}]")
