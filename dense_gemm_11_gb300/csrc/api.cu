@@ -49,6 +49,8 @@ struct ScratchEntry {
     size_t partial_floats = 0;
     unsigned *counters = nullptr;
     size_t ncounters = 0;
+    float *operands = nullptr;
+    size_t operand_floats = 0;
 };
 std::mutex g_scratch_mu;
 std::map<std::pair<int, uintptr_t>, ScratchEntry> g_scratch;
@@ -122,6 +124,25 @@ cudaError_t acquire_scratch(cudaStream_t stream, size_t partial_floats, size_t n
     }
     out->partials = e.partials;
     out->counters = e.counters;
+    return cudaSuccess;
+}
+
+cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **out) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    ScratchEntry &e = g_scratch[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (e.operand_floats < floats) {
+        cudaError_t r = cudaStreamSynchronize(stream);  // queued work may still read the old buffer
+        if (r != cudaSuccess) return r;
+        if (e.operands) cudaFree(e.operands);
+        e.operands = nullptr;
+        e.operand_floats = 0;
+        r = cudaMalloc(&e.operands, floats * sizeof(float));
+        if (r != cudaSuccess) return r;
+        e.operand_floats = floats;
+    }
+    *out = e.operands;
     return cudaSuccess;
 }
 

@@ -19,6 +19,10 @@ struct Scratch {
 // `ncounters` zeroed counters usable on `stream` (current device).
 cudaError_t acquire_scratch(cudaStream_t stream, size_t partial_floats, size_t ncounters, Scratch *out);
 
+// A second per-(device, stream) buffer for repacked operands (used together
+// with the partials above), grown on demand.
+cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **out);
+
 // Device address of the current device's watchdog word.
 unsigned *watchdog_word();
 

@@ -68,7 +68,8 @@ def test_f32_irregular_full(i):
 
 def test_f32_irregular_4095_4097_4099_sampled():
     _, plan = check_workload("f32_irr1", rows=sample_rows(4095, seed=2))
-    assert "vec4b" in plan  # lda = 4099: rows are not 16-byte aligned
+    # lda = 4099: rows are not 16-byte aligned; large problems are repacked
+    assert "repack" in plan or "vec4b" in plan
 
 
 SHAPES = [1, 3, 17, 32, 64, 128, 129]
@@ -104,6 +105,15 @@ def test_f32_leading_dims_larger_than_width(lds):
     assert_within(got[:, :N], ref, S, TOL_F32, f"ld {lds} [{plan}]")
     # columns past N in C are untouched
     np.testing.assert_array_equal(got[:, N:], d["C"][:, N:])
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb", [(1300, 1500, 1100, 1101, 1500), (1024, 2050, 1031, 1031, 2053)])
+def test_f32_repacked_unaligned_large(M, N, K, lda, ldb):
+    d = inputs.make(M, N, K, kind="f32", dist="normal", seed=23, beta=0.25, lda=lda, ldb=ldb)
+    got, plan = run_f32(d, 1.0, 0.25, K=K, N=N)
+    assert "repack" in plan
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=0.25, K=K, N=N, rows=sample_rows(M, seed=3))
+    assert_within(got[sample_rows(M, seed=3)], ref, S, TOL_F32, f"repacked [{plan}]")
 
 
 @pytest.mark.parametrize("offset", [1, 2, 3])
