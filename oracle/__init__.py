@@ -61,6 +61,8 @@ def _load():
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_gelu_f64.restype = ctypes.c_double
             lib.oracle_gelu_f64.argtypes = [ctypes.c_double]
+            lib.oracle_act_f64.restype = ctypes.c_double
+            lib.oracle_act_f64.argtypes = [ctypes.c_int, ctypes.c_double]
             _lib = lib
     return _lib
 
@@ -127,3 +129,8 @@ def gemm(A, B, C0=None, *, alpha=1.0, beta=0.0, bias=None, act=0, rows=None,
 def gelu(x: float) -> float:
     """Exact-erf GELU in double (the oracle's activation)."""
     return float(_load().oracle_gelu_f64(float(x)))
+
+
+def act(kind: int, x: float) -> float:
+    """Activation `kind` (0 identity, 1 exact GELU, 2 ReLU, 3 tanh GELU) in double."""
+    return float(_load().oracle_act_f64(int(kind), float(x)))

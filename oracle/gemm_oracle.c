@@ -24,7 +24,12 @@
  *   - beta == 0: C0 is not read (a NaN in C0 does not propagate);
  *   - alpha == 0 or K == 0: A and B are not read; the product term is 0;
  *   - bias == NULL: no bias term;  act: 0 = identity, 1 = exact GELU,
- *     GELU(x) = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))).
+ *     GELU(x) = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))); 2 = ReLU,
+ *     max(x, 0); 3 = the tanh approximation of GELU (Hendrycks and Gimpel,
+ *     "Gaussian Error Linear Units"), 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *     The pages name "activation" and GELU in the epilogue without fixing a
+ *     form; the exact form is the default, the other two are the common
+ *     alternatives an inference epilogue offers.
  *
  * Arithmetic: every input arrives as double (fp32 and fp16 values are
  * exactly representable in double); the sum over k is taken in double with k
@@ -59,6 +64,18 @@ typedef struct {
 } oracle_job;
 
 static double gelu_exact(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+static double gelu_tanh(double x) {
+    const double pi = 3.14159265358979323846;
+    return 0.5 * x * (1.0 + tanh(sqrt(2.0 / pi) * (x + 0.044715 * x * x * x)));
+}
+static double apply_act(int act, double v) {
+    switch (act) {
+        case 1: return gelu_exact(v);
+        case 2: return v > 0.0 ? v : 0.0;
+        case 3: return gelu_tanh(v);
+        default: return v;
+    }
+}
 
 static void *oracle_rows(void *arg) {
     oracle_job *J = (oracle_job *)arg;
@@ -104,7 +121,7 @@ static void *oracle_rows(void *arg) {
                 v += J->bias[j];
                 sc += fabs(J->bias[j]);
             }
-            if (J->act == 1) v = gelu_exact(v);
+            v = apply_act(J->act, v);
             o[j] = v;
             if (s) s[j] = sc;
         }
@@ -126,7 +143,7 @@ int oracle_gemm_f64(long M, long N, long K, double alpha, const double *A, long 
                     const double *bias, int act, const long *rows, long nrows, double *out,
                     double *scale, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || nrows < 0 || !out) return -1;
-    if (act != 0 && act != 1) return -1;
+    if (act < 0 || act > 3) return -1;
     if (nrows == 0 || N == 0) return 0;
     if (alpha != 0.0 && K > 0 && (!A || !B || lda < K || ldb < N)) return -1;
     if (beta != 0.0 && (!C0 || ldc < N)) return -1;
@@ -170,5 +187,6 @@ int oracle_gemm_f64(long M, long N, long K, double alpha, const double *A, long 
     return status;
 }
 
-/* GELU alone, exposed so that its special values can be pinned directly. */
+/* The activations alone, exposed so that their special values can be pinned. */
 double oracle_gelu_f64(double x) { return gelu_exact(x); }
+double oracle_act_f64(int act, double x) { return apply_act(act, x); }

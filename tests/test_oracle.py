@@ -221,3 +221,24 @@ def test_rejects_bad_arguments():
         oracle.gemm(A, B, rows=[2])
     with pytest.raises(ValueError):
         oracle.gemm(A, B, act=5)
+
+
+def test_relu_and_tanh_gelu():
+    # ReLU
+    assert oracle.act(2, 3.5) == 3.5 and oracle.act(2, -2.0) == 0.0 and oracle.act(2, 0.0) == 0.0
+    # tanh-GELU: f(x) - f(-x) = x for any odd inner function (tanh is odd)
+    for x in (0.1, 0.5, 1.0, 2.0, 3.7):
+        assert abs((oracle.act(3, x) - oracle.act(3, -x)) - x) < 1e-15 * max(1.0, x)
+    assert oracle.act(3, 0.0) == 0.0
+    assert oracle.act(3, 20.0) == 20.0 and abs(oracle.act(3, -20.0)) < 1e-30
+    # it approximates the exact GELU to better than 1e-3 everywhere (x * Phi(x))
+    for x, phi in PHI.items():
+        assert abs(oracle.act(3, x) - x * phi) < 1e-3 * max(1.0, abs(x))
+        assert oracle.act(3, x) != oracle.act(1, x)  # and it is not the exact form
+    # identity / exact GELU dispatch
+    assert oracle.act(0, -1.25) == -1.25
+    assert oracle.act(1, 1.0) == oracle.gelu(1.0)
+    # act applies after bias inside the GEMM
+    out, _ = oracle.gemm(np.zeros((1, 2), np.float32), np.zeros((2, 3), np.float32),
+                         bias=np.array([-1.0, 0.0, 2.0], np.float32), act=2)
+    np.testing.assert_array_equal(out, [[0.0, 0.0, 2.0]])
