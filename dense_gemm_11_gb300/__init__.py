@@ -7,6 +7,7 @@ fallback: if the shared library is missing, every call raises.
     gemm_f32(A, B, C, alpha=1.0, beta=0.0)            C = alpha*A@B + beta*C (fp32)
     gemm_f16_f32acc_epilogue(A, B, C, alpha=1.0, beta=0.0, bias=None, act=0)
                                                       C = act(alpha*A@B + beta*C + bias)
+    gemm_bf16_f32acc_epilogue(...)                    the same with bf16 A and B
 
 Tensors are torch CUDA tensors on the current device; A and B may be 2-D
 views with a leading dimension larger than their width (unit column stride).
@@ -28,8 +29,11 @@ GEMM_ERR_TIMEOUT = -4
 GEMM_ERR_SCRATCH_LIMIT = -5
 GEMM_ACT_NONE = 0
 GEMM_ACT_GELU = 1
+GEMM_ACT_RELU = 2
+GEMM_ACT_GELU_TANH = 3
 
-EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_f16_f32acc_epilogue_noalloc",
+EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_bf16_f32acc_epilogue",
+                    "gemm_f16_f32acc_epilogue_noalloc",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count")
 
@@ -61,6 +65,8 @@ def lib():
             L.gemm_f16_f32acc_epilogue.restype = c_int
             L.gemm_f16_f32acc_epilogue.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_float,
                                                    c_void_p, c_void_p, c_int, c_void_p]
+            L.gemm_bf16_f32acc_epilogue.restype = c_int
+            L.gemm_bf16_f32acc_epilogue.argtypes = L.gemm_f16_f32acc_epilogue.argtypes
             L.gemm_f16_f32acc_epilogue_noalloc.restype = c_int
             L.gemm_f16_f32acc_epilogue_noalloc.argtypes = L.gemm_f16_f32acc_epilogue.argtypes
             L.gemm_status_string.restype = ctypes.c_char_p
@@ -125,6 +131,13 @@ def gemm_f16_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, s
                                           ctypes.c_void_p(bias_ptr or None), int(act), ctypes.c_void_p(stream_ptr))
 
 
+def gemm_bf16_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, stream_ptr=0) -> int:
+    """Direct C-ABI call of the BF16-input entry point; returns the status code."""
+    return lib().gemm_bf16_f32acc_epilogue(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr),
+                                           ctypes.c_void_p(B_ptr), float(beta), ctypes.c_void_p(C_ptr),
+                                           ctypes.c_void_p(bias_ptr or None), int(act), ctypes.c_void_p(stream_ptr))
+
+
 def gemm_f16_noalloc_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, stream_ptr=0) -> int:
     """C-ABI call of the no-allocation variant (M <= 64); returns the status code.
 
@@ -154,11 +167,9 @@ def gemm_f32(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, stream=None) -> 
         raise GemmError(st, "gemm_f32")
 
 
-def gemm_f16_f32acc_epilogue(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: int = 0, *,
-                             stream=None) -> None:
-    """C = act(alpha * A @ B + beta * C + bias): fp16 A, B; fp32 accumulate, bias and C."""
+def _gemm_16bit(fn_name, in_dtype, A, B, C, alpha, beta, bias, act, stream) -> None:
     import torch
-    for name, t, dt in (("A", A, torch.float16), ("B", B, torch.float16), ("C", C, torch.float32)):
+    for name, t, dt in (("A", A, in_dtype), ("B", B, in_dtype), ("C", C, torch.float32)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dt or t.dim() != 2:
             raise TypeError(f"{name} must be a 2-D CUDA {dt} tensor")
         if not t.is_contiguous():
@@ -172,11 +183,25 @@ def gemm_f16_f32acc_epilogue(A, B, C, alpha: float = 1.0, beta: float = 0.0, bia
         if not bias.is_cuda or bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous():
             raise TypeError("bias must be a contiguous CUDA float32 tensor of length N")
         bias_ptr = bias.data_ptr()
-    st = lib().gemm_f16_f32acc_epilogue(M, N, K, float(alpha), ctypes.c_void_p(A.data_ptr()),
-                                        ctypes.c_void_p(B.data_ptr()), float(beta), ctypes.c_void_p(C.data_ptr()),
-                                        ctypes.c_void_p(bias_ptr), int(act), _stream_handle(stream))
+    st = getattr(lib(), fn_name)(M, N, K, float(alpha), ctypes.c_void_p(A.data_ptr()),
+                                 ctypes.c_void_p(B.data_ptr()), float(beta), ctypes.c_void_p(C.data_ptr()),
+                                 ctypes.c_void_p(bias_ptr), int(act), _stream_handle(stream))
     if st != GEMM_OK:
-        raise GemmError(st, "gemm_f16_f32acc_epilogue")
+        raise GemmError(st, fn_name)
+
+
+def gemm_f16_f32acc_epilogue(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: int = 0, *,
+                             stream=None) -> None:
+    """C = act(alpha * A @ B + beta * C + bias): fp16 A, B; fp32 accumulate, bias and C."""
+    import torch
+    _gemm_16bit("gemm_f16_f32acc_epilogue", torch.float16, A, B, C, alpha, beta, bias, act, stream)
+
+
+def gemm_bf16_f32acc_epilogue(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: int = 0, *,
+                              stream=None) -> None:
+    """C = act(alpha * A @ B + beta * C + bias): bf16 A, B; fp32 accumulate, bias and C."""
+    import torch
+    _gemm_16bit("gemm_bf16_f32acc_epilogue", torch.bfloat16, A, B, C, alpha, beta, bias, act, stream)
 
 
 def watchdog_selftest(wait_ms: int = 20, stream=None) -> int:

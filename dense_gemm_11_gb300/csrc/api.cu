@@ -177,10 +177,18 @@ int gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const fl
     return GEMM_OK;
 }
 
-int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
-                             const float *bias, int act, void *stream) {
+}  // extern "C"
+
+namespace {
+
+bool valid_act(int act) { return act >= GEMM_ACT_NONE && act <= GEMM_ACT_GELU_TANH; }
+
+// The 16-bit-input entry points (FP16 or BF16 operands, FP32 accumulate and
+// output, fused epilogue) share validation and planning.
+int gemm_16bit_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
+                               const float *bias, int act, bool bf16, void *stream) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-    if (act != GEMM_ACT_NONE && act != GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
+    if (!valid_act(act)) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) {
         t_last_plan = "noop_empty";
         t_last_launches = 0;
@@ -205,7 +213,7 @@ int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, co
     if (!product) {
         e = run_scale_c(M, N, beta, C, N, bias, act, s, &info);
     } else {
-        e = run_gemm_f16(M, N, K, alpha, A, B, beta, C, bias, act, s, &info);
+        e = run_gemm_f16(M, N, K, alpha, A, B, beta, C, bias, act, bf16, s, &info);
         if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return fail_cuda(e);
@@ -214,10 +222,24 @@ int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, co
     return GEMM_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
+                             const float *bias, int act, void *stream) {
+    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, beta, C, bias, act, false, stream);
+}
+
+int gemm_bf16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta,
+                              float *C, const float *bias, int act, void *stream) {
+    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, beta, C, bias, act, true, stream);
+}
+
 int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const void *A, const void *B, float beta,
                                      float *C, const float *bias, int act, void *stream) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-    if (act != GEMM_ACT_NONE && act != GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
+    if (!valid_act(act)) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) {
         t_last_plan = "noop_empty";
         t_last_launches = 0;

@@ -59,6 +59,7 @@ struct HgemmArgs {
     float *ws;
     unsigned *counters;
     unsigned *err;
+    uint32_t idesc_fmt;  // operand-format bits OR'ed into the MMA instruction descriptor (BF16: A and B)
     // stream-K schedule (non-transposed, splits == 1): the first dp_tiles
     // tiles of the raster are whole units, the last sk_tiles are shared out
     // by k blocks over the grid; partial tiles go to 2 slots per CTA.
@@ -83,7 +84,6 @@ struct HgemmCfg {
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
 };
 
-__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.f + erff(v * 0.70710678118654752f)); }
 
 struct UnitCoord {
     int tile, split, m0, n0, kb0, kb1;
@@ -201,9 +201,16 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
                 if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
         }
     }
+    // One uniform pass per activation (the branch is taken once per chunk).
     if (p.act == 1) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
+        for (int j = 0; j < 32; ++j) v[j] = apply_activation(1, v[j]);
+    } else if (p.act == 2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = apply_activation(2, v[j]);
+    } else if (p.act == 3) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = apply_activation(3, v[j]);
     }
 }
 
@@ -211,7 +218,7 @@ __device__ __forceinline__ float epi_value(float acc, const HgemmArgs &p, float 
     float v = p.alpha * acc;
     if (p.beta != 0.f) v = fmaf(p.beta, cold, v);
     v += b;
-    if (p.act == 1) v = gelu_f(v);
+    v = apply_activation(p.act, v);
     return v;
 }
 
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         adesc = umma_desc_sw128(a_addr + kk * 2048, 8192, 1024);
                         bdesc = umma_desc_sw128(b_addr + kk * 32, 16, 1024);
                     }
-                    umma_f16(d_tmem, adesc, bdesc, kIdesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+                    umma_f16(d_tmem, adesc, bdesc, kIdesc | p.idesc_fmt, (kb > c.kb0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
                 if (++stage == STAGES) {
@@ -723,7 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kBK / kUmmaK; ++kk)
                     umma_f16_pair(d_tmem, umma_desc_sw128(a_addr + kk * 32, 16, 1024),
-                                  umma_desc_sw128(b_addr + kk * 2048, 8192, 1024), kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                                  umma_desc_sw128(b_addr + kk * 2048, 8192, 1024), kIdesc | p.idesc_fmt,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
                 umma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
                 if (++stage == STAGES) {
                     stage = 0;
@@ -894,9 +902,13 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
 }  // namespace
 
 cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
-                         const float *bias, int act, cudaStream_t stream, CallInfo *info) {
+                         const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info) {
     const int sms = device_sm_count();
+    // FP16 and BF16 inputs share every kernel: the tensor maps carry the
+    // element type and the MMA instruction descriptor the operand format.
+    const CUtensorMapDataType in_dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     HgemmArgs a{};
+    a.idesc_fmt = bf16 ? kIdescBf16Operands : 0u;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -976,8 +988,8 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
             a.splits = 1;
             a.units = t2;
             CUtensorMap ta, tb, tc;
-            if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, kBM) ||
-                !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK) ||
+            if (!encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, kBM) ||
+                !encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK) ||
                 !encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32))
                 return cudaErrorNotSupported;
             int used = 0;
@@ -1021,12 +1033,12 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     std::memset(&tc, 0, sizeof(tc));
     bool ok = true;
     if (!swap) {
-        ok = ok && encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, kBM);
-        ok = ok && encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK);
+        ok = ok && encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, kBM);
+        ok = ok && encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK);
         ok = ok && encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32);
     } else {
-        ok = ok && encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, bn);
-        ok = ok && encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK);
+        ok = ok && encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, bn);
+        ok = ok && encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK);
         tc = tb;  // unused by the transposed variant
     }
     if (!ok) return cudaErrorNotSupported;

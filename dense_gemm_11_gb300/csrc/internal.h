@@ -55,8 +55,9 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
 // ---- FP16 tensor-core path (hgemm.cu) ----
 // Returns cudaSuccess, or cudaErrorNotSupported when the tensor-map encoder
 // is unavailable.
+// A and B are FP16 (bf16 == false) or BF16 (bf16 == true); the plans are the same.
 cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
-                         const float *bias, int act, cudaStream_t stream, CallInfo *info);
+                         const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info);
 
 // The same small-M (M <= 64) transposed split-K plan with its scratch in a
 // fixed device array (no allocation).  *reject = 1 if M > 64, 2 if the plan's

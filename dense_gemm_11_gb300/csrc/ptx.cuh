@@ -25,6 +25,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- epilogue activations
+// 0 identity, 1 exact GELU x*Phi(x) (erff), 2 ReLU, 3 tanh-approximate GELU
+// 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) (tanhf).
+__device__ __forceinline__ float apply_activation(int act, float v) {
+    switch (act) {
+        case 1: return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+        case 2: return fmaxf(v, 0.f);
+        case 3: return 0.5f * v * (1.f + tanhf(0.79788456080286536f * fmaf(0.044715f * v, v * v, v)));
+        default: return v;
+    }
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte copy global -> shared; src_bytes < 16 zero-fills the rest (0: all zero).
 __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src, int src_bytes) {
@@ -263,5 +275,8 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16_f32(int M, int N, int a_mn
            | (static_cast<uint32_t>(N >> 3) << 17)    // N >> 3
            | (static_cast<uint32_t>(M >> 4) << 24);   // M >> 4
 }
+// Operand-format bits for BF16 A and B (the same kind::f16 MMA; only the two
+// 3-bit format fields change, F16 = 0, BF16 = 1).
+constexpr uint32_t kIdescBf16Operands = (1u << 7) | (1u << 10);
 
 }  // namespace gemm11

@@ -699,7 +699,7 @@ __global__ void scale_c_kernel(int M, int N, float beta, float *C, int ldc, cons
         float *c = C + static_cast<size_t>(i) * ldc + j;
         float v = beta != 0.f ? beta * *c : 0.f;
         if (bias) v += bias[j];
-        if (act == 1) v = 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+        v = apply_activation(act, v);
         *c = v;
     }
 }

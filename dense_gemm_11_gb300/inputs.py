@@ -7,10 +7,13 @@ their inputs from here, so both see the identical arrays.
 Recipe (the same for every workload):
   * generator ``numpy.random.default_rng(seed)`` (PCG64);
   * draw order A, then B, then C, then bias; each drawn as float64 and then
-    cast (float32, or float16 with round-to-nearest-even);
+    cast (float32, or float16 with round-to-nearest-even; bf16 inputs are
+    cast to float32 and then rounded to bfloat16, nearest-even on the float32
+    bit pattern, and held in float32 arrays whose values are all exact
+    bfloat16 numbers -- numpy has no bfloat16 type);
   * ``uniform`` = U[-1, 1]; ``normal`` = N(0, sigma) with sigma the standard
     deviation; ``normal_k`` = N(0, 1/sqrt(K)); ``smallint`` = integers drawn
-    uniformly from [-4, 4] (exact in fp16 and fp32; every partial sum of K
+    uniformly from [-4, 4] (exact in fp16, bf16 and fp32; every partial sum of K
     products stays below 2**24 for K <= 2**20);
   * when beta == 0, C is filled with NaN so that a kernel that reads it fails.
 
@@ -29,7 +32,7 @@ import numpy as np
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str            # "f32" or "f16"
+    kind: str            # "f32", "f16" or "bf16"
     M: int
     N: int
     K: int
@@ -37,8 +40,8 @@ class Workload:
     beta: float
     dist: str            # uniform | normal | normal_k | smallint
     seed: int
-    bias: bool = False   # f16 only: bias ~ N(0, 0.1), fp32, length N
-    act: int = 0         # 0 none, 1 exact GELU
+    bias: bool = False   # 16-bit inputs only: bias ~ N(0, 0.1), fp32, length N
+    act: int = 0         # 0 none, 1 exact GELU, 2 ReLU, 3 tanh GELU
     note: str = ""
 
     @property
@@ -69,6 +72,14 @@ def _registry():
         w[f"f16_epi{i}"] = Workload(f"f16_epi{i}", "f16", m, n, k, 0.5, 0.0, "normal_k", i,
                                     bias=True, act=1,
                                     note=f"FP16 GELU(0.5*A*B+bias) {m}x{n}x{k}")
+    w["bf16_4096"] = Workload("bf16_4096", "bf16", 4096, 4096, 4096, 1.0, 0.0, "normal_k", 10,
+                              note="BF16-in FP32-acc 4096^3")
+    w["bf16_4096_int"] = Workload("bf16_4096_int", "bf16", 4096, 4096, 4096, 1.0, 0.0, "smallint", 11,
+                                  note="BF16-in 4096^3, integers in [-4,4], exact")
+    for i, ((m, n, k), act) in enumerate(zip(EPILOGUE_SHAPES, (2, 3, 2, 3))):
+        w[f"bf16_epi{i}"] = Workload(f"bf16_epi{i}", "bf16", m, n, k, 0.5, 0.0, "normal_k", 12 + i,
+                                     bias=True, act=act,
+                                     note=f"BF16 {'ReLU' if act == 2 else 'tanh-GELU'}(0.5*A*B+bias) {m}x{n}x{k}")
     return w
 
 
@@ -87,6 +98,27 @@ def _draw(rng, dist, shape, K):
     raise ValueError(f"unknown distribution {dist!r}")
 
 
+def round_to_bf16(x):
+    """Round to the nearest bfloat16 (ties to even), returned as float32.
+
+    x is cast to float32 first; the low 16 bits of each float32 pattern are
+    then rounded away.  Finite inputs only (the generators draw no inf/NaN).
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def _cast_input(x, kind):
+    if kind == "f32":
+        return x.astype(np.float32)
+    if kind == "f16":
+        return x.astype(np.float16)
+    if kind == "bf16":
+        return round_to_bf16(x)
+    raise ValueError(f"unknown input kind {kind!r}")
+
+
 def make(M, N, K, *, kind="f32", dist="uniform", seed=0, beta=0.0, bias=False,
          lda=None, ldb=None, ldc=None):
     """Draw A (M x lda), B (K x ldb), C (M x ldc) and bias (N) for one GEMM.
@@ -94,7 +126,8 @@ def make(M, N, K, *, kind="f32", dist="uniform", seed=0, beta=0.0, bias=False,
     Leading dimensions default to the widths (K, N, N).  Columns past the
     logical width are drawn too (they are part of the buffer but never part of
     the product).  Returns a dict with numpy arrays: A and B are float32
-    (kind "f32") or float16 (kind "f16"); C and bias are float32.
+    (kind "f32"), float16 (kind "f16") or float32 holding bfloat16 values
+    (kind "bf16"); C and bias are float32.
     """
     lda = K if lda is None else lda
     ldb = N if ldb is None else ldb
@@ -102,9 +135,8 @@ def make(M, N, K, *, kind="f32", dist="uniform", seed=0, beta=0.0, bias=False,
     if lda < K or ldb < N or ldc < N:
         raise ValueError("leading dimension smaller than the width")
     rng = np.random.default_rng(seed)
-    in_t = np.float32 if kind == "f32" else np.float16
-    A = _draw(rng, dist, (M, lda), K).astype(in_t)
-    B = _draw(rng, dist, (K, ldb), K).astype(in_t)
+    A = _cast_input(_draw(rng, dist, (M, lda), K), kind)
+    B = _cast_input(_draw(rng, dist, (K, ldb), K), kind)
     if beta != 0.0:
         Cdist = "uniform" if dist in ("uniform", "normal_k") else dist
         C = _draw(rng, Cdist, (M, ldc), K).astype(np.float32)

@@ -59,8 +59,10 @@ typedef enum {
 } gemm_status;
 
 typedef enum {
-    GEMM_ACT_NONE = 0, /* identity */
-    GEMM_ACT_GELU = 1  /* exact GELU: x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))) */
+    GEMM_ACT_NONE = 0,      /* identity */
+    GEMM_ACT_GELU = 1,      /* exact GELU: x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))) */
+    GEMM_ACT_RELU = 2,      /* max(x, 0) */
+    GEMM_ACT_GELU_TANH = 3  /* 0.5 * x * (1 + tanh(sqrt(2/pi) * (x + 0.044715 * x^3))) */
 } gemm_act;
 
 /*
@@ -93,7 +95,9 @@ GEMM11_API int gemm_f32(int M, int N, int K, float alpha, const float *A, int ld
  *   B     __half, K x N, row-major, ldb = N.
  *   C     float,  M x N, row-major, ldc = N.
  *   bias  float, length N, or NULL for no bias.
- *   act   GEMM_ACT_NONE or GEMM_ACT_GELU.
+ *   act   one of gemm_act; any other value returns GEMM_ERR_INVALID_ARG.
+ *         The pages name an activation (GELU) in the epilogue without fixing
+ *         its form; exact GELU, ReLU and the tanh form of GELU are offered.
  * The tensor-memory-access path needs K % 8 == 0, N % 8 == 0 and A, B, C
  * 16-byte aligned ("第24讲 ... GEMM 分块与 Tensor Core 思维", section 7.2 item 7:
  * pad tensor-core operands to aligned sizes); anything else returns
@@ -101,6 +105,19 @@ GEMM11_API int gemm_f32(int M, int N, int K, float alpha, const float *A, int ld
  */
 GEMM11_API int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B,
                              float beta, float *C, const float *bias, int act, void *stream);
+
+/*
+ * gemm_bf16_f32acc_epilogue -- gemm_f16_f32acc_epilogue with BF16 inputs:
+ * A and B hold __nv_bfloat16 values (8 exponent bits, 8 significand bits),
+ * everything else -- the formula, C, bias, act, the alignment rules, the
+ * return codes and the kernels -- is the same.  "第24讲 ... GEMM 分块与
+ * Tensor Core 思维", section 5.1 (tensor-core half precision is FP16/BF16)
+ * and section 7.2 item 7 (large-model tensor-core operands are FP16 or BF16).
+ * Products of two BF16 values are exact in FP32, so the accuracy bound is the
+ * FP16 path's: rounding of the FP32 accumulation only.
+ */
+GEMM11_API int gemm_bf16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B,
+                                         float beta, float *C, const float *bias, int act, void *stream);
 
 /*
  * gemm_f16_f32acc_epilogue_noalloc -- the same operation and arguments as

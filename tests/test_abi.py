@@ -65,13 +65,25 @@ def test_empty_shapes_are_noops_without_cuda(L):
     assert g.gemm_f16_raw(0, 8, 8, 1.0, 0, 0, 0.0, 0) == g.GEMM_OK
 
 
-def test_f16_rejects_bad_args(L):
-    assert g.gemm_f16_raw(-1, 8, 8, 1.0, FAKE, FAKE, 0.0, FAKE) == g.GEMM_ERR_INVALID_ARG
-    assert g.gemm_f16_raw(8, 8, 8, 1.0, FAKE, FAKE, 0.0, FAKE, act=7) == g.GEMM_ERR_INVALID_ARG
-    assert g.gemm_f16_raw(8, 8, 8, 1.0, 0, FAKE, 0.0, FAKE) == g.GEMM_ERR_INVALID_ARG
-    assert g.gemm_f16_raw(8, 8, 8, 1.0, FAKE, FAKE, 0.0, 0) == g.GEMM_ERR_INVALID_ARG
+@pytest.mark.parametrize("raw", ["gemm_f16_raw", "gemm_bf16_raw", "gemm_f16_noalloc_raw"])
+def test_16bit_rejects_bad_args(L, raw):
+    f = getattr(g, raw)
+    assert f(-1, 8, 8, 1.0, FAKE, FAKE, 0.0, FAKE) == g.GEMM_ERR_INVALID_ARG
+    for act in (-1, 4, 7):
+        assert f(8, 8, 8, 1.0, FAKE, FAKE, 0.0, FAKE, act=act) == g.GEMM_ERR_INVALID_ARG
+    assert f(8, 8, 8, 1.0, 0, FAKE, 0.0, FAKE) == g.GEMM_ERR_INVALID_ARG
+    assert f(8, 8, 8, 1.0, FAKE, FAKE, 0.0, 0) == g.GEMM_ERR_INVALID_ARG
+    assert f(0, 8, 8, 1.0, 0, 0, 0.0, 0, act=3) == g.GEMM_OK
 
 
+def test_activation_codes_match_the_header():
+    text = open(HEADER).read()
+    for name in ("GEMM_ACT_NONE", "GEMM_ACT_GELU", "GEMM_ACT_RELU", "GEMM_ACT_GELU_TANH"):
+        m = re.search(name + r"\s*=\s*(\d+)", text)
+        assert m and int(m.group(1)) == getattr(g, name), name
+
+
+@pytest.mark.parametrize("raw", ["gemm_f16_raw", "gemm_bf16_raw"])
 @pytest.mark.parametrize("M,N,K,a,b,c", [
     (8, 8, 12, FAKE, FAKE, FAKE),          # K % 8 != 0
     (8, 12, 8, FAKE, FAKE, FAKE),          # N % 8 != 0
@@ -79,8 +91,8 @@ def test_f16_rejects_bad_args(L):
     (8, 8, 8, FAKE, FAKE + 8, FAKE),       # B not 16-byte aligned
     (8, 8, 8, FAKE, FAKE, FAKE + 4),       # C not 16-byte aligned
 ])
-def test_f16_unsupported_layouts(L, M, N, K, a, b, c):
-    assert g.gemm_f16_raw(M, N, K, 1.0, a, b, 0.0, c) == g.GEMM_ERR_UNSUPPORTED
+def test_16bit_unsupported_layouts(L, raw, M, N, K, a, b, c):
+    assert getattr(g, raw)(M, N, K, 1.0, a, b, 0.0, c) == g.GEMM_ERR_UNSUPPORTED
 
 
 def test_status_strings(L):

@@ -78,7 +78,7 @@ def test_f16_small_integers_exact_paths(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 512), (16, 1024, 2048), (2048, 4096, 1024)])
-@pytest.mark.parametrize("act", [0, 1])
+@pytest.mark.parametrize("act", [0, 1, 2, 3])
 def test_f16_beta_and_bias_epilogue(M, N, K, act):
     d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=7, beta=-0.5, bias=True)
     got, plan = run_f16(d, 0.5, -0.5, d["bias"], act)
@@ -101,17 +101,18 @@ def test_f16_beta_zero_does_not_read_c():
     assert np.isfinite(got).all(), plan
 
 
-def test_f16_alpha_zero_epilogue_only():
+@pytest.mark.parametrize("act", [1, 2, 3])
+def test_f16_alpha_zero_epilogue_only(act):
     rng = np.random.default_rng(9)
     C0 = rng.uniform(-1, 1, (33, 24)).astype(np.float32)
     bias = rng.normal(0, 0.1, 24).astype(np.float32)
     A = torch.full((33, 16), float("nan"), dtype=torch.float16, device=DEV)
     B = torch.full((16, 24), float("nan"), dtype=torch.float16, device=DEV)
     C = torch.from_numpy(C0).to(DEV)
-    g.gemm_f16_f32acc_epilogue(A, B, C, alpha=0.0, beta=2.0, bias=torch.from_numpy(bias).to(DEV), act=1)
+    g.gemm_f16_f32acc_epilogue(A, B, C, alpha=0.0, beta=2.0, bias=torch.from_numpy(bias).to(DEV), act=act)
     torch.cuda.synchronize()
-    ref, S = oracle.gemm(np.zeros((33, 16)), np.zeros((16, 24)), C0, alpha=0.0, beta=2.0, bias=bias, act=1)
-    assert_within(C.cpu().numpy(), ref, S, 1e-6, "alpha=0")
+    ref, S = oracle.gemm(np.zeros((33, 16)), np.zeros((16, 24)), C0, alpha=0.0, beta=2.0, bias=bias, act=act)
+    assert_within(C.cpu().numpy(), ref, S, 1e-6, f"alpha=0 act={act}")
 
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (16, 4096, 4096), (128, 11008, 4096)])
