@@ -9,8 +9,8 @@ The arithmetic lives in ``gemm_oracle.c`` (plain C, double accumulation, k
 ascending) and follows the GEMM definition C = alpha*A*B + beta*C of
 "SGEMM优化，从naive到warptiling" (section 项目概况 / 问题与估算), with the
 bias/scale/GELU epilogue of the DeepGEMM essay "企业官网建设流程全解析"
-(sections 1.3 and 3.2).  This module only compiles that file and marshals
-numpy arrays into it.
+(sections 1.3 and 3.2), and the rounding of a 16-bit output.  This module
+only compiles that file and marshals numpy arrays into it.
 
 Every oracle function is pinned by ``tests/test_oracle.py`` against closed
 forms, exact brute force and textbook values (none is "parity unpinned").
@@ -61,6 +61,8 @@ def _load():
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_gelu_f64.restype = ctypes.c_double
             lib.oracle_gelu_f64.argtypes = [ctypes.c_double]
+            lib.oracle_round_f64.restype = ctypes.c_int
+            lib.oracle_round_f64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_long]
             lib.oracle_act_f64.restype = ctypes.c_double
             lib.oracle_act_f64.argtypes = [ctypes.c_int, ctypes.c_double]
             _lib = lib
@@ -124,6 +126,20 @@ def gemm(A, B, C0=None, *, alpha=1.0, beta=0.0, bias=None, act=0, rows=None,
     if rc != 0:
         raise ValueError("oracle_gemm_f64 rejected its arguments")
     return out, scale
+
+
+OUT_TYPES = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def round_to(out_type: str, x):
+    """Round each value of x once, to nearest (ties to even), to the output
+    type "f32", "f16" or "bf16"; overflow gives +-inf.  Returns float64."""
+    x64 = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty_like(x64)
+    rc = _load().oracle_round_f64(OUT_TYPES[out_type], x64.ctypes.data, out.ctypes.data, x64.size)
+    if rc != 0:
+        raise ValueError("oracle_round_f64 rejected its arguments")
+    return out
 
 
 def gelu(x: float) -> float:

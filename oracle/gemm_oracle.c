@@ -43,6 +43,14 @@
  *
  * used by the tolerance |C - C_ref| <= tol * S + 1e-6.
  *
+ * Output element type (the tensor-core entry point may write C as FP16 or
+ * BF16): the value above is rounded once, to nearest with ties to even, to
+ * the output format; beyond the largest finite value it becomes +-inf
+ * (IEEE 754 roundTiesToEven).  FP16 = binary16 (11 significand bits,
+ * exponents -14..15), BF16 = 8 significand bits with binary32's exponent
+ * range (-126..127).  round_format below writes that rule out for any such
+ * format.
+ *
  * Threads: the listed rows are split into contiguous ranges, one per thread.
  * Build with -ffp-contract=off so that x86 and Arm hosts give the same bits.
  */
@@ -185,6 +193,45 @@ int oracle_gemm_f64(long M, long N, long K, double alpha, const double *A, long 
         if (jobs[t].status != 0) status = -1;
     }
     return status;
+}
+
+/*
+ * Round x to the nearest number of a binary floating-point format with p
+ * significand bits (the leading bit included), smallest normal exponent emin
+ * and largest exponent emax; ties go to the even neighbour; results past the
+ * largest finite number are +-inf.  The last kept bit of x has weight 2^q,
+ * q = max(exponent of x's leading bit, emin) - (p - 1) (below emin the
+ * spacing stays that of the subnormals); x / 2^q is rounded to an integer in
+ * the default rounding mode (nearest, ties to even) and scaled back.  Both
+ * scalings are exact.
+ */
+static double round_format(double x, int p, int emin, int emax) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    frexp(x, &e); /* |x| = m * 2^e with m in [0.5, 1): the leading bit is 2^(e-1) */
+    int lead = e - 1;
+    if (lead < emin) lead = emin;
+    const int q = lead - (p - 1);
+    double r = ldexp(nearbyint(ldexp(x, -q)), q);
+    const double max_finite = ldexp(2.0 - ldexp(1.0, 1 - p), emax);
+    if (fabs(r) > max_finite) r = copysign(INFINITY, x);
+    return r;
+}
+
+/*
+ * oracle_round_f64: out[i] = x[i] rounded to the output type (0 = FP32,
+ * 1 = FP16, 2 = BF16).  Returns 0, or -1 for an unknown type.
+ */
+int oracle_round_f64(int type, const double *x, double *out, long n) {
+    int p, emin, emax;
+    switch (type) {
+        case 0: p = 24; emin = -126; emax = 127; break;
+        case 1: p = 11; emin = -14; emax = 15; break;
+        case 2: p = 8; emin = -126; emax = 127; break;
+        default: return -1;
+    }
+    for (long i = 0; i < n; ++i) out[i] = round_format(x[i], p, emin, emax);
+    return 0;
 }
 
 /* The activations alone, exposed so that their special values can be pinned. */

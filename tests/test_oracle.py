@@ -242,3 +242,57 @@ def test_relu_and_tanh_gelu():
     out, _ = oracle.gemm(np.zeros((1, 2), np.float32), np.zeros((2, 3), np.float32),
                          bias=np.array([-1.0, 0.0, 2.0], np.float32), act=2)
     np.testing.assert_array_equal(out, [[0.0, 0.0, 2.0]])
+
+
+def test_round_to_f16_matches_numpy_binary16():
+    # numpy converts float64 to IEEE binary16 directly with round-to-nearest-
+    # even, including subnormals and overflow: an independent implementation.
+    rng = np.random.default_rng(11)
+    x = rng.uniform(1.0, 2.0, 40000) * np.exp2(rng.integers(-28, 18, 40000)) * rng.choice([-1.0, 1.0], 40000)
+    # exact ties and just-past-tie values at several binades
+    ties = np.array([(1 + (2 * k + 1) * 2.0 ** -11) * 2.0 ** e for k in range(8) for e in (-20, -14, -3, 0, 9, 15)])
+    x = np.concatenate([x, ties, -ties, ties + np.spacing(ties), [65504.0, 65519.0, 65520.0, 1e6, 2.0 ** -25,
+                                                                 3 * 2.0 ** -26, 2.0 ** -24, 0.0, -0.0]])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).astype(np.float64)
+    got = oracle.round_to("f16", x)
+    np.testing.assert_array_equal(got, ref)
+    assert np.signbit(got[-1])
+
+
+def test_round_to_f32_matches_numpy_binary32():
+    rng = np.random.default_rng(12)
+    x = rng.normal(size=40000) * np.exp2(rng.integers(-140, 128, 40000).astype(np.float64))
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(oracle.round_to("f32", x), ref)
+
+
+def test_round_to_bf16_special_cases():
+    u = 2.0 ** -7  # spacing of bfloat16 in [1, 2)
+    cases = {
+        1.0: 1.0,
+        1.0 + u / 2: 1.0,                      # tie -> even (1.0)
+        1.0 + 3 * u / 2: 1.0 + 2 * u,          # tie -> even (1 + 2u)
+        1.0 + u / 2 + 2.0 ** -40: 1.0 + u,     # just past the tie: up (rounding through
+                                               # binary32 first would give 1.0)
+        -(1.0 + u / 2 + 2.0 ** -40): -(1.0 + u),
+        3.0 * 2.0 ** 100: 3.0 * 2.0 ** 100,
+        2.0 ** -133: 2.0 ** -133,              # smallest subnormal
+        2.0 ** -134: 0.0,                      # half of it: tie -> even (0)
+        1.5 * 2.0 ** -134: 2.0 ** -133,
+        (2.0 - 2.0 ** -7) * 2.0 ** 127: (2.0 - 2.0 ** -7) * 2.0 ** 127,  # largest finite
+        (2.0 - 2.0 ** -8) * 2.0 ** 127: np.inf,                          # its tie: to inf
+    }
+    x = np.array(list(cases.keys()))
+    np.testing.assert_array_equal(oracle.round_to("bf16", x), np.array(list(cases.values())))
+
+
+def test_round_to_bf16_matches_bit_rounding_of_binary32_values():
+    # For values that are already binary32 numbers the result must equal the
+    # round-to-nearest-even of the float32 bit pattern's top 16 bits.
+    from dense_gemm_11_gb300 import inputs
+    rng = np.random.default_rng(13)
+    x = (rng.normal(size=40000) * np.exp2(rng.integers(-120, 120, 40000))).astype(np.float32)
+    np.testing.assert_array_equal(oracle.round_to("bf16", x.astype(np.float64)),
+                                  inputs.round_to_bf16(x).astype(np.float64))
