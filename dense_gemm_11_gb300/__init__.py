@@ -8,6 +8,7 @@ fallback: if the shared library is missing, every call raises.
     gemm_f16_f32acc_epilogue(A, B, C, alpha=1.0, beta=0.0, bias=None, act=0)
                                                       C = act(alpha*A@B + beta*C + bias)
     gemm_bf16_f32acc_epilogue(...)                    the same with bf16 A and B
+    gemm_tc(A, B, C, ...)                             the same for fp16/bf16 A, B and fp32/fp16/bf16 C
 
 Tensors are torch CUDA tensors on the current device; A and B may be 2-D
 views with a leading dimension larger than their width (unit column stride).
@@ -31,9 +32,12 @@ GEMM_ACT_NONE = 0
 GEMM_ACT_GELU = 1
 GEMM_ACT_RELU = 2
 GEMM_ACT_GELU_TANH = 3
+GEMM_DTYPE_F32 = 0
+GEMM_DTYPE_F16 = 1
+GEMM_DTYPE_BF16 = 2
 
 EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_bf16_f32acc_epilogue",
-                    "gemm_f16_f32acc_epilogue_noalloc",
+                    "gemm_tc_f32acc_epilogue", "gemm_f16_f32acc_epilogue_noalloc",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count")
 
@@ -67,6 +71,9 @@ def lib():
                                                    c_void_p, c_void_p, c_int, c_void_p]
             L.gemm_bf16_f32acc_epilogue.restype = c_int
             L.gemm_bf16_f32acc_epilogue.argtypes = L.gemm_f16_f32acc_epilogue.argtypes
+            L.gemm_tc_f32acc_epilogue.restype = c_int
+            L.gemm_tc_f32acc_epilogue.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_int,
+                                                  c_float, c_void_p, c_int, c_void_p, c_int, c_void_p]
             L.gemm_f16_f32acc_epilogue_noalloc.restype = c_int
             L.gemm_f16_f32acc_epilogue_noalloc.argtypes = L.gemm_f16_f32acc_epilogue.argtypes
             L.gemm_status_string.restype = ctypes.c_char_p
@@ -138,6 +145,15 @@ def gemm_bf16_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, 
                                            ctypes.c_void_p(bias_ptr or None), int(act), ctypes.c_void_p(stream_ptr))
 
 
+def gemm_tc_raw(M, N, K, alpha, A_ptr, B_ptr, ab_type, beta, C_ptr, c_type, bias_ptr=0, act=0,
+                stream_ptr=0) -> int:
+    """Direct C-ABI call of the general tensor-core entry point; returns the status code."""
+    return lib().gemm_tc_f32acc_epilogue(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr),
+                                         ctypes.c_void_p(B_ptr), int(ab_type), float(beta), ctypes.c_void_p(C_ptr),
+                                         int(c_type), ctypes.c_void_p(bias_ptr or None), int(act),
+                                         ctypes.c_void_p(stream_ptr))
+
+
 def gemm_f16_noalloc_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, act=0, stream_ptr=0) -> int:
     """C-ABI call of the no-allocation variant (M <= 64); returns the status code.
 
@@ -202,6 +218,38 @@ def gemm_bf16_f32acc_epilogue(A, B, C, alpha: float = 1.0, beta: float = 0.0, bi
     """C = act(alpha * A @ B + beta * C + bias): bf16 A, B; fp32 accumulate, bias and C."""
     import torch
     _gemm_16bit("gemm_bf16_f32acc_epilogue", torch.bfloat16, A, B, C, alpha, beta, bias, act, stream)
+
+
+def gemm_tc(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: int = 0, *, stream=None) -> None:
+    """C = act(alpha * A @ B + beta * C + bias) on the tensor cores, FP32 accumulate.
+
+    A and B: both fp16 or both bf16.  C: fp32, fp16 or bf16 (a 16-bit C is the
+    FP32 epilogue value rounded once to nearest even).  bias: fp32 or None.
+    """
+    import torch
+    types = {torch.float32: GEMM_DTYPE_F32, torch.float16: GEMM_DTYPE_F16, torch.bfloat16: GEMM_DTYPE_BF16}
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 2 or t.dtype not in types:
+            raise TypeError(f"{name} must be a 2-D CUDA float32/float16/bfloat16 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (leading dimension = width)")
+    if A.dtype != B.dtype or A.dtype == torch.float32:
+        raise TypeError("A and B must both be float16 or both bfloat16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
+    bias_ptr = 0
+    if bias is not None:
+        if not bias.is_cuda or bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous():
+            raise TypeError("bias must be a contiguous CUDA float32 tensor of length N")
+        bias_ptr = bias.data_ptr()
+    st = lib().gemm_tc_f32acc_epilogue(M, N, K, float(alpha), ctypes.c_void_p(A.data_ptr()),
+                                       ctypes.c_void_p(B.data_ptr()), types[A.dtype], float(beta),
+                                       ctypes.c_void_p(C.data_ptr()), types[C.dtype],
+                                       ctypes.c_void_p(bias_ptr or None), int(act), _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_tc_f32acc_epilogue")
 
 
 def watchdog_selftest(wait_ms: int = 20, stream=None) -> int:

@@ -183,12 +183,15 @@ namespace {
 
 bool valid_act(int act) { return act >= GEMM_ACT_NONE && act <= GEMM_ACT_GELU_TANH; }
 
-// The 16-bit-input entry points (FP16 or BF16 operands, FP32 accumulate and
-// output, fused epilogue) share validation and planning.
-int gemm_16bit_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
-                               const float *bias, int act, bool bf16, void *stream) {
+// The tensor-core entry points (FP16 or BF16 operands, FP32 accumulate,
+// FP32/FP16/BF16 output, fused epilogue) share validation and planning.
+int gemm_16bit_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, int ab_type,
+                               float beta, void *C, int c_type, const float *bias, int act, void *stream) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (!valid_act(act)) return GEMM_ERR_INVALID_ARG;
+    if (ab_type != GEMM_DTYPE_F16 && ab_type != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    if (c_type != GEMM_DTYPE_F32 && c_type != GEMM_DTYPE_F16 && c_type != GEMM_DTYPE_BF16)
+        return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) {
         t_last_plan = "noop_empty";
         t_last_launches = 0;
@@ -211,9 +214,10 @@ int gemm_16bit_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, 
     CallInfo info;
     cudaError_t e;
     if (!product) {
-        e = run_scale_c(M, N, beta, C, N, bias, act, s, &info);
+        e = c_type == GEMM_DTYPE_F32 ? run_scale_c(M, N, beta, static_cast<float *>(C), N, bias, act, s, &info)
+                                     : run_scale_c16(M, N, beta, C, c_type, bias, act, s, &info);
     } else {
-        e = run_gemm_f16(M, N, K, alpha, A, B, beta, C, bias, act, bf16, s, &info);
+        e = run_gemm_f16(M, N, K, alpha, A, B, beta, C, c_type, bias, act, ab_type == GEMM_DTYPE_BF16, s, &info);
         if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return fail_cuda(e);
@@ -228,12 +232,19 @@ extern "C" {
 
 int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
                              const float *bias, int act, void *stream) {
-    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, beta, C, bias, act, false, stream);
+    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, GEMM_DTYPE_F16, beta, C, GEMM_DTYPE_F32, bias, act,
+                                      stream);
 }
 
 int gemm_bf16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta,
                               float *C, const float *bias, int act, void *stream) {
-    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, beta, C, bias, act, true, stream);
+    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, GEMM_DTYPE_BF16, beta, C, GEMM_DTYPE_F32, bias, act,
+                                      stream);
+}
+
+int gemm_tc_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, int ab_type, float beta,
+                            void *C, int c_type, const float *bias, int act, void *stream) {
+    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, ab_type, beta, C, c_type, bias, act, stream);
 }
 
 int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const void *A, const void *B, float beta,

@@ -54,7 +54,8 @@ struct HgemmArgs {
     float alpha, beta;
     const float *bias;
     int act;
-    float *C;  // row-major M x N (ldc = N), for beta reads and transposed stores
+    void *C;     // row-major M x N (ldc = N), for beta reads and transposed stores
+    int c_type;  // kOutF32, kOutF16 or kOutBF16
     int tiles_m, tiles_n, kb_total, splits, units;
     float *ws;
     unsigned *counters;
@@ -169,16 +170,31 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
     if (p.beta != 0.f && grow < p.M) {
-        const float *crow = p.C + static_cast<size_t>(grow) * p.N;
+        if (p.c_type == kOutF32) {
+            const float *crow = static_cast<const float *>(p.C) + static_cast<size_t>(grow) * p.N;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int gc = col0 + 4 * q;
-            if (gc < p.N) {  // N % 8 == 0: the whole group of 4 is in range
-                const float4 c4 = *reinterpret_cast<const float4 *>(crow + gc);
-                v[4 * q] = fmaf(p.beta, c4.x, v[4 * q]);
-                v[4 * q + 1] = fmaf(p.beta, c4.y, v[4 * q + 1]);
-                v[4 * q + 2] = fmaf(p.beta, c4.z, v[4 * q + 2]);
-                v[4 * q + 3] = fmaf(p.beta, c4.w, v[4 * q + 3]);
+            for (int q = 0; q < 8; ++q) {
+                const int gc = col0 + 4 * q;
+                if (gc < p.N) {  // N % 8 == 0: the whole group of 4 is in range
+                    const float4 c4 = *reinterpret_cast<const float4 *>(crow + gc);
+                    v[4 * q] = fmaf(p.beta, c4.x, v[4 * q]);
+                    v[4 * q + 1] = fmaf(p.beta, c4.y, v[4 * q + 1]);
+                    v[4 * q + 2] = fmaf(p.beta, c4.z, v[4 * q + 2]);
+                    v[4 * q + 3] = fmaf(p.beta, c4.w, v[4 * q + 3]);
+                }
+            }
+        } else {
+            // 16-bit C: groups of 8 columns are 16-byte aligned (N % 8 == 0)
+            const uint16_t *crow = static_cast<const uint16_t *>(p.C) + static_cast<size_t>(grow) * p.N;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int gc = col0 + 8 * q;
+                if (gc < p.N) {
+                    float c8[8];
+                    unpack8_out16(*reinterpret_cast<const uint4 *>(crow + gc), p.c_type, c8);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[8 * q + i] = fmaf(p.beta, c8[i], v[8 * q + i]);
+                }
             }
         }
     }
@@ -211,6 +227,46 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
     } else if (p.act == 3) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = apply_activation(3, v[j]);
+    }
+}
+
+// Stage one finished 32 x 32 block (this lane's row: v) in one of the warp's
+// two 4 KB buffers and TMA-store it at (row0, col0).  FP32: 128-byte rows,
+// 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7)).  16-bit types:
+// 64-byte rows, 64-byte swizzle (chunk c of row r at c ^ ((r >> 1) & 3)).
+// Both patterns put the 32 lanes' 16-byte writes on distinct banks per
+// quarter warp.  One bulk group is committed per chunk (possibly empty), so
+// waiting for all but the newest group frees the buffer about to be reused.
+__device__ __forceinline__ void store_row_chunk(const float (&v)[32], const HgemmArgs &p, const CUtensorMap *tm_c,
+                                                uint8_t *stage_base, uint32_t &n_staged, int lane, int row0,
+                                                int col0) {
+    uint8_t *stage = stage_base + (n_staged & 1u) * 4096;
+    ++n_staged;
+    if (lane == 0) bulk_wait_read_all_but_one();
+    __syncwarp();
+    if (p.c_type == kOutF32) {
+        float *st = reinterpret_cast<float *>(stage) + lane * 32;
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+            *reinterpret_cast<float4 *>(st + ((c4 ^ (lane & 7)) << 2)) =
+                make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+    } else {
+        uint4 *st = reinterpret_cast<uint4 *>(stage + lane * 64);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 w;
+            w.x = pack2_out16(v[8 * c8], v[8 * c8 + 1], p.c_type);
+            w.y = pack2_out16(v[8 * c8 + 2], v[8 * c8 + 3], p.c_type);
+            w.z = pack2_out16(v[8 * c8 + 4], v[8 * c8 + 5], p.c_type);
+            w.w = pack2_out16(v[8 * c8 + 6], v[8 * c8 + 7], p.c_type);
+            st[c8 ^ ((lane >> 1) & 3)] = w;
+        }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (row0 < p.M && col0 < p.N) tma_store_2d(tm_c, stage, col0, row0);
+        bulk_commit();
     }
 }
 
@@ -363,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Two 4 KB staging buffers per warp used alternately (running chunk
         // count), so a chunk's shared-memory writes only wait for the TMA
         // store issued two chunks earlier.
-        float *const stage_base = reinterpret_cast<float *>(sC + (warp - 2) * 8192);
+        uint8_t *const stage_base = sC + (warp - 2) * 8192;
         uint32_t n_staged = 0;
         int local = 0;
         for (int idx = 0; !*abort_flag; ++idx, ++local) {
@@ -405,21 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int grow = c.m0 + row_in_tile;
                     const int col0 = c.n0 + ch * 32;
                     epilogue_row_chunk(v, p, grow, col0);
-                    // stage the 32x32 block (128-byte swizzle) and TMA-store it
-                    float *stage_c = stage_base + (n_staged & 1u) * 1024;
-                    ++n_staged;
-                    if (lane == 0) bulk_wait_read_all_but_one();
-                    __syncwarp();
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        *reinterpret_cast<float4 *>(stage_c + lane * 32 + ((c4 ^ (lane & 7)) << 2)) =
-                            make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (c.m0 + q * 32 < p.M && col0 < p.N) tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
-                        bulk_commit();  // one group per chunk, possibly empty
-                    }
+                    store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0);
                 } else {
                     // transposed: this thread owns column n of C, registers walk rows m
                     const int gn = c.n0 + row_in_tile;
@@ -429,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j) {
                             const int gm = ch * 32 + j;
                             if (gm < p.M) {
-                                float *cp = p.C + static_cast<size_t>(gm) * p.N + gn;
-                                const float cold = p.beta != 0.f ? *cp : 0.f;
-                                *cp = epi_value(v[j], p, cold, b);
+                                const size_t ci = static_cast<size_t>(gm) * p.N + gn;
+                                const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
+                                store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
                             }
                         }
                     }
@@ -520,20 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int grow = c.m0 + row_in_tile;
                             const int col0 = c.n0 + ch * 32;
                             epilogue_row_chunk(v, p, grow, col0);
-                            float *stage_c = stage_base + (n_staged & 1u) * 1024;
-                            ++n_staged;
-                            if (lane == 0) bulk_wait_read_all_but_one();
-                            __syncwarp();
-#pragma unroll
-                            for (int c4 = 0; c4 < 8; ++c4)
-                                *reinterpret_cast<float4 *>(stage_c + lane * 32 + ((c4 ^ (lane & 7)) << 2)) =
-                                    make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                if (c.m0 + q * 32 < p.M && col0 < p.N) tma_store_2d(&tm_c, stage_c, col0, c.m0 + q * 32);
-                                bulk_commit();  // one group per chunk, possibly empty
-                            }
+                            store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0);
                         } else {
                             const int gn = c.n0 + row_in_tile;
                             if (gn < p.N) {
@@ -542,9 +571,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = 0; j < 32; ++j) {
                                     const int gm = ch * 32 + j;
                                     if (gm < p.M) {
-                                        float *cp = p.C + static_cast<size_t>(gm) * p.N + gn;
-                                        const float cold = p.beta != 0.f ? *cp : 0.f;
-                                        *cp = epi_value(v[j], p, cold, b);
+                                        const size_t ci = static_cast<size_t>(gm) * p.N + gn;
+                                        const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
+                                        store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
                                     }
                                 }
                             }
@@ -748,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Two 4 KB staging buffers per warp used alternately (running chunk
         // count), so a chunk's shared-memory writes only wait for the TMA
         // store issued two chunks earlier.
-        float *const stage_base = reinterpret_cast<float *>(sC + (warp - 2) * 8192);
+        uint8_t *const stage_base = sC + (warp - 2) * 8192;
         uint32_t n_staged = 0;
         int local = 0;
         for (int t = cid; t < p.units && !*abort_flag; t += ncl, ++local) {
@@ -774,20 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 epilogue_row_chunk(v, p, grow, col0);
-                float *stage_c = stage_base + (n_staged & 1u) * 1024;
-                ++n_staged;
-                if (lane == 0) bulk_wait_read_all_but_one();
-                __syncwarp();
-#pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                    *reinterpret_cast<float4 *>(stage_c + lane * 32 + ((c4 ^ (lane & 7)) << 2)) =
-                        make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (my_m + q * 32 < p.M && col0 < p.N) tma_store_2d(&tm_c, stage_c, col0, my_m + q * 32);
-                    bulk_commit();  // one group per chunk, possibly empty
-                }
+                store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0);
             }
             tc_fence_before();
             __syncwarp();
@@ -838,7 +854,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 }
 
 bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem_bytes, const void *base, uint64_t inner,
-               uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = get_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -846,9 +863,18 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem_bytes, const v
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Store map of C: 32 x 32 boxes; FP32 rows of the box are 128 bytes (128-byte
+// swizzle), 16-bit rows 64 bytes (64-byte swizzle), matching store_row_chunk.
+bool encode_c(CUtensorMap *map, void *C, int c_type, int M, int N) {
+    if (c_type == kOutF32) return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32);
+    const CUtensorMapDataType dt =
+        c_type == kOutF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return encode_2d(map, dt, 2, C, N, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 template <int BN, int STAGES, bool SWAP>
@@ -901,8 +927,8 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
 
 }  // namespace
 
-cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
-                         const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info) {
+cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, void *C,
+                         int c_type, const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info) {
     const int sms = device_sm_count();
     // FP16 and BF16 inputs share every kernel: the tensor maps carry the
     // element type and the MMA instruction descriptor the operand format.
@@ -917,6 +943,7 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     a.bias = bias;
     a.act = act;
     a.C = C;
+    a.c_type = c_type;
     a.kb_total = (K + kBK - 1) / kBK;
     a.err = watchdog_word();
 
@@ -990,7 +1017,7 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
             CUtensorMap ta, tb, tc;
             if (!encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, kBM) ||
                 !encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK) ||
-                !encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32))
+                !encode_c(&tc, C, c_type, M, N))
                 return cudaErrorNotSupported;
             int used = 0;
             cudaError_t e;
@@ -1035,7 +1062,7 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     if (!swap) {
         ok = ok && encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, kBM);
         ok = ok && encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK);
-        ok = ok && encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32);
+        ok = ok && encode_c(&tc, C, c_type, M, N);
     } else {
         ok = ok && encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, bn);
         ok = ok && encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK);

@@ -55,9 +55,11 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
 // ---- FP16 tensor-core path (hgemm.cu) ----
 // Returns cudaSuccess, or cudaErrorNotSupported when the tensor-map encoder
 // is unavailable.
-// A and B are FP16 (bf16 == false) or BF16 (bf16 == true); the plans are the same.
-cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
-                         const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info);
+// A and B are FP16 (bf16 == false) or BF16 (bf16 == true); C is FP32, FP16
+// or BF16 (c_type: 0, 1, 2 -- the C ABI's gemm_dtype codes).  The plans are
+// the same for every combination.
+cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, void *C,
+                         int c_type, const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info);
 
 // The same small-M (M <= 64) transposed split-K plan with its scratch in a
 // fixed device array (no allocation).  *reject = 1 if M > 64, 2 if the plan's
@@ -70,5 +72,9 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
 // bias/act applied when given (the FP16 path), in sgemm.cu.
 cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float *bias, int act,
                         cudaStream_t stream, CallInfo *info);
+// The same for a 16-bit C (c_type 1 = FP16, 2 = BF16; ldc = N): the value is
+// computed in FP32 and rounded once to nearest even.
+cudaError_t run_scale_c16(int M, int N, float beta, void *C, int c_type, const float *bias, int act,
+                          cudaStream_t stream, CallInfo *info);
 
 }  // namespace gemm11

@@ -5,6 +5,8 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace gemm11 {
@@ -34,6 +36,56 @@ __device__ __forceinline__ float apply_activation(int act, float v) {
         case 2: return fmaxf(v, 0.f);
         case 3: return 0.5f * v * (1.f + tanhf(0.79788456080286536f * fmaf(0.044715f * v, v * v, v)));
         default: return v;
+    }
+}
+
+// ---------------------------------------------------------------- output element types
+// C of the tensor-core path is FP32, FP16 or BF16 (codes of the C ABI's
+// gemm_dtype).  16-bit results are rounded once, to nearest even, from the
+// FP32 epilogue value.
+constexpr int kOutF32 = 0;
+constexpr int kOutF16 = 1;
+constexpr int kOutBF16 = 2;
+
+__device__ __forceinline__ float load_out(const void *C, size_t idx, int type) {
+    if (type == kOutF16) return __half2float(static_cast<const __half *>(C)[idx]);
+    if (type == kOutBF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(C)[idx]);
+    return static_cast<const float *>(C)[idx];
+}
+
+__device__ __forceinline__ void store_out(void *C, size_t idx, int type, float v) {
+    if (type == kOutF16)
+        static_cast<__half *>(C)[idx] = __float2half_rn(v);
+    else if (type == kOutBF16)
+        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
+    else
+        static_cast<float *>(C)[idx] = v;
+}
+
+// Two values rounded to a 16-bit type and packed low-first into 32 bits.
+__device__ __forceinline__ uint32_t pack2_out16(float lo, float hi, int type) {
+    if (type == kOutF16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// Eight packed 16-bit values -> floats.
+__device__ __forceinline__ void unpack8_out16(const uint4 &w, int type, float *out) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (type == kOutF16) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[i]));
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        } else {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u[i]));
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
     }
 }
 

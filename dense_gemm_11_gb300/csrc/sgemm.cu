@@ -704,6 +704,18 @@ __global__ void scale_c_kernel(int M, int N, float beta, float *C, int ldc, cons
     }
 }
 
+// The same with a 16-bit C (ldc = N); c_type as in load_out / store_out.
+__global__ void scale_c16_kernel(int M, int N, float beta, void *C, int c_type, const float *bias, int act) {
+    const long long total = static_cast<long long>(M) * N;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(e % N);
+        float v = beta != 0.f ? beta * load_out(C, static_cast<size_t>(e), c_type) : 0.f;
+        if (bias) v += bias[j];
+        store_out(C, static_cast<size_t>(e), c_type, apply_activation(act, v));
+    }
+}
+
 // Copy a rows x cols window with leading dimension ld_src into a buffer with
 // leading dimension ld_dst (a multiple of 4, 16-byte aligned rows).  Each CTA
 // copies whole rows (blockIdx.y strides over rows); threads walk the columns.
@@ -744,6 +756,21 @@ cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4LL * device_sm_count()));
     scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc, bias, act);
     info->plan = "scale_c";
+    info->launches = 1;
+    return cudaPeekAtLastError();
+}
+
+cudaError_t run_scale_c16(int M, int N, float beta, void *C, int c_type, const float *bias, int act,
+                          cudaStream_t stream, CallInfo *info) {
+    if (beta == 1.f && !bias && act == 0) {
+        info->plan = "noop_beta1";
+        info->launches = 0;
+        return cudaSuccess;
+    }
+    const long long total = static_cast<long long>(M) * N;
+    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4LL * device_sm_count()));
+    scale_c16_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, c_type, bias, act);
+    info->plan = "scale_c16";
     info->launches = 1;
     return cudaPeekAtLastError();
 }

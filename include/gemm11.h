@@ -65,6 +65,13 @@ typedef enum {
     GEMM_ACT_GELU_TANH = 3  /* 0.5 * x * (1 + tanh(sqrt(2/pi) * (x + 0.044715 * x^3))) */
 } gemm_act;
 
+/* Element types of the tensor-core entry point gemm_tc_f32acc_epilogue. */
+typedef enum {
+    GEMM_DTYPE_F32 = 0,  /* IEEE binary32 */
+    GEMM_DTYPE_F16 = 1,  /* IEEE binary16 (__half) */
+    GEMM_DTYPE_BF16 = 2  /* bfloat16 (__nv_bfloat16): binary32 with the low 16 bits dropped */
+} gemm_dtype;
+
 /*
  * gemm_f32 -- true-FP32 SGEMM on the CUDA cores (FFMA, round-to-nearest).
  *   C[i*ldc + j] = alpha * sum_k A[i*lda + k] * B[k*ldb + j] + beta * C[i*ldc + j]
@@ -118,6 +125,26 @@ GEMM11_API int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const 
  */
 GEMM11_API int gemm_bf16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B,
                                          float beta, float *C, const float *bias, int act, void *stream);
+
+/*
+ * gemm_tc_f32acc_epilogue -- the general form of the two entry points above:
+ * A and B of element type ab_type (GEMM_DTYPE_F16 or GEMM_DTYPE_BF16), FP32
+ * accumulation, and C of element type c_type (GEMM_DTYPE_F32, GEMM_DTYPE_F16
+ * or GEMM_DTYPE_BF16):
+ *   C[i*N + j] = round_c( act( alpha * sum_k A[i*K + k] * B[k*N + j]
+ *                              + beta * C[i*N + j] + bias[j] ) )
+ * Everything inside round_c is evaluated in FP32 (the beta term reads the
+ * 16-bit C and widens it exactly); round_c is the identity for FP32 and one
+ * round-to-nearest-even for the 16-bit types (overflow gives +-inf).  The
+ * DeepGEMM essay "企业官网建设流程全解析" (section 1.1) argues for folding
+ * the work around a GEMM into its epilogue so that no extra pass over HBM
+ * is needed; a 16-bit C is one more such step (it halves C's bytes).
+ * Layouts, alignment rules (C 16-byte aligned, N % 8 == 0, K % 8 == 0) and
+ * return codes are those of gemm_f16_f32acc_epilogue; an ab_type or c_type
+ * outside the lists above returns GEMM_ERR_INVALID_ARG.
+ */
+GEMM11_API int gemm_tc_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, int ab_type,
+                                       float beta, void *C, int c_type, const float *bias, int act, void *stream);
 
 /*
  * gemm_f16_f32acc_epilogue_noalloc -- the same operation and arguments as

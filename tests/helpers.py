@@ -6,6 +6,9 @@ import numpy as np
 TOL_F32 = 1e-5
 TOL_F16 = 2e-3
 ABS_FLOOR = 1e-6
+# Unit roundoff of a 16-bit result: rounding the FP32 epilogue value v once to
+# the output format adds at most u * |v| <= u * (|ref| + tol * S).
+UNIT_ROUNDOFF = {"f32": 2.0 ** -24, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}
 
 
 def sample_rows(M, seed=0, n_random=24, tile=128):
@@ -18,10 +21,14 @@ def sample_rows(M, seed=0, n_random=24, tile=128):
     return np.array(sorted(r for r in rows if 0 <= r < M), dtype=np.int64)
 
 
-def assert_within(got, ref, S, tol, what=""):
+def assert_within(got, ref, S, tol, what="", out="f32"):
+    """|got - ref| <= tol * S + 1e-6, widened by one output rounding for a
+    16-bit result (out = "f16" or "bf16")."""
     got = np.asarray(got, dtype=np.float64)
     err = np.abs(got - ref)
     bound = tol * S + ABS_FLOOR
+    if out != "f32":
+        bound = bound + UNIT_ROUNDOFF[out] * (np.abs(ref) + tol * S)
     bad = ~(err <= bound)  # NaN counts as bad
     if bad.any():
         idx = np.argwhere(bad)[:5].tolist()

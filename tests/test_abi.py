@@ -76,6 +76,25 @@ def test_16bit_rejects_bad_args(L, raw):
     assert f(0, 8, 8, 1.0, 0, 0, 0.0, 0, act=3) == g.GEMM_OK
 
 
+def test_tc_rejects_bad_types(L):
+    for ab in (-1, 0, 3):   # F32 operands are not a tensor-core input type here
+        assert g.gemm_tc_raw(8, 8, 8, 1.0, FAKE, FAKE, ab, 0.0, FAKE, 0) == g.GEMM_ERR_INVALID_ARG
+    for ct in (-1, 3, 9):
+        assert g.gemm_tc_raw(8, 8, 8, 1.0, FAKE, FAKE, 1, 0.0, FAKE, ct) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_tc_raw(8, 8, 8, 1.0, FAKE, FAKE, 2, 0.0, FAKE, 1, act=4) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_tc_raw(0, 8, 8, 1.0, 0, 0, 2, 0.0, 0, 2) == g.GEMM_OK
+    # 16-bit C: the same alignment rules
+    assert g.gemm_tc_raw(8, 8, 8, 1.0, FAKE, FAKE, 1, 0.0, FAKE + 2, 1) == g.GEMM_ERR_UNSUPPORTED
+    assert g.gemm_tc_raw(8, 12, 8, 1.0, FAKE, FAKE, 1, 0.0, FAKE, 2) == g.GEMM_ERR_UNSUPPORTED
+
+
+def test_dtype_codes_match_the_header():
+    text = open(HEADER).read()
+    for name in ("GEMM_DTYPE_F32", "GEMM_DTYPE_F16", "GEMM_DTYPE_BF16"):
+        m = re.search(name + r"\s*=\s*(\d+)", text)
+        assert m and int(m.group(1)) == getattr(g, name), name
+
+
 def test_activation_codes_match_the_header():
     text = open(HEADER).read()
     for name in ("GEMM_ACT_NONE", "GEMM_ACT_GELU", "GEMM_ACT_RELU", "GEMM_ACT_GELU_TANH"):
