@@ -380,7 +380,7 @@ def run_profile_case(case: str, repeats: int):
     print(f"{case}: {repeats} launches of plan {g.last_plan()}")
 
 
-def run_sweep(reps: int):
+def run_sweep(reps: int, only=None):
     """Time every named workload (one JSON line each).
 
     Two figures per workload: `ms` is the median of single calls, each after
@@ -401,19 +401,36 @@ def run_sweep(reps: int):
     stream = torch.cuda.current_stream(dev)
     l2_bytes = 129 * 1024 * 1024
     for name, w in inputs.WORKLOADS.items():
+        if only and name not in only:
+            continue
         d = inputs.make_workload(w)
         set_bytes = sum(d[k].nbytes for k in ("A", "B", "C"))
         nbuf = max(1, min(16, -(-3 * l2_bytes // set_bytes)))
+        in_t = torch.bfloat16 if w.kind == "bf16" else None
+        out_t = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out]
+        general = w.kind != "f32" and (w.batch > 1 or w.b_trans or w.out != "f32")
         sets = []
         for _ in range(nbuf):
-            sets.append({k: torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")})
+            t = {k: torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")}
+            if in_t is not None:  # bf16 values travel as float32 arrays
+                t["A"], t["B"] = t["A"].to(in_t), t["B"].to(in_t)
+            t["C"] = t["C"].to(out_t)
+            if general and w.batch == 1 and not w.b_trans:
+                t = {k: v.unsqueeze(0) for k, v in t.items()}
+            sets.append(t)
         C0 = sets[0]["C"].clone()
         bias = torch.from_numpy(d["bias"]).to(dev) if "bias" in d else None
 
         def call(t, st=None):
             st = torch.cuda.current_stream(dev) if st is None else st
-            if w.kind == "f32":
+            if general:
+                g.gemm_tc_batched(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias, act=w.act,
+                                  b_trans=w.b_trans, stream=st)
+            elif w.kind == "f32":
                 g.gemm_f32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
+            elif w.kind == "bf16":
+                g.gemm_bf16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
+                                            act=w.act, stream=st)
             else:
                 g.gemm_f16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
                                            act=w.act, stream=st)
@@ -445,12 +462,7 @@ def run_sweep(reps: int):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
             for i in range(n_steady):
-                t = sets[i % nbuf]
-                if w.kind == "f32":
-                    g.gemm_f32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=cap)
-                else:
-                    g.gemm_f16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
-                                               act=w.act, stream=cap)
+                call(sets[i % nbuf], cap)
         graph.replay()
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -462,13 +474,14 @@ def run_sweep(reps: int):
         ms_steady = e0.elapsed_time(e1) / n_steady
         del graph
         ms = statistics.median(times)
-        flops = roofline.gemm_flops(w.M, w.N, w.K)
+        flops = roofline.gemm_flops(w.M, w.N, w.K, w.batch)
         nbytes = roofline.gemm_bytes(w.M, w.N, w.K, in_bytes=4 if w.kind == "f32" else 2,
-                                     beta_nonzero=w.beta != 0.0, bias=w.bias)
+                                     beta_nonzero=w.beta != 0.0, bias=w.bias, out_bytes=4 if w.out == "f32" else 2,
+                                     batch=w.batch)
         peak = f32_peak if w.kind == "f32" else tc_peak
         roof, bound = roofline.roofline_tflops(flops, nbytes, peak, hbm_gbs)
         tflops = flops / (ms_steady * 1e-3) / 1e12
-        print(json.dumps({"workload": name, "M": w.M, "N": w.N, "K": w.K, "plan": plan, "ms": ms,
+        print(json.dumps({"workload": name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K, "plan": plan, "ms": ms,
                           "ms_steady": ms_steady, "input_sets": nbuf, "tflops": tflops,
                           "gbs": nbytes / (ms_steady * 1e-3) / 1e9, "bound": bound, "roofline_tflops": roof,
                           "frac": tflops / roof,
@@ -489,9 +502,10 @@ def main():
                     help="launch one 4096^3 GEMM of the workload a few times (for ncu) and exit")
     ap.add_argument("--repeats", type=int, default=2)
     ap.add_argument("--sweep", action="store_true", help="time every named workload, one JSON line each")
+    ap.add_argument("--workloads", default="", help="comma-separated workload names for --sweep (default: all)")
     args = ap.parse_args()
     if args.sweep:
-        run_sweep(max(3, args.steps // 10))
+        run_sweep(max(3, args.steps // 10), [w for w in args.workloads.split(",") if w])
         return
     if args.profile_case:
         run_profile_case(args.profile_case, args.repeats)

@@ -9,6 +9,7 @@ fallback: if the shared library is missing, every call raises.
                                                       C = act(alpha*A@B + beta*C + bias)
     gemm_bf16_f32acc_epilogue(...)                    the same with bf16 A and B
     gemm_tc(A, B, C, ...)                             the same for fp16/bf16 A, B and fp32/fp16/bf16 C
+    gemm_tc_batched(A, B, C, ..., b_trans=False)      a strided batch of those (3-D tensors), op(B) = B or B^T
 
 Tensors are torch CUDA tensors on the current device; A and B may be 2-D
 views with a leading dimension larger than their width (unit column stride).
@@ -37,7 +38,7 @@ GEMM_DTYPE_F16 = 1
 GEMM_DTYPE_BF16 = 2
 
 EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_bf16_f32acc_epilogue",
-                    "gemm_tc_f32acc_epilogue", "gemm_f16_f32acc_epilogue_noalloc",
+                    "gemm_tc_f32acc_epilogue", "gemm_tc_strided_batched", "gemm_f16_f32acc_epilogue_noalloc",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count")
 
@@ -74,6 +75,11 @@ def lib():
             L.gemm_tc_f32acc_epilogue.restype = c_int
             L.gemm_tc_f32acc_epilogue.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_int,
                                                   c_float, c_void_p, c_int, c_void_p, c_int, c_void_p]
+            c_ll = ctypes.c_longlong
+            L.gemm_tc_strided_batched.restype = c_int
+            L.gemm_tc_strided_batched.argtypes = [c_int, c_int, c_int, c_int, c_float, c_void_p, c_ll, c_void_p,
+                                                  c_ll, c_int, c_int, c_float, c_void_p, c_ll, c_int, c_void_p,
+                                                  c_int, c_void_p]
             L.gemm_f16_f32acc_epilogue_noalloc.restype = c_int
             L.gemm_f16_f32acc_epilogue_noalloc.argtypes = L.gemm_f16_f32acc_epilogue.argtypes
             L.gemm_status_string.restype = ctypes.c_char_p
@@ -150,6 +156,16 @@ def gemm_tc_raw(M, N, K, alpha, A_ptr, B_ptr, ab_type, beta, C_ptr, c_type, bias
     """Direct C-ABI call of the general tensor-core entry point; returns the status code."""
     return lib().gemm_tc_f32acc_epilogue(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr),
                                          ctypes.c_void_p(B_ptr), int(ab_type), float(beta), ctypes.c_void_p(C_ptr),
+                                         int(c_type), ctypes.c_void_p(bias_ptr or None), int(act),
+                                         ctypes.c_void_p(stream_ptr))
+
+
+def gemm_tc_batched_raw(batch, M, N, K, alpha, A_ptr, stride_a, B_ptr, stride_b, ab_type, b_trans, beta, C_ptr,
+                        stride_c, c_type, bias_ptr=0, act=0, stream_ptr=0) -> int:
+    """Direct C-ABI call of the strided-batched entry point; returns the status code."""
+    return lib().gemm_tc_strided_batched(int(batch), int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr),
+                                         int(stride_a), ctypes.c_void_p(B_ptr), int(stride_b), int(ab_type),
+                                         int(b_trans), float(beta), ctypes.c_void_p(C_ptr), int(stride_c),
                                          int(c_type), ctypes.c_void_p(bias_ptr or None), int(act),
                                          ctypes.c_void_p(stream_ptr))
 
@@ -250,6 +266,60 @@ def gemm_tc(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: int 
                                        ctypes.c_void_p(bias_ptr or None), int(act), _stream_handle(stream))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_tc_f32acc_epilogue")
+
+
+def _batched_operand(t, name, rows, cols):
+    """(pointer, batch stride in elements, batch) of a 2-D (shared) or 3-D operand
+    whose matrices are row-major with unit column stride and row stride = cols."""
+    if t.dim() == 2:
+        if tuple(t.shape) != (rows, cols) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {rows} x {cols} matrix")
+        return t.data_ptr(), 0, None
+    if t.dim() != 3 or tuple(t.shape[1:]) != (rows, cols) or t.stride(2) != 1 or t.stride(1) != cols:
+        raise ValueError(f"{name} must be (batch, {rows}, {cols}) with row-major matrices, got "
+                         f"shape {tuple(t.shape)} strides {t.stride()}")
+    return t.data_ptr(), t.stride(0), t.shape[0]
+
+
+def gemm_tc_batched(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: int = 0, *,
+                    b_trans: bool = False, stream=None) -> None:
+    """C[z] = act(alpha * A[z] @ op(B[z]) + beta * C[z] + bias) for every z, one launch.
+
+    C: (batch, M, N) fp32/fp16/bf16.  A: (batch, M, K) or a shared (M, K).
+    B: (batch, K, N), or (batch, N, K) with b_trans=True (op(B) = B^T, e.g. the
+    keys of Q K^T); a 2-D B is shared by the batch.  A 3-D operand may have
+    batch stride 0 (torch.expand).  A and B both fp16 or both bf16.
+    """
+    import torch
+    types = {torch.float32: GEMM_DTYPE_F32, torch.float16: GEMM_DTYPE_F16, torch.bfloat16: GEMM_DTYPE_BF16}
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in types:
+            raise TypeError(f"{name} must be a CUDA float32/float16/bfloat16 tensor")
+    if A.dtype != B.dtype or A.dtype == torch.float32:
+        raise TypeError("A and B must both be float16 or both bfloat16")
+    if C.dim() != 3:
+        raise ValueError("C must be (batch, M, N)")
+    batch, M, N = C.shape
+    K = A.shape[-1]
+    c_ptr, sc, _ = _batched_operand(C, "C", M, N)
+    a_ptr, sa, ba = _batched_operand(A, "A", M, K)
+    b_ptr, sb, bb = _batched_operand(B, "B", N if b_trans else K, K if b_trans else N)
+    for nb, name in ((ba, "A"), (bb, "B")):
+        if nb is not None and nb != batch:
+            raise ValueError(f"{name} has batch {nb}, C has {batch}")
+    if batch > 1 and sc < M * N:
+        raise ValueError("C's matrices overlap (batch stride < M * N)")
+    bias_ptr = 0
+    if bias is not None:
+        if not bias.is_cuda or bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous():
+            raise TypeError("bias must be a contiguous CUDA float32 tensor of length N")
+        bias_ptr = bias.data_ptr()
+    st = lib().gemm_tc_strided_batched(batch, M, N, K, float(alpha), ctypes.c_void_p(a_ptr), sa,
+                                       ctypes.c_void_p(b_ptr), sb, types[A.dtype], 1 if b_trans else 0, float(beta),
+                                       ctypes.c_void_p(c_ptr), sc if batch > 1 else M * N, types[C.dtype],
+                                       ctypes.c_void_p(bias_ptr or None), int(act), _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_tc_strided_batched")
 
 
 def watchdog_selftest(wait_ms: int = 20, stream=None) -> int:

@@ -184,27 +184,31 @@ namespace {
 bool valid_act(int act) { return act >= GEMM_ACT_NONE && act <= GEMM_ACT_GELU_TANH; }
 
 // The tensor-core entry points (FP16 or BF16 operands, FP32 accumulate,
-// FP32/FP16/BF16 output, fused epilogue) share validation and planning.
-int gemm_16bit_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, int ab_type,
-                               float beta, void *C, int c_type, const float *bias, int act, void *stream) {
-    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-    if (!valid_act(act)) return GEMM_ERR_INVALID_ARG;
+// FP32/FP16/BF16 output, fused epilogue, optional strided batch and
+// transposed B) share validation and planning.
+int gemm_tc_checked(const TcGemm &g, int ab_type, void *stream) {
+    if (g.batch < 0 || g.M < 0 || g.N < 0 || g.K < 0) return GEMM_ERR_INVALID_ARG;
+    if (!valid_act(g.act)) return GEMM_ERR_INVALID_ARG;
     if (ab_type != GEMM_DTYPE_F16 && ab_type != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
-    if (c_type != GEMM_DTYPE_F32 && c_type != GEMM_DTYPE_F16 && c_type != GEMM_DTYPE_BF16)
+    if (g.c_type != GEMM_DTYPE_F32 && g.c_type != GEMM_DTYPE_F16 && g.c_type != GEMM_DTYPE_BF16)
         return GEMM_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) {
+    if (g.b_trans != 0 && g.b_trans != 1) return GEMM_ERR_INVALID_ARG;
+    if (g.batch == 0 || g.M == 0 || g.N == 0) {
         t_last_plan = "noop_empty";
         t_last_launches = 0;
         return GEMM_OK;
     }
-    if (!C) return GEMM_ERR_INVALID_ARG;
-    const bool product = (K > 0) && (alpha != 0.f);
-    if (product && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    if (!g.C) return GEMM_ERR_INVALID_ARG;
+    const long long mn = static_cast<long long>(g.M) * g.N;
+    if (g.batch > 1 && (g.stride_a < 0 || g.stride_b < 0 || g.stride_c < mn)) return GEMM_ERR_INVALID_ARG;
+    const bool product = (g.K > 0) && (g.alpha != 0.f);
+    if (product && (!g.A || !g.B)) return GEMM_ERR_INVALID_ARG;
+    // Tensor-map constraints: 16-byte aligned bases, row and matrix strides
+    // (the epilogue-only path, alpha == 0 or K == 0, has none).
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (product) {
-        // Tensor-map constraints: 16-byte aligned bases and row strides.
-        const bool ok = (K % 8 == 0) && (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) &&
-                        ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) &&
-                        ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+        const bool ok = (g.K % 8 == 0) && (g.N % 8 == 0) && al16(g.A) && al16(g.B) && al16(g.C) &&
+                        (g.batch == 1 || (g.stride_a % 8 == 0 && g.stride_b % 8 == 0 && g.stride_c % 8 == 0));
         if (!ok) return GEMM_ERR_UNSUPPORTED;
     }
     DeviceState *ds = device_state();
@@ -214,10 +218,13 @@ int gemm_16bit_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, 
     CallInfo info;
     cudaError_t e;
     if (!product) {
-        e = c_type == GEMM_DTYPE_F32 ? run_scale_c(M, N, beta, static_cast<float *>(C), N, bias, act, s, &info)
-                                     : run_scale_c16(M, N, beta, C, c_type, bias, act, s, &info);
+        e = run_scale_c_batched(g.batch, g.M, g.N, g.beta, g.C, g.batch > 1 ? g.stride_c : mn, g.c_type, g.bias,
+                                g.act, s, &info);
     } else {
-        e = run_gemm_f16(M, N, K, alpha, A, B, beta, C, c_type, bias, act, ab_type == GEMM_DTYPE_BF16, s, &info);
+        TcGemm gg = g;
+        gg.bf16 = ab_type == GEMM_DTYPE_BF16;
+        if (gg.batch == 1) gg.stride_a = gg.stride_b = 0, gg.stride_c = mn;
+        e = run_gemm_f16(gg, s, &info);
         if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return fail_cuda(e);
@@ -226,25 +233,54 @@ int gemm_16bit_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, 
     return GEMM_OK;
 }
 
+TcGemm tc_single(int M, int N, int K, float alpha, const void *A, const void *B, float beta, void *C, int c_type,
+                 const float *bias, int act) {
+    TcGemm g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.alpha = alpha;
+    g.A = A;
+    g.B = B;
+    g.beta = beta;
+    g.C = C;
+    g.c_type = c_type;
+    g.bias = bias;
+    g.act = act;
+    return g;
+}
+
 }  // namespace
 
 extern "C" {
 
 int gemm_f16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta, float *C,
                              const float *bias, int act, void *stream) {
-    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, GEMM_DTYPE_F16, beta, C, GEMM_DTYPE_F32, bias, act,
-                                      stream);
+    return gemm_tc_checked(tc_single(M, N, K, alpha, A, B, beta, C, GEMM_DTYPE_F32, bias, act), GEMM_DTYPE_F16,
+                           stream);
 }
 
 int gemm_bf16_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, float beta,
                               float *C, const float *bias, int act, void *stream) {
-    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, GEMM_DTYPE_BF16, beta, C, GEMM_DTYPE_F32, bias, act,
-                                      stream);
+    return gemm_tc_checked(tc_single(M, N, K, alpha, A, B, beta, C, GEMM_DTYPE_F32, bias, act), GEMM_DTYPE_BF16,
+                           stream);
 }
 
 int gemm_tc_f32acc_epilogue(int M, int N, int K, float alpha, const void *A, const void *B, int ab_type, float beta,
                             void *C, int c_type, const float *bias, int act, void *stream) {
-    return gemm_16bit_f32acc_epilogue(M, N, K, alpha, A, B, ab_type, beta, C, c_type, bias, act, stream);
+    return gemm_tc_checked(tc_single(M, N, K, alpha, A, B, beta, C, c_type, bias, act), ab_type, stream);
+}
+
+int gemm_tc_strided_batched(int batch, int M, int N, int K, float alpha, const void *A, long long stride_a,
+                            const void *B, long long stride_b, int ab_type, int b_trans, float beta, void *C,
+                            long long stride_c, int c_type, const float *bias, int act, void *stream) {
+    TcGemm g = tc_single(M, N, K, alpha, A, B, beta, C, c_type, bias, act);
+    g.batch = batch;
+    g.stride_a = stride_a;
+    g.stride_b = stride_b;
+    g.stride_c = stride_c;
+    g.b_trans = b_trans;
+    return gemm_tc_checked(g, ab_type, stream);
 }
 
 int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const void *A, const void *B, float beta,

@@ -60,7 +60,14 @@ struct HgemmArgs {
     float *ws;
     unsigned *counters;
     unsigned *err;
-    uint32_t idesc_fmt;  // operand-format bits OR'ed into the MMA instruction descriptor (BF16: A and B)
+    uint32_t idesc_fmt;  // operand-format bits of the MMA instruction descriptor (BF16: A and B)
+    uint32_t idesc;      // the whole instruction descriptor (set by the launcher for its tile shape)
+    // Strided batch: matrix z of A/B/C starts z * stride elements after the
+    // first (the tensor maps carry the strides).  za / zb are 0 for an operand
+    // shared by every matrix of the batch (stride 0), else 1.
+    int batch, za, zb;
+    long long stride_c;
+    int b_kmajor;  // 1: B is stored N x K (the product uses its transpose), 0: K x N
     // stream-K schedule (non-transposed, splits == 1): the first dp_tiles
     // tiles of the raster are whole units, the last sk_tiles are shared out
     // by k blocks over the grid; partial tiles go to 2 slots per CTA.
@@ -87,25 +94,33 @@ struct HgemmCfg {
 
 
 struct UnitCoord {
-    int tile, split, m0, n0, kb0, kb1;
+    int tile, split, m0, n0, kb0, kb1, batch;
     int slot;  // stream-K partial slot, -1 when the unit finishes its tile
 };
+
+// Tile number (over the whole batch) -> matrix index and tile origin.
+__device__ __forceinline__ void tile_origin(const HgemmArgs &p, int tile, int bn_tile, bool swap, UnitCoord &c) {
+    const int per = p.tiles_m * p.tiles_n;
+    c.batch = tile / per;
+    const int t = tile - c.batch * per;
+    if (swap) {
+        c.m0 = 0;
+        c.n0 = t * kBM;
+    } else {
+        // Grouped raster: 8 M-tiles per sweep over N (L2 reuse of B panels).
+        const int group_tiles = 8 * p.tiles_n;
+        const int first_m = (t / group_tiles) * 8;
+        const int gsz = min(p.tiles_m - first_m, 8);
+        c.m0 = (first_m + (t % group_tiles) % gsz) * kBM;
+        c.n0 = ((t % group_tiles) / gsz) * bn_tile;
+    }
+}
 
 __device__ __forceinline__ UnitCoord decode_unit(const HgemmArgs &p, int u, int bn_tile, bool swap) {
     UnitCoord c;
     c.tile = u / p.splits;
     c.split = u % p.splits;
-    if (swap) {
-        c.m0 = 0;
-        c.n0 = c.tile * kBM;
-    } else {
-        // Grouped raster: 8 M-tiles per sweep over N (L2 reuse of B panels).
-        const int group_tiles = 8 * p.tiles_n;
-        const int first_m = (c.tile / group_tiles) * 8;
-        const int gsz = min(p.tiles_m - first_m, 8);
-        c.m0 = (first_m + (c.tile % group_tiles) % gsz) * kBM;
-        c.n0 = ((c.tile % group_tiles) / gsz) * bn_tile;
-    }
+    tile_origin(p, c.tile, bn_tile, swap, c);
     c.kb0 = static_cast<int>(static_cast<long long>(p.kb_total) * c.split / p.splits);
     c.kb1 = static_cast<int>(static_cast<long long>(p.kb_total) * (c.split + 1) / p.splits);
     c.slot = -1;
@@ -146,11 +161,7 @@ __device__ __forceinline__ bool next_unit(const HgemmArgs &p, int idx, int bn_ti
     }
     c.tile = tile;
     c.split = 0;
-    const int group_tiles = 8 * p.tiles_n;
-    const int first_m = (tile / group_tiles) * 8;
-    const int gsz = min(p.tiles_m - first_m, 8);
-    c.m0 = (first_m + (tile % group_tiles) % gsz) * kBM;
-    c.n0 = ((tile % group_tiles) / gsz) * bn_tile;
+    tile_origin(p, tile, bn_tile, swap, c);
     return true;
 }
 
@@ -166,12 +177,13 @@ __device__ __forceinline__ void flag_timeout(volatile int *abort_flag, unsigned 
 // v = act(alpha * acc + beta * C + bias).  N % 8 == 0 and 16-byte aligned
 // C rows let in-range groups of 4 columns use 128-bit loads (bias too when
 // it is 16-byte aligned).
-__device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmArgs &p, int grow, int col0) {
+__device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmArgs &p, int grow, int col0,
+                                                   size_t cbase) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
     if (p.beta != 0.f && grow < p.M) {
         if (p.c_type == kOutF32) {
-            const float *crow = static_cast<const float *>(p.C) + static_cast<size_t>(grow) * p.N;
+            const float *crow = static_cast<const float *>(p.C) + cbase + static_cast<size_t>(grow) * p.N;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int gc = col0 + 4 * q;
@@ -185,7 +197,7 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
             }
         } else {
             // 16-bit C: groups of 8 columns are 16-byte aligned (N % 8 == 0)
-            const uint16_t *crow = static_cast<const uint16_t *>(p.C) + static_cast<size_t>(grow) * p.N;
+            const uint16_t *crow = static_cast<const uint16_t *>(p.C) + cbase + static_cast<size_t>(grow) * p.N;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int gc = col0 + 8 * q;
@@ -239,7 +251,7 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
 // waiting for all but the newest group frees the buffer about to be reused.
 __device__ __forceinline__ void store_row_chunk(const float (&v)[32], const HgemmArgs &p, const CUtensorMap *tm_c,
                                                 uint8_t *stage_base, uint32_t &n_staged, int lane, int row0,
-                                                int col0) {
+                                                int col0, int batch) {
     uint8_t *stage = stage_base + (n_staged & 1u) * 4096;
     ++n_staged;
     if (lane == 0) bulk_wait_read_all_but_one();
@@ -265,7 +277,7 @@ __device__ __forceinline__ void store_row_chunk(const float (&v)[32], const Hgem
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        if (row0 < p.M && col0 < p.N) tma_store_2d(tm_c, stage, col0, row0);
+        if (row0 < p.M && col0 < p.N) tma_store_3d(tm_c, stage, col0, row0, batch);
         bulk_commit();
     }
 }
@@ -300,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int kBnTile = SWAP ? kBM : BN;  // columns of C per tile
-    constexpr uint32_t kIdesc = SWAP ? umma_idesc_f16_f32(kBM, BN, 1, 0) : umma_idesc_f16_f32(kBM, BN, 0, 1);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -347,15 +358,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int k0 = kb * kBK;
                 uint8_t *a_dst = sA + stage * Cfg::kABytes;
                 uint8_t *b_dst = sB + stage * Cfg::kBBytes;
+                const int za = c.batch * p.za, zb = c.batch * p.zb;
                 if constexpr (!SWAP) {
-                    tma_load_2d(&tm_a, &full[stage], a_dst, k0, c.m0);
+                    tma_load_3d(&tm_a, &full[stage], a_dst, k0, c.m0, za);
+                    if (p.b_kmajor) {
+                        tma_load_3d(&tm_b, &full[stage], b_dst, k0, c.n0, zb);  // BN rows of 64 k
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j) tma_load_2d(&tm_b, &full[stage], b_dst + j * 8192, c.n0 + 64 * j, k0);
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_3d(&tm_b, &full[stage], b_dst + j * 8192, c.n0 + 64 * j, k0, zb);
+                    }
                 } else {
-                    // MMA operand A = B^T (N rows, MN-major), operand B = A (M rows, K-major).
-                    tma_load_2d(&tm_b, &full[stage], a_dst, c.n0, k0);
-                    tma_load_2d(&tm_b, &full[stage], a_dst + 8192, c.n0 + 64, k0);
-                    tma_load_2d(&tm_a, &full[stage], b_dst, k0, 0);
+                    // MMA operand A = B^T (N rows; MN-major, or K-major when B
+                    // is stored N x K), operand B = A (M rows, K-major).
+                    if (p.b_kmajor) {
+                        tma_load_3d(&tm_b, &full[stage], a_dst, k0, c.n0, zb);
+                    } else {
+                        tma_load_3d(&tm_b, &full[stage], a_dst, c.n0, k0, zb);
+                        tma_load_3d(&tm_b, &full[stage], a_dst + 8192, c.n0 + 64, k0, zb);
+                    }
+                    tma_load_3d(&tm_a, &full[stage], b_dst, k0, 0, za);
                 }
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -393,15 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
                 for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                    uint64_t adesc, bdesc;
-                    if constexpr (!SWAP) {
-                        adesc = umma_desc_sw128(a_addr + kk * 32, 16, 1024);      // K-major: +32 B per k16
-                        bdesc = umma_desc_sw128(b_addr + kk * 2048, 8192, 1024);  // MN-major: +2 k-groups
-                    } else {
-                        adesc = umma_desc_sw128(a_addr + kk * 2048, 8192, 1024);
-                        bdesc = umma_desc_sw128(b_addr + kk * 32, 16, 1024);
-                    }
-                    umma_f16(d_tmem, adesc, bdesc, kIdesc | p.idesc_fmt, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+                    // K-major: +32 B per k16; MN-major: +2 k-groups of 8 rows.
+                    const uint64_t kdesc = umma_desc_sw128((SWAP ? b_addr : a_addr) + kk * 32, 16, 1024);
+                    const uint32_t o_addr = SWAP ? a_addr : b_addr;  // the operand holding B
+                    const uint64_t odesc = p.b_kmajor ? umma_desc_sw128(o_addr + kk * 32, 16, 1024)
+                                                      : umma_desc_sw128(o_addr + kk * 2048, 8192, 1024);
+                    const uint64_t adesc = SWAP ? odesc : kdesc;
+                    const uint64_t bdesc = SWAP ? kdesc : odesc;
+                    umma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
                 if (++stage == STAGES) {
@@ -438,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A unit leaves a partial tile when K is split evenly (splits > 1) or
             // when it covers only part of a stream-K tile (slot >= 0).
             const bool partial = (p.splits > 1) || (c.slot >= 0);
+            const size_t cbase = static_cast<size_t>(c.batch) * static_cast<size_t>(p.stride_c);
             float *part = nullptr;
             if (partial)
                 part = p.ws + (c.slot >= 0 ? static_cast<size_t>(c.slot)
@@ -460,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (!SWAP) {
                     const int grow = c.m0 + row_in_tile;
                     const int col0 = c.n0 + ch * 32;
-                    epilogue_row_chunk(v, p, grow, col0);
-                    store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0);
+                    epilogue_row_chunk(v, p, grow, col0, cbase);
+                    store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
                 } else {
                     // transposed: this thread owns column n of C, registers walk rows m
                     const int gn = c.n0 + row_in_tile;
@@ -471,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j) {
                             const int gm = ch * 32 + j;
                             if (gm < p.M) {
-                                const size_t ci = static_cast<size_t>(gm) * p.N + gn;
+                                const size_t ci = cbase + static_cast<size_t>(gm) * p.N + gn;
                                 const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
                                 store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
                             }
@@ -561,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (!SWAP) {
                             const int grow = c.m0 + row_in_tile;
                             const int col0 = c.n0 + ch * 32;
-                            epilogue_row_chunk(v, p, grow, col0);
-                            store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0);
+                            epilogue_row_chunk(v, p, grow, col0, cbase);
+                            store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
                         } else {
                             const int gn = c.n0 + row_in_tile;
                             if (gn < p.N) {
@@ -571,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = 0; j < 32; ++j) {
                                     const int gm = ch * 32 + j;
                                     if (gm < p.M) {
-                                        const size_t ci = static_cast<size_t>(gm) * p.N + gn;
+                                        const size_t ci = cbase + static_cast<size_t>(gm) * p.N + gn;
                                         const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
                                         store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
                                     }
@@ -634,9 +656,12 @@ struct HgemmPairCfg {
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
 };
 
-// Pair tile t -> (first row of the pair, first column), grouped raster of 4
-// pair rows per sweep over N.
-__device__ __forceinline__ void pair_tile_origin(const HgemmArgs &p, int t, int bn, int &m0, int &n0) {
+// Pair tile t (over the whole batch) -> (matrix index, first row of the
+// pair, first column), grouped raster of 4 pair rows per sweep over N.
+__device__ __forceinline__ void pair_tile_origin(const HgemmArgs &p, int t, int bn, int &m0, int &n0, int &batch) {
+    const int per = p.tiles_m * p.tiles_n;
+    batch = t / per;
+    t -= batch * per;
     const int group_tiles = 4 * p.tiles_n;
     const int first_m = (t / group_tiles) * 4;
     const int gsz = min(p.tiles_m - first_m, 4);
@@ -669,7 +694,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
-    constexpr uint32_t kIdesc = umma_idesc_f16_f32(2 * kBM, BN, 0, 1);
+    // Bytes each CTA stages per k block: its A rows and its half of B (64-column
+    // boxes when B is K x N; exactly BN/2 rows of 64 k when B is N x K).
+    const uint32_t stage_tx = Cfg::kABytes + (p.b_kmajor ? Cfg::kBHalf * kBK * 2 : Cfg::kBBytes);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -705,10 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         for (int t = cid; t < p.units && !*abort_flag; t += ncl) {
-            int m0, n0;
-            pair_tile_origin(p, t, BN, m0, n0);
+            int m0, n0, bz;
+            pair_tile_origin(p, t, BN, m0, n0, bz);
             const int my_m = m0 + static_cast<int>(rank) * kBM;
             const int my_n = n0 + static_cast<int>(rank) * Cfg::kBHalf;
+            const int za = bz * p.za, zb = bz * p.zb;
             bool ok = true;
             for (int kb = 0; kb < p.kb_total; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u)) {
@@ -716,13 +744,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
+                if (leader) mbar_arrive_expect_tx(&full[stage], 2 * stage_tx);
                 const uint32_t full_even = mapa_shared(smem_u32(&full[stage]), 0);
                 const int k0 = kb * kBK;
-                tma_load_2d_pair(&tm_a, full_even, sA + stage * Cfg::kABytes, k0, my_m);
+                tma_load_3d_pair(&tm_a, full_even, sA + stage * Cfg::kABytes, k0, my_m, za);
+                if (p.b_kmajor) {
+                    tma_load_3d_pair(&tm_b, full_even, sB + stage * Cfg::kBBytes, k0, my_n, zb);
+                } else {
 #pragma unroll
-                for (int j = 0; j < Cfg::kBBoxes; ++j)
-                    tma_load_2d_pair(&tm_b, full_even, sB + stage * Cfg::kBBytes + j * 8192, my_n + 64 * j, k0);
+                    for (int j = 0; j < Cfg::kBBoxes; ++j)
+                        tma_load_3d_pair(&tm_b, full_even, sB + stage * Cfg::kBBytes + j * 8192, my_n + 64 * j, k0,
+                                         zb);
+                }
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) {
@@ -757,10 +790,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a_addr = smem_u32(sA + stage * Cfg::kABytes);
                 const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
-                for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-                    umma_f16_pair(d_tmem, umma_desc_sw128(a_addr + kk * 32, 16, 1024),
-                                  umma_desc_sw128(b_addr + kk * 2048, 8192, 1024), kIdesc | p.idesc_fmt,
+                for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                    const uint64_t bdesc = p.b_kmajor ? umma_desc_sw128(b_addr + kk * 32, 16, 1024)
+                                                      : umma_desc_sw128(b_addr + kk * 2048, 8192, 1024);
+                    umma_f16_pair(d_tmem, umma_desc_sw128(a_addr + kk * 32, 16, 1024), bdesc, p.idesc,
                                   (kb > 0 || kk > 0) ? 1u : 0u);
+                }
                 umma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
                 if (++stage == STAGES) {
                     stage = 0;
@@ -781,9 +816,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t n_staged = 0;
         int local = 0;
         for (int t = cid; t < p.units && !*abort_flag; t += ncl, ++local) {
-            int m0, n0;
-            pair_tile_origin(p, t, BN, m0, n0);
+            int m0, n0, bz;
+            pair_tile_origin(p, t, BN, m0, n0, bz);
             const int my_m = m0 + static_cast<int>(rank) * kBM;
+            const size_t cbase = static_cast<size_t>(bz) * static_cast<size_t>(p.stride_c);
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait(&tfull[buf], acc_phase)) {
@@ -802,8 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                epilogue_row_chunk(v, p, grow, col0);
-                store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0);
+                epilogue_row_chunk(v, p, grow, col0, cbase);
+                store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0, bz);
             }
             tc_fence_before();
             __syncwarp();
@@ -853,28 +889,42 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int elem_bytes, const void *base, uint64_t inner,
-               uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+// A strided batch of `depth` row-major matrices (outer rows of inner
+// elements, rows row_stride apart, matrices mat_stride apart; elements).
+// With depth 1 the matrix stride is unused and set to one matrix.
+bool encode_3d(CUtensorMap *map, CUtensorMapDataType dt, int elem_bytes, const void *base, uint64_t inner,
+               uint64_t outer, uint64_t depth, uint64_t row_stride, uint64_t mat_stride, uint32_t box_inner,
+               uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = get_encoder();
     if (!enc) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {row_stride_elems * static_cast<uint64_t>(elem_bytes)};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const uint64_t eb = static_cast<uint64_t>(elem_bytes);
+    cuuint64_t dims[3] = {inner, outer, depth};
+    cuuint64_t strides[2] = {row_stride * eb, (depth > 1 ? mat_stride : row_stride * outer) * eb};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 // Store map of C: 32 x 32 boxes; FP32 rows of the box are 128 bytes (128-byte
 // swizzle), 16-bit rows 64 bytes (64-byte swizzle), matching store_row_chunk.
-bool encode_c(CUtensorMap *map, void *C, int c_type, int M, int N) {
-    if (c_type == kOutF32) return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32, 32);
+bool encode_c(CUtensorMap *map, const TcGemm &g) {
+    if (g.c_type == kOutF32)
+        return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.C, g.N, g.M, g.batch, g.N, g.stride_c, 32, 32);
     const CUtensorMapDataType dt =
-        c_type == kOutF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    return encode_2d(map, dt, 2, C, N, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+        g.c_type == kOutF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return encode_3d(map, dt, 2, g.C, g.N, g.M, g.batch, g.N, g.stride_c, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// Operand maps.  A: K x M per matrix, boxes of 64 k x `rows` rows.  B stored
+// K x N: boxes of 64 columns x 64 k; stored N x K: boxes of 64 k x `rows` rows.
+bool encode_a(CUtensorMap *map, const TcGemm &g, CUtensorMapDataType dt, uint32_t rows) {
+    return encode_3d(map, dt, 2, g.A, g.K, g.M, g.stride_a ? g.batch : 1, g.K, g.stride_a, kBK, rows);
+}
+bool encode_b(CUtensorMap *map, const TcGemm &g, CUtensorMapDataType dt, uint32_t rows) {
+    if (g.b_trans) return encode_3d(map, dt, 2, g.B, g.K, g.N, g.stride_b ? g.batch : 1, g.K, g.stride_b, kBK, rows);
+    return encode_3d(map, dt, 2, g.B, g.N, g.K, g.stride_b ? g.batch : 1, g.N, g.stride_b, 64, kBK);
 }
 
 template <int BN, int STAGES, bool SWAP>
@@ -885,7 +935,13 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, tc, a);
+    // The tile's MMA shape and operand majors: A is K-major; B is MN-major
+    // when stored K x N, K-major when stored N x K.  The transposed variant
+    // swaps the operands (B^T first).
+    HgemmArgs args = a;
+    const int b_mn = a.b_kmajor ? 0 : 1;
+    args.idesc = (SWAP ? umma_idesc_f16_f32(kBM, BN, b_mn, 0) : umma_idesc_f16_f32(kBM, BN, 0, b_mn)) | a.idesc_fmt;
+    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, tc, args);
     return cudaPeekAtLastError();
 }
 
@@ -920,40 +976,46 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     const int clusters = std::min(a.units, max_clusters);
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     *clusters_used = clusters;
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, a);
+    HgemmArgs args = a;
+    args.idesc = umma_idesc_f16_f32(2 * kBM, BN, 0, a.b_kmajor ? 0 : 1) | a.idesc_fmt;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
 
 }  // namespace
 
-cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, void *C,
-                         int c_type, const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info) {
+cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     const int sms = device_sm_count();
+    const int M = g.M, N = g.N, K = g.K;
     // FP16 and BF16 inputs share every kernel: the tensor maps carry the
     // element type and the MMA instruction descriptor the operand format.
-    const CUtensorMapDataType in_dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType in_dt = g.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     HgemmArgs a{};
-    a.idesc_fmt = bf16 ? kIdescBf16Operands : 0u;
+    a.idesc_fmt = g.bf16 ? kIdescBf16Operands : 0u;
     a.M = M;
     a.N = N;
     a.K = K;
-    a.alpha = alpha;
-    a.beta = beta;
-    a.bias = bias;
-    a.act = act;
-    a.C = C;
-    a.c_type = c_type;
+    a.alpha = g.alpha;
+    a.beta = g.beta;
+    a.bias = g.bias;
+    a.act = g.act;
+    a.C = g.C;
+    a.c_type = g.c_type;
     a.kb_total = (K + kBK - 1) / kBK;
     a.err = watchdog_word();
+    a.batch = g.batch;
+    a.za = g.stride_a ? 1 : 0;
+    a.zb = g.stride_b ? 1 : 0;
+    a.stride_c = g.stride_c;
+    a.b_kmajor = g.b_trans ? 1 : 0;
 
     // Tile table.  M <= 64: transposed product with MMA N = M rounded up to
-    // 32 or 64.  Otherwise 128 x 256 tiles (128 x 128 when N <= 128).  With
-    // at least a wave of tiles, one persistent CTA per SM takes whole tiles
-    // round-robin and the tiles of the last partial wave are shared out by
-    // k blocks (stream-K); with fewer tiles than
-    // SMs, K is split evenly.  Partial tiles are reduced in k order by the
-    // last contributor to arrive (per 32-row slice), inside the kernel.
+    // 32 or 64.  Otherwise 128 x 256 tiles (128 x 128 when N <= 128).  Every
+    // CTA is persistent and takes whole tiles round-robin (tiles of all
+    // matrices of a batch in one sequence); with fewer tiles than a third of
+    // the SMs, K is split evenly and partial tiles are reduced in k order by
+    // the last contributor to arrive (per 32-row slice), inside the kernel.
     const bool swap = M <= 64;
     int bn;
     if (swap) {
@@ -961,13 +1023,15 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     } else {
         // Few tiles of 128 x 256: 128 x 128 tiles put twice as many SMs to work
         // streaming B (measured at 128 x 11008 x 4096: 36.5 us vs 48.8 us).
-        const int t256 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
+        const long long t256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256) * g.batch;
         bn = (N > 128 && t256 >= sms / 2) ? 256 : 128;
     }
     const int bn_tile = swap ? kBM : bn;
     a.tiles_m = swap ? 1 : (M + kBM - 1) / kBM;
     a.tiles_n = (N + bn_tile - 1) / bn_tile;
-    const int tiles = a.tiles_m * a.tiles_n;
+    const long long tiles_ll = static_cast<long long>(a.tiles_m) * a.tiles_n * g.batch;
+    if (tiles_ll > (1LL << 26)) return cudaErrorNotSupported;  // keeps every unit index and counter in int
+    const int tiles = static_cast<int>(tiles_ll);
     // K is split only while the tiles fill less than a third of the SMs; the
     // memory-bound small-M shapes stream B fastest from about half the SMs
     // without the partial-tile round trip (measured: 16 x 4096 x 4096 is best
@@ -1001,23 +1065,21 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
         int best_bn = 0;
         double best_cost = 0.0;
         for (int cand : {256, 224, 192}) {
-            const int t2 = rows2 * ((N + cand - 1) / cand);
+            const long long t2 = static_cast<long long>(rows2) * ((N + cand - 1) / cand) * g.batch;
             const double cost = static_cast<double>((t2 + pairs - 1) / pairs) * (cand + 64);
             if (best_bn == 0 || cost < best_cost - 1e-9) {
                 best_bn = cand;
                 best_cost = cost;
             }
         }
-        const int t2 = rows2 * ((N + best_bn - 1) / best_bn);
+        const int t2 = rows2 * ((N + best_bn - 1) / best_bn) * g.batch;
         if (t2 * 2 >= pairs) {
             a.tiles_m = rows2;
             a.tiles_n = (N + best_bn - 1) / best_bn;
             a.splits = 1;
             a.units = t2;
             CUtensorMap ta, tb, tc;
-            if (!encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, kBM) ||
-                !encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK) ||
-                !encode_c(&tc, C, c_type, M, N))
+            if (!encode_a(&ta, g, in_dt, kBM) || !encode_b(&tb, g, in_dt, best_bn / 2) || !encode_c(&tc, g))
                 return cudaErrorNotSupported;
             int used = 0;
             cudaError_t e;
@@ -1060,12 +1122,12 @@ cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const 
     std::memset(&tc, 0, sizeof(tc));
     bool ok = true;
     if (!swap) {
-        ok = ok && encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, kBM);
-        ok = ok && encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK);
-        ok = ok && encode_c(&tc, C, c_type, M, N);
+        ok = ok && encode_a(&ta, g, in_dt, kBM);
+        ok = ok && encode_b(&tb, g, in_dt, bn);
+        ok = ok && encode_c(&tc, g);
     } else {
-        ok = ok && encode_2d(&ta, in_dt, 2, A, K, M, K, kBK, bn);
-        ok = ok && encode_2d(&tb, in_dt, 2, B, N, K, N, 64, kBK);
+        ok = ok && encode_a(&ta, g, in_dt, bn);
+        ok = ok && encode_b(&tb, g, in_dt, kBM);
         tc = tb;  // unused by the transposed variant
     }
     if (!ok) return cudaErrorNotSupported;
@@ -1150,6 +1212,9 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
     a.C = C;
     a.kb_total = (K + kBK - 1) / kBK;
     a.err = watchdog_word();
+    a.batch = 1;
+    a.za = a.zb = 0;
+    a.stride_c = static_cast<long long>(M) * N;
     const int bn = M <= 32 ? 32 : 64;
     a.tiles_m = 1;
     a.tiles_n = (N + kBM - 1) / kBM;
@@ -1172,9 +1237,14 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
         a.ws = partials;
         a.counters = counters;
     }
+    TcGemm g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.A = A;
+    g.B = B;
     CUtensorMap ta, tb;
-    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, K, kBK, bn) ||
-        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, N, 64, kBK))
+    if (!encode_a(&ta, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bn) || !encode_b(&tb, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kBM))
         return cudaErrorNotSupported;
     const int grid = std::min(a.units, sms);
     if (bn == 32) {

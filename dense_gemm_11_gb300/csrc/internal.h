@@ -55,11 +55,30 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
 // ---- FP16 tensor-core path (hgemm.cu) ----
 // Returns cudaSuccess, or cudaErrorNotSupported when the tensor-map encoder
 // is unavailable.
-// A and B are FP16 (bf16 == false) or BF16 (bf16 == true); C is FP32, FP16
-// or BF16 (c_type: 0, 1, 2 -- the C ABI's gemm_dtype codes).  The plans are
-// the same for every combination.
-cudaError_t run_gemm_f16(int M, int N, int K, float alpha, const void *A, const void *B, float beta, void *C,
-                         int c_type, const float *bias, int act, bool bf16, cudaStream_t stream, CallInfo *info);
+// One tensor-core GEMM or a strided batch of them, every matrix row-major:
+//   C_z = act(alpha * A_z * op(B_z) + beta * C_z + bias),  z < batch,
+// A_z = A + z * stride_a (M x K), B_z = B + z * stride_b (K x N, or N x K
+// with b_trans, op(B) = B^T), C_z = C + z * stride_c (M x N); strides in
+// elements, 0 for an operand shared by the whole batch.  A and B are FP16
+// (bf16 == false) or BF16 (bf16 == true); C is FP32, FP16 or BF16 (c_type:
+// 0, 1, 2 -- the C ABI's gemm_dtype codes).  Every combination uses the same
+// kernels and plans.
+struct TcGemm {
+    int batch = 1, M = 0, N = 0, K = 0;
+    float alpha = 1.f, beta = 0.f;
+    const void *A = nullptr;
+    long long stride_a = 0;
+    const void *B = nullptr;
+    long long stride_b = 0;
+    int b_trans = 0;
+    void *C = nullptr;
+    long long stride_c = 0;
+    int c_type = 0;
+    const float *bias = nullptr;
+    int act = 0;
+    bool bf16 = false;
+};
+cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info);
 
 // The same small-M (M <= 64) transposed split-K plan with its scratch in a
 // fixed device array (no allocation).  *reject = 1 if M > 64, 2 if the plan's
@@ -72,9 +91,11 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
 // bias/act applied when given (the FP16 path), in sgemm.cu.
 cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float *bias, int act,
                         cudaStream_t stream, CallInfo *info);
-// The same for a 16-bit C (c_type 1 = FP16, 2 = BF16; ldc = N): the value is
-// computed in FP32 and rounded once to nearest even.
-cudaError_t run_scale_c16(int M, int N, float beta, void *C, int c_type, const float *bias, int act,
-                          cudaStream_t stream, CallInfo *info);
+// The same over a strided batch of `batch` M x N matrices (ldc = N, matrices
+// stride_c elements apart) of any output type (c_type 0 = FP32, 1 = FP16,
+// 2 = BF16; a 16-bit value is computed in FP32 and rounded once to nearest
+// even).
+cudaError_t run_scale_c_batched(int batch, int M, int N, float beta, void *C, long long stride_c, int c_type,
+                                const float *bias, int act, cudaStream_t stream, CallInfo *info);
 
 }  // namespace gemm11

@@ -704,15 +704,19 @@ __global__ void scale_c_kernel(int M, int N, float beta, float *C, int ldc, cons
     }
 }
 
-// The same with a 16-bit C (ldc = N); c_type as in load_out / store_out.
-__global__ void scale_c16_kernel(int M, int N, float beta, void *C, int c_type, const float *bias, int act) {
-    const long long total = static_cast<long long>(M) * N;
+// The same over a strided batch of M x N matrices (ldc = N) of any output
+// type (c_type as in load_out / store_out).
+__global__ void scale_c_batched_kernel(int M, int N, long long total, float beta, void *C, long long stride_c,
+                                       int c_type, const float *bias, int act) {
+    const long long mn = static_cast<long long>(M) * N;
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int j = static_cast<int>(e % N);
-        float v = beta != 0.f ? beta * load_out(C, static_cast<size_t>(e), c_type) : 0.f;
+        const long long z = e / mn, r = e - z * mn;
+        const int j = static_cast<int>(r % N);
+        const size_t idx = static_cast<size_t>(z * stride_c + r);
+        float v = beta != 0.f ? beta * load_out(C, idx, c_type) : 0.f;
         if (bias) v += bias[j];
-        store_out(C, static_cast<size_t>(e), c_type, apply_activation(act, v));
+        store_out(C, idx, c_type, apply_activation(act, v));
     }
 }
 
@@ -760,17 +764,17 @@ cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float
     return cudaPeekAtLastError();
 }
 
-cudaError_t run_scale_c16(int M, int N, float beta, void *C, int c_type, const float *bias, int act,
-                          cudaStream_t stream, CallInfo *info) {
+cudaError_t run_scale_c_batched(int batch, int M, int N, float beta, void *C, long long stride_c, int c_type,
+                                const float *bias, int act, cudaStream_t stream, CallInfo *info) {
     if (beta == 1.f && !bias && act == 0) {
         info->plan = "noop_beta1";
         info->launches = 0;
         return cudaSuccess;
     }
-    const long long total = static_cast<long long>(M) * N;
+    const long long total = static_cast<long long>(batch) * M * N;
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4LL * device_sm_count()));
-    scale_c16_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, c_type, bias, act);
-    info->plan = "scale_c16";
+    scale_c_batched_kernel<<<blocks, 256, 0, stream>>>(M, N, total, beta, C, stride_c, c_type, bias, act);
+    info->plan = "scale_c_batched";
     info->launches = 1;
     return cudaPeekAtLastError();
 }

@@ -43,10 +43,13 @@ class Workload:
     bias: bool = False   # 16-bit inputs only: bias ~ N(0, 0.1), fp32, length N
     act: int = 0         # 0 none, 1 exact GELU, 2 ReLU, 3 tanh GELU
     note: str = ""
+    batch: int = 1       # > 1: a strided batch of independent GEMMs
+    b_trans: bool = False  # B stored N x K (op(B) = B^T)
+    out: str = "f32"     # element type of C: f32, f16 or bf16
 
     @property
     def flops(self) -> int:
-        return 2 * self.M * self.N * self.K
+        return 2 * self.batch * self.M * self.N * self.K
 
 
 SWEEP_SIZES = (128, 256, 512, 1024, 2048, 4096)
@@ -80,6 +83,16 @@ def _registry():
         w[f"bf16_epi{i}"] = Workload(f"bf16_epi{i}", "bf16", m, n, k, 0.5, 0.0, "normal_k", 12 + i,
                                      bias=True, act=act,
                                      note=f"BF16 {'ReLU' if act == 2 else 'tanh-GELU'}(0.5*A*B+bias) {m}x{n}x{k}")
+    w["f16_4096_out16"] = Workload("f16_4096_out16", "f16", 4096, 4096, 4096, 1.0, 0.0, "normal_k", 16,
+                                   out="f16", note="FP16-in FP32-acc 4096^3, FP16 C")
+    # Attention products per head (32 = batch 4 x 8 heads, sequence 2048, head
+    # dimension 128): scores Q K^T / sqrt(d) with the keys stored S x d, and
+    # P V; BF16 in and out.  P is a stand-in drawn like the other operands.
+    w["bf16_attn_qk"] = Workload("bf16_attn_qk", "bf16", 2048, 2048, 128, 128 ** -0.5, 0.0, "normal", 17,
+                                 batch=32, b_trans=True, out="bf16",
+                                 note="32 x (2048x128) (2048x128)^T / sqrt(128), BF16 in/out")
+    w["bf16_attn_pv"] = Workload("bf16_attn_pv", "bf16", 2048, 128, 2048, 1.0, 0.0, "normal_k", 18,
+                                 batch=32, out="bf16", note="32 x (2048x2048) (2048x128), BF16 in/out")
     return w
 
 
@@ -148,5 +161,26 @@ def make(M, N, K, *, kind="f32", dist="uniform", seed=0, beta=0.0, bias=False,
     return out
 
 
+def make_batched(batch, M, N, K, *, kind="f16", dist="normal_k", seed=0, beta=0.0, bias=False, b_trans=False):
+    """Draw a strided batch: A (batch, M, K), B (batch, K, N) -- or
+    (batch, N, K) with b_trans, the layout of attention keys -- C
+    (batch, M, N) and bias (N); same recipe and draw order as make()."""
+    rng = np.random.default_rng(seed)
+    A = _cast_input(_draw(rng, dist, (batch, M, K), K), kind)
+    B = _cast_input(_draw(rng, dist, (batch, N, K) if b_trans else (batch, K, N), K), kind)
+    if beta != 0.0:
+        Cdist = "uniform" if dist in ("uniform", "normal_k") else dist
+        C = _draw(rng, Cdist, (batch, M, N), K).astype(np.float32)
+    else:
+        C = np.full((batch, M, N), np.nan, dtype=np.float32)
+    out = {"A": A, "B": B, "C": C}
+    if bias:
+        out["bias"] = rng.normal(0.0, 0.1, size=(N,)).astype(np.float32)
+    return out
+
+
 def make_workload(w: Workload):
+    if w.batch > 1 or w.b_trans:
+        return make_batched(w.batch, w.M, w.N, w.K, kind=w.kind, dist=w.dist, seed=w.seed, beta=w.beta,
+                            bias=w.bias, b_trans=w.b_trans)
     return make(w.M, w.N, w.K, kind=w.kind, dist=w.dist, seed=w.seed, beta=w.beta, bias=w.bias)

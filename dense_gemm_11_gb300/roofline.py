@@ -12,14 +12,15 @@ The epilogue's O(M*N) operations are not counted as flops, as on the pages.
 from __future__ import annotations
 
 
-def gemm_flops(M: int, N: int, K: int) -> int:
-    return 2 * M * N * K
+def gemm_flops(M: int, N: int, K: int, batch: int = 1) -> int:
+    return 2 * batch * M * N * K
 
 
 def gemm_bytes(M: int, N: int, K: int, *, in_bytes: int, beta_nonzero: bool,
-               bias: bool = False, out_bytes: int = 4) -> int:
-    """Minimum bytes a GEMM must move: A and B once, C written (and read if beta != 0)."""
-    b = in_bytes * (M * K + K * N) + out_bytes * M * N * (2 if beta_nonzero else 1)
+               bias: bool = False, out_bytes: int = 4, batch: int = 1) -> int:
+    """Minimum bytes a GEMM (or each of `batch` independent ones) must move:
+    A and B once, C written (and read if beta != 0), the bias once."""
+    b = batch * (in_bytes * (M * K + K * N) + out_bytes * M * N * (2 if beta_nonzero else 1))
     if bias:
         b += 4 * N
     return b

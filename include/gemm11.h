@@ -147,6 +147,33 @@ GEMM11_API int gemm_tc_f32acc_epilogue(int M, int N, int K, float alpha, const v
                                        float beta, void *C, int c_type, const float *bias, int act, void *stream);
 
 /*
+ * gemm_tc_strided_batched -- `batch` independent tensor-core GEMMs in one
+ * launch, each the operation of gemm_tc_f32acc_epilogue:
+ *   C_z = round_c( act( alpha * A_z * op(B_z) + beta * C_z + bias ) ),  0 <= z < batch
+ *   A_z = A + z * stride_a   M x K, row-major
+ *   B_z = B + z * stride_b   K x N row-major (b_trans = 0, op(B) = B) or
+ *                            N x K row-major (b_trans = 1, op(B) = B^T)
+ *   C_z = C + z * stride_c   M x N, row-major
+ * Strides count elements of the operand's type.  stride_a or stride_b may be
+ * 0 (one matrix shared by the whole batch); stride_c >= M * N (the outputs
+ * must not overlap).  bias (length N) is shared by every matrix.  The pages
+ * name attention as the consumer of such products: "第24讲 ... GEMM 分块与
+ * Tensor Core 思维" (its opening guide: QK^T and PV are GEMMs) and the DeepGEMM
+ * essay "企业官网建设流程全解析" (section 1.1: projections, attention and FFN
+ * are GEMMs); QK^T is the b_trans = 1 form (K stored row-major, S x d).
+ * Alignment, as for the single GEMM: A, B, C 16-byte aligned, K % 8 == 0,
+ * N % 8 == 0, and for batch > 1 every stride % 8 == 0; otherwise
+ * GEMM_ERR_UNSUPPORTED.  batch < 0, b_trans not 0/1, a negative stride or
+ * stride_c < M * N (batch > 1) return GEMM_ERR_INVALID_ARG; batch == 0 is a
+ * no-op.  The tiles of all matrices form one persistent schedule (one launch
+ * for the whole batch).
+ */
+GEMM11_API int gemm_tc_strided_batched(int batch, int M, int N, int K, float alpha, const void *A, long long stride_a,
+                                       const void *B, long long stride_b, int ab_type, int b_trans, float beta,
+                                       void *C, long long stride_c, int c_type, const float *bias, int act,
+                                       void *stream);
+
+/*
  * gemm_f16_f32acc_epilogue_noalloc -- the same operation and arguments as
  * gemm_f16_f32acc_epilogue, restricted to M <= 64, and guaranteed not to
  * allocate: no cudaMalloc, cudaFree or allocating library routine is called.

@@ -88,6 +88,25 @@ def test_tc_rejects_bad_types(L):
     assert g.gemm_tc_raw(8, 12, 8, 1.0, FAKE, FAKE, 1, 0.0, FAKE, 2) == g.GEMM_ERR_UNSUPPORTED
 
 
+def test_batched_rejects_bad_args(L):
+    f = g.gemm_tc_batched_raw
+    ok = dict(stride_a=64, stride_b=64, stride_c=64)
+    args = lambda **kw: {**dict(batch=2, M=8, N=8, K=8, alpha=1.0, A_ptr=FAKE, B_ptr=FAKE, ab_type=1, b_trans=0,
+                                beta=0.0, C_ptr=FAKE, c_type=0), **ok, **kw}
+    assert f(**args(batch=-1)) == g.GEMM_ERR_INVALID_ARG
+    assert f(**args(b_trans=2)) == g.GEMM_ERR_INVALID_ARG
+    assert f(**args(stride_a=-8)) == g.GEMM_ERR_INVALID_ARG
+    assert f(**args(stride_c=56)) == g.GEMM_ERR_INVALID_ARG      # outputs overlap
+    assert f(**args(ab_type=0)) == g.GEMM_ERR_INVALID_ARG
+    assert f(**args(act=9)) == g.GEMM_ERR_INVALID_ARG
+    assert f(**args(A_ptr=0)) == g.GEMM_ERR_INVALID_ARG
+    assert f(**args(stride_b=68)) == g.GEMM_ERR_UNSUPPORTED      # 16-byte matrix starts
+    assert f(**args(stride_c=68)) == g.GEMM_ERR_UNSUPPORTED
+    assert f(**args(K=12, stride_a=96, stride_b=96)) == g.GEMM_ERR_UNSUPPORTED
+    assert f(**args(batch=0)) == g.GEMM_OK and g.last_launch_count() == 0
+    assert f(**args(M=0)) == g.GEMM_OK
+
+
 def test_dtype_codes_match_the_header():
     text = open(HEADER).read()
     for name in ("GEMM_DTYPE_F32", "GEMM_DTYPE_F16", "GEMM_DTYPE_BF16"):

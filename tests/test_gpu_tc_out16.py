@@ -89,7 +89,7 @@ def test_out16_alpha_zero_epilogue_only(out, act):
     C = torch.from_numpy(C0.astype(np.float32)).to(TORCH_T[out]).to(DEV)
     g.gemm_tc(A, B, C, alpha=0.0, beta=-1.5, bias=torch.from_numpy(bias).to(DEV), act=act)
     torch.cuda.synchronize()
-    assert g.last_plan() == "scale_c16"
+    assert g.last_plan() == "scale_c_batched"
     ref, S = oracle.gemm(np.zeros((33, 16)), np.zeros((16, 24)), C0, alpha=0.0, beta=-1.5, bias=bias, act=act)
     assert_within(C.float().cpu().numpy(), ref, S, 1e-6, f"alpha=0 {out} act={act}", out=out)
 
