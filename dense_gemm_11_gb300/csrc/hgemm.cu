@@ -230,15 +230,25 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
         }
     }
     // One uniform pass per activation (the branch is taken once per chunk).
-    if (p.act == 1) {
+    // The GELU forms run as a rolled loop over four groups of 8 that rotates
+    // the register array by 8 each trip (register moves): 8 inlined copies of
+    // the function per call site instead of 32, which measured 3-4 % faster
+    // on the CTA-pair kernel (smaller code beside the MMA issuer's loop).
+    if (p.act == 2) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = apply_activation(1, v[j]);
-    } else if (p.act == 2) {
+        for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.f);
+    } else if (p.act == 1 || p.act == 3) {
+        const int act = p.act;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float t[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = apply_activation(2, v[j]);
-    } else if (p.act == 3) {
+            for (int i = 0; i < 8; ++i) t[i] = act == 1 ? gelu_erf(v[i]) : gelu_tanh(v[i]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = apply_activation(3, v[j]);
+            for (int i = 0; i < 24; ++i) v[i] = v[i + 8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[24 + i] = t[i];
+        }
     }
 }
 
@@ -248,13 +258,21 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
 // 64-byte rows, 64-byte swizzle (chunk c of row r at c ^ ((r >> 1) & 3)).
 // Both patterns put the 32 lanes' 16-byte writes on distinct banks per
 // quarter warp.  One bulk group is committed per chunk (possibly empty), so
-// waiting for all but the newest group frees the buffer about to be reused.
+// with two buffers waiting for all but the newest group frees the buffer
+// about to be reused (with one buffer: waiting for all groups).
+template <int NBUF = 2>
 __device__ __forceinline__ void store_row_chunk(const float (&v)[32], const HgemmArgs &p, const CUtensorMap *tm_c,
                                                 uint8_t *stage_base, uint32_t &n_staged, int lane, int row0,
                                                 int col0, int batch) {
-    uint8_t *stage = stage_base + (n_staged & 1u) * 4096;
+    static_assert(NBUF == 1 || NBUF == 2, "one or two staging buffers per warp");
+    uint8_t *stage = stage_base + (NBUF == 2 ? (n_staged & 1u) * 4096 : 0u);
     ++n_staged;
-    if (lane == 0) bulk_wait_read_all_but_one();
+    if (lane == 0) {
+        if (NBUF == 2)
+            bulk_wait_read_all_but_one();
+        else
+            bulk_wait_read_all();
+    }
     __syncwarp();
     if (p.c_type == kOutF32) {
         float *st = reinterpret_cast<float *>(stage) + lane * 32;
@@ -641,18 +659,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the MMA thread's commits arrive on both CTAs' "empty" and "accumulator
 // full" barriers (multicast); both CTAs' epilogue warps arrive on the even
 // CTA's "accumulator empty" barrier.
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI>
 struct HgemmPairCfg {
+    static constexpr int kNBuf = EPI == 4 ? 2 : 1;    // 4 KB staging buffers per epilogue warp
+    static constexpr int kThreadsPair = 64 + 32 * EPI;
     static constexpr int kABytes = kBM * kBK * 2;  // this CTA's 128 rows
     static constexpr int kBHalf = BN / 2;          // this CTA's columns of B
     static constexpr int kBBoxes = (kBHalf + 63) / 64;
     static constexpr int kBBytes = kBBoxes * 64 * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kCStageBytes = kEpiWarps * 2 * 32 * 32 * 4;  // 2 x 4 KB per warp
+    static constexpr int kCStageBytes = EPI * kNBuf * 32 * 32 * 4;
     static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
     static constexpr int kTmemCols = tmem_cols_for(BN);
     static_assert(BN % 32 == 0 && BN <= 256 && kBHalf % 16 == 0, "pair MMA N");
+    static_assert(EPI == 4 || EPI == 8, "epilogue warps");
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
 };
 
@@ -669,11 +690,11 @@ __device__ __forceinline__ void pair_tile_origin(const HgemmArgs &p, int t, int 
     n0 = ((t % group_tiles) / gsz) * bn;
 }
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(64 + 32 * EPI, 1)
     hgemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_c, const HgemmArgs p) {
-    using Cfg = HgemmPairCfg<BN, STAGES>;
+    using Cfg = HgemmPairCfg<BN, STAGES, EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -705,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 2 * kEpiWarps);
+            mbar_init(&tempty[b], 2 * EPI);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -807,12 +828,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue warps (both CTAs)
+        // Warp w reads TMEM lane quarter w % 4.  With 8 epilogue warps two
+        // warps share a quarter and take alternate 32-column chunks.  Four
+        // warps use two 4 KB staging buffers each, alternately (a chunk's
+        // shared-memory writes only wait for the TMA store issued two chunks
+        // earlier); eight warps one each.
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
-        // Two 4 KB staging buffers per warp used alternately (running chunk
-        // count), so a chunk's shared-memory writes only wait for the TMA
-        // store issued two chunks earlier.
-        uint8_t *const stage_base = sC + (warp - 2) * 8192;
+        const int ch_first = (warp - 2) >> 2, ch_step = EPI / 4;
+        uint8_t *const stage_base = sC + (warp - 2) * (Cfg::kNBuf * 4096);
         uint32_t n_staged = 0;
         int local = 0;
         for (int t = cid; t < p.units && !*abort_flag; t += ncl, ++local) {
@@ -830,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
             const int grow = my_m + row_in_tile;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = ch_first; ch < BN / 32; ch += ch_step) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_row + ch * 32, r);
                 tmem_wait_ld();
@@ -839,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 epilogue_row_chunk(v, p, grow, col0, cbase);
-                store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0, bz);
+                store_row_chunk<Cfg::kNBuf>(v, p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0, bz);
             }
             tc_fence_before();
             __syncwarp();
@@ -945,11 +969,11 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     return cudaPeekAtLastError();
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI>
 cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const HgemmArgs &a,
                               cudaStream_t stream, int *clusters_used) {
-    using Cfg = HgemmPairCfg<BN, STAGES>;
-    auto kern = hgemm_tc_pair_kernel<BN, STAGES>;
+    using Cfg = HgemmPairCfg<BN, STAGES, EPI>;
+    auto kern = hgemm_tc_pair_kernel<BN, STAGES, EPI>;
     static int max_clusters = -1;  // per instantiation; one device type per process
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set);
@@ -960,7 +984,7 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreadsPair, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1083,14 +1107,17 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
                 return cudaErrorNotSupported;
             int used = 0;
             cudaError_t e;
+            // (8 epilogue warps, two per TMEM lane quarter with one staging
+            // buffer each, measured no faster: the epilogue is off the
+            // critical path.)
             if (best_bn == 256) {
-                e = launch_hgemm_pair<256, 6>(ta, tb, tc, a, stream, &used);
+                e = launch_hgemm_pair<256, 6, 4>(ta, tb, tc, a, stream, &used);
                 info->plan = "tc_pair_256x256";
             } else if (best_bn == 224) {
-                e = launch_hgemm_pair<224, 6>(ta, tb, tc, a, stream, &used);
+                e = launch_hgemm_pair<224, 6, 4>(ta, tb, tc, a, stream, &used);
                 info->plan = "tc_pair_256x224";
             } else {
-                e = launch_hgemm_pair<192, 6>(ta, tb, tc, a, stream, &used);
+                e = launch_hgemm_pair<192, 6, 4>(ta, tb, tc, a, stream, &used);
                 info->plan = "tc_pair_256x192";
             }
             info->launches = 1;

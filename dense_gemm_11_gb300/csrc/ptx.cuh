@@ -28,13 +28,54 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------- epilogue activations
-// 0 identity, 1 exact GELU x*Phi(x) (erff), 2 ReLU, 3 tanh-approximate GELU
-// 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) (tanhf).
+// 0 identity, 1 exact GELU x * Phi(x), 2 ReLU, 3 tanh-approximate GELU
+// 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+//
+// Both GELU forms are written with one exponential (__expf) and one
+// approximate reciprocal (rcp.approx) instead of the library's erff / tanhf.
+// Epilogue arithmetic slows the tensor-core pipeline beside it (the SM clock
+// is higher, not lower, when it runs), so fewer instructions per element pay:
+// FP16 4096 x 11008 x 4096 with exact GELU measured 295 us against 310 us
+// with erff and 313 us with a correctly rounded reciprocal (identity: 268 us;
+// same GB300, CUDA-graph replays).
+//
+// Exact GELU: Phi(x) = 1 - Q(x) for x >= 0 and Q(|x|) for x < 0, with the
+// upper tail Q(x) = erfc(x / sqrt 2) / 2 taken from Abramowitz & Stegun,
+// Handbook of Mathematical Functions, formula 7.1.26 (Hastings):
+//   erfc(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2) + e(z),
+//   t = 1 / (1 + p z),  |e(z)| <= 1.5e-7 for z >= 0,
+//   p = 0.3275911, a1..a5 = 0.254829592, -0.284496736, 1.421413741,
+//   -1.453152027, 1.061405429.
+// So |GELU error| <= 0.75e-7 |x| plus FP32 rounding and the few-ulp errors
+// of __expf and rcp.approx.
+// 1 / x to about 1 ulp (PTX rcp.approx.ftz.f32; 1 / inf = 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float gelu_erf(float x) {
+    const float z = fabsf(x) * 0.70710678118654752f;
+    const float t = rcp_approx(fmaf(0.3275911f, z, 1.f));
+    float poly = fmaf(1.061405429f, t, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    const float q = 0.5f * poly * t * __expf(-z * z);  // Q(|x|)
+    return x * (x >= 0.f ? 1.f - q : q);
+}
+// tanh-approximate GELU through the identity 0.5 (1 + tanh u) = 1 / (1 + exp(-2u)):
+// x / (1 + exp(-2u)), u = sqrt(2/pi) (x + 0.044715 x^3).  exp overflow
+// (x very negative) gives x * 0 = -0, underflow x.
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float u = 0.79788456080286536f * fmaf(0.044715f * x, x * x, x);
+    return x * rcp_approx(1.f + __expf(-2.f * u));
+}
 __device__ __forceinline__ float apply_activation(int act, float v) {
     switch (act) {
-        case 1: return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+        case 1: return gelu_erf(v);
         case 2: return fmaxf(v, 0.f);
-        case 3: return 0.5f * v * (1.f + tanhf(0.79788456080286536f * fmaf(0.044715f * v, v * v, v)));
+        case 3: return gelu_tanh(v);
         default: return v;
     }
 }

@@ -146,3 +146,20 @@ def test_f16_unaligned_bias_pointer(M, N, K):
     assert g.check() == g.GEMM_OK
     ref, S = oracle.gemm(d["A"], d["B"], None, alpha=0.5, beta=0.0, bias=d["bias"], act=1)
     assert_within(C.cpu().numpy(), ref, S, TOL_F16, f"unaligned bias [{g.last_plan()}]")
+
+
+@pytest.mark.parametrize("act", [1, 2, 3])
+def test_activation_accuracy_on_exact_preactivations(act):
+    # Small-integer operands and a dyadic alpha make every pre-activation
+    # exact in FP32 (x = k / 32, |x| up to about 7.6), so the only error left
+    # is the activation's own: held to 1e-6 |x| + 1e-7, far inside the GEMM
+    # bound.
+    M, N, K = 256, 1024, 64
+    d = inputs.make(M, N, K, kind="f16", dist="smallint", seed=40)
+    got, plan = run_f16(d, 1.0 / 32, 0.0, None, act)
+    ref, _ = oracle.gemm(d["A"], d["B"], None, alpha=1.0 / 32, act=act, with_scale=False)
+    x, _ = oracle.gemm(d["A"], d["B"], None, alpha=1.0 / 32, with_scale=False)
+    assert np.unique(x).size > 400  # a dense sweep of the range
+    err = np.abs(got.astype(np.float64) - ref)
+    bound = 1e-6 * np.abs(x) + 1e-7 if act != 2 else np.zeros_like(x)
+    assert np.all(err <= bound), f"act {act} [{plan}]: max err {err.max():.3e} at x={x.flat[np.argmax(err - bound)]}"
