@@ -407,6 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
+        // Shared-memory descriptors of stage 0; later stages and k steps only
+        // move the 14-bit start-address field (address / 16, below 2^14 for
+        // any shared-memory address), so the loop adds small constants.
+        const uint64_t k_desc0 = umma_desc_sw128(smem_u32(SWAP ? sB : sA), 16, 1024);  // K-major operand
+        const uint64_t o_desc0 = p.b_kmajor ? umma_desc_sw128(smem_u32(SWAP ? sA : sB), 16, 1024)
+                                            : umma_desc_sw128(smem_u32(SWAP ? sA : sB), 8192, 1024);
+        constexpr uint32_t k_stage = (SWAP ? Cfg::kBBytes : Cfg::kABytes) >> 4;
+        constexpr uint32_t o_stage = (SWAP ? Cfg::kABytes : Cfg::kBBytes) >> 4;
+        const uint32_t o_kstep = p.b_kmajor ? 2u : 128u;  // 32 B (K-major) or 2048 B (MN-major) per k16
         int stage = 0;
         uint32_t phase = 0;
         int local = 0;
@@ -429,15 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(sA + stage * Cfg::kABytes);
-                const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+                const uint64_t kd = k_desc0 + stage * k_stage;
+                const uint64_t od = o_desc0 + stage * o_stage;
 #pragma unroll
                 for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                    // K-major: +32 B per k16; MN-major: +2 k-groups of 8 rows.
-                    const uint64_t kdesc = umma_desc_sw128((SWAP ? b_addr : a_addr) + kk * 32, 16, 1024);
-                    const uint32_t o_addr = SWAP ? a_addr : b_addr;  // the operand holding B
-                    const uint64_t odesc = p.b_kmajor ? umma_desc_sw128(o_addr + kk * 32, 16, 1024)
-                                                      : umma_desc_sw128(o_addr + kk * 2048, 8192, 1024);
+                    const uint64_t kdesc = kd + 2u * kk;  // K-major: +32 B per k16
+                    const uint64_t odesc = od + o_kstep * kk;
                     const uint64_t adesc = SWAP ? odesc : kdesc;
                     const uint64_t bdesc = SWAP ? kdesc : odesc;
                     umma_f16(d_tmem, adesc, bdesc, p.idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
@@ -788,6 +794,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------ MMA issuer (even CTA)
+        // Descriptors of stage 0, moved by address / 16 per stage and k step.
+        const uint64_t a_desc0 = umma_desc_sw128(smem_u32(sA), 16, 1024);
+        const uint64_t b_desc0 = p.b_kmajor ? umma_desc_sw128(smem_u32(sB), 16, 1024)
+                                            : umma_desc_sw128(smem_u32(sB), 8192, 1024);
+        const uint32_t b_kstep = p.b_kmajor ? 2u : 128u;
         int stage = 0;
         uint32_t phase = 0;
         int local = 0;
@@ -808,15 +819,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(sA + stage * Cfg::kABytes);
-                const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+                const uint64_t ad = a_desc0 + stage * (Cfg::kABytes >> 4);
+                const uint64_t bd = b_desc0 + stage * (Cfg::kBBytes >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                    const uint64_t bdesc = p.b_kmajor ? umma_desc_sw128(b_addr + kk * 32, 16, 1024)
-                                                      : umma_desc_sw128(b_addr + kk * 2048, 8192, 1024);
-                    umma_f16_pair(d_tmem, umma_desc_sw128(a_addr + kk * 32, 16, 1024), bdesc, p.idesc,
-                                  (kb > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+                    umma_f16_pair(d_tmem, ad + 2u * kk, bd + b_kstep * kk, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                 umma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
                 if (++stage == STAGES) {
                     stage = 0;
