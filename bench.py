@@ -338,8 +338,8 @@ def run_ours(args, rank, world, local_rank):
 
 def _traffic_from_profiles():
     """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) from
-    profiles/traffic.json; an entry counts only while its kernel source is unchanged."""
-    import hashlib
+    profiles/traffic.json; an entry counts only while its kernel sources (the
+    .cu file and the shared PTX header) are unchanged."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     out = {}
     try:
@@ -349,12 +349,20 @@ def _traffic_from_profiles():
         return out
     for key, r in rec.items():
         try:
-            with open(os.path.join(ROOT, r["source"]), "rb") as f:
-                sha = hashlib.sha256(f.read()).hexdigest()[:16]
-            out[key] = r["bytes"] if sha == r["sha"] else None
+            out[key] = r["bytes"] if source_sha(r["sources"]) == r["sha"] else None
         except Exception:
             out[key] = None
     return out
+
+
+def source_sha(sources):
+    """First 16 hex digits of the SHA-256 of the listed source files, concatenated."""
+    import hashlib
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def run_profile_case(case: str, repeats: int):
