@@ -436,6 +436,8 @@ def run_sweep(reps: int, only=None):
                                   b_trans=w.b_trans, stream=st)
             elif w.kind == "f32":
                 g.gemm_f32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
+            elif w.kind == "f32x3":
+                g.gemm_f32_3xtf32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
             elif w.kind == "bf16":
                 g.gemm_bf16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
                                             act=w.act, stream=st)
@@ -483,17 +485,21 @@ def run_sweep(reps: int, only=None):
         del graph
         ms = statistics.median(times)
         flops = roofline.gemm_flops(w.M, w.N, w.K, w.batch)
-        nbytes = roofline.gemm_bytes(w.M, w.N, w.K, in_bytes=4 if w.kind == "f32" else 2,
+        nbytes = roofline.gemm_bytes(w.M, w.N, w.K, in_bytes=4 if w.kind in ("f32", "f32x3") else 2,
                                      beta_nonzero=w.beta != 0.0, bias=w.bias, out_bytes=4 if w.out == "f32" else 2,
                                      batch=w.batch)
-        peak = f32_peak if w.kind == "f32" else tc_peak
+        # 3 x TF32: the FP32 product's flops against the tensor core's TF32 rate
+        # (half the measured bf16 rate) divided by the three products it takes.
+        peak = f32_peak if w.kind == "f32" else (tc_peak / 2 / 3 if w.kind == "f32x3" else tc_peak)
         roof, bound = roofline.roofline_tflops(flops, nbytes, peak, hbm_gbs)
         tflops = flops / (ms_steady * 1e-3) / 1e12
         print(json.dumps({"workload": name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K, "plan": plan, "ms": ms,
                           "ms_steady": ms_steady, "input_sets": nbuf, "tflops": tflops,
                           "gbs": nbytes / (ms_steady * 1e-3) / 1e9, "bound": bound, "roofline_tflops": roof,
                           "frac": tflops / roof,
-                          "peak_note": "fp32 FFMA at 2070 MHz" if w.kind == "f32" else "measured bf16 burst"}),
+                          "peak_note": {"f32": "fp32 FFMA at 2070 MHz",
+                                        "f32x3": "measured bf16 burst / 2 (TF32) / 3 products"}.get(
+                                            w.kind, "measured bf16 burst")}),
               flush=True)
         del sets
         torch.cuda.empty_cache()

@@ -5,6 +5,7 @@ kernels behind the C ABI declared in ``include/gemm11.h``.  There is no
 fallback: if the shared library is missing, every call raises.
 
     gemm_f32(A, B, C, alpha=1.0, beta=0.0)            C = alpha*A@B + beta*C (fp32)
+    gemm_f32_3xtf32(A, B, C, alpha=1.0, beta=0.0)     the same on the tensor cores (3 TF32 products)
     gemm_f16_f32acc_epilogue(A, B, C, alpha=1.0, beta=0.0, bias=None, act=0)
                                                       C = act(alpha*A@B + beta*C + bias)
     gemm_bf16_f32acc_epilogue(...)                    the same with bf16 A and B
@@ -37,7 +38,7 @@ GEMM_DTYPE_F32 = 0
 GEMM_DTYPE_F16 = 1
 GEMM_DTYPE_BF16 = 2
 
-EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f16_f32acc_epilogue", "gemm_bf16_f32acc_epilogue",
+EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_f16_f32acc_epilogue", "gemm_bf16_f32acc_epilogue",
                     "gemm_tc_f32acc_epilogue", "gemm_tc_strided_batched", "gemm_f16_f32acc_epilogue_noalloc",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count")
@@ -67,6 +68,8 @@ def lib():
             L.gemm_f32.restype = c_int
             L.gemm_f32.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_int, c_void_p, c_int, c_float,
                                    c_void_p, c_int, c_void_p]
+            L.gemm_f32_3xtf32.restype = c_int
+            L.gemm_f32_3xtf32.argtypes = L.gemm_f32.argtypes
             L.gemm_f16_f32acc_epilogue.restype = c_int
             L.gemm_f16_f32acc_epilogue.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_float,
                                                    c_void_p, c_void_p, c_int, c_void_p]
@@ -183,8 +186,24 @@ def gemm_f16_noalloc_raw(M, N, K, alpha, A_ptr, B_ptr, beta, C_ptr, bias_ptr=0, 
                                                   ctypes.c_void_p(stream_ptr))
 
 
+def gemm_f32_3xtf32_raw(M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream_ptr=0) -> int:
+    """Direct C-ABI call of the 3xTF32 FP32 GEMM; returns the status code."""
+    return lib().gemm_f32_3xtf32(int(M), int(N), int(K), float(alpha), ctypes.c_void_p(A_ptr), int(lda),
+                                 ctypes.c_void_p(B_ptr), int(ldb), float(beta), ctypes.c_void_p(C_ptr), int(ldc),
+                                 ctypes.c_void_p(stream_ptr))
+
+
+def gemm_f32_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, stream=None) -> None:
+    """C = alpha * A @ B + beta * C, FP32 operands, on the tensor cores (3 TF32 products)."""
+    _gemm_f32_like("gemm_f32_3xtf32", A, B, C, alpha, beta, stream)
+
+
 def gemm_f32(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, stream=None) -> None:
     """C = alpha * A @ B + beta * C in true FP32 (CUDA-core FFMA)."""
+    _gemm_f32_like("gemm_f32", A, B, C, alpha, beta, stream)
+
+
+def _gemm_f32_like(fn_name, A, B, C, alpha, beta, stream) -> None:
     import torch
     a_ptr, lda = _mat(A, "A", torch.float32)
     b_ptr, ldb = _mat(B, "B", torch.float32)
@@ -193,10 +212,10 @@ def gemm_f32(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, stream=None) -> 
     K2, N = B.shape
     if K2 != K or tuple(C.shape) != (M, N):
         raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
-    st = lib().gemm_f32(M, N, K, float(alpha), ctypes.c_void_p(a_ptr), lda, ctypes.c_void_p(b_ptr), ldb,
-                        float(beta), ctypes.c_void_p(c_ptr), ldc, _stream_handle(stream))
+    st = getattr(lib(), fn_name)(M, N, K, float(alpha), ctypes.c_void_p(a_ptr), lda, ctypes.c_void_p(b_ptr), ldb,
+                                 float(beta), ctypes.c_void_p(c_ptr), ldc, _stream_handle(stream))
     if st != GEMM_OK:
-        raise GemmError(st, "gemm_f32")
+        raise GemmError(st, fn_name)
 
 
 def _gemm_16bit(fn_name, in_dtype, A, B, C, alpha, beta, bias, act, stream) -> None:

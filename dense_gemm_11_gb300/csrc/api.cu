@@ -177,6 +177,34 @@ int gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const fl
     return GEMM_OK;
 }
 
+int gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+                    float *C, int ldc, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) {
+        t_last_plan = "noop_empty";
+        t_last_launches = 0;
+        return GEMM_OK;
+    }
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    const bool product = (K > 0) && (alpha != 0.f);
+    if (product && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    // C is written by TMA stores: 16-byte aligned base and rows.
+    if (product && (((reinterpret_cast<uintptr_t>(C) & 15u) != 0) || (ldc % 4) != 0)) return GEMM_ERR_UNSUPPORTED;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CallInfo info;
+    cudaError_t e = product ? run_gemm_f32_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, &info)
+                            : run_scale_c(M, N, beta, C, ldc, nullptr, 0, s, &info);
+    if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_plan = info.plan;
+    t_last_launches = info.launches;
+    return GEMM_OK;
+}
+
 }  // extern "C"
 
 namespace {

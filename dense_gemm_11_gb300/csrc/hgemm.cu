@@ -48,13 +48,15 @@ constexpr int kBK = 64;           // k per stage: one 128-byte swizzle row of fp
 constexpr int kUmmaK = 16;        // k per tcgen05.mma (kind::f16)
 constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpiWarps = 4;
+constexpr int kX3ChunkKB = 4;     // FP32-accuracy mode: k blocks (of 32) per tensor-core accumulation
 
 struct HgemmArgs {
     int M, N, K;
     float alpha, beta;
     const float *bias;
     int act;
-    void *C;     // row-major M x N (ldc = N), for beta reads and transposed stores
+    void *C;     // row-major M x N, rows ldc elements apart (beta reads, transposed stores)
+    int ldc;
     int c_type;  // kOutF32, kOutF16 or kOutBF16
     int tiles_m, tiles_n, kb_total, splits, units;
     float *ws;
@@ -183,21 +185,25 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
     for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
     if (p.beta != 0.f && grow < p.M) {
         if (p.c_type == kOutF32) {
-            const float *crow = static_cast<const float *>(p.C) + cbase + static_cast<size_t>(grow) * p.N;
+            const float *crow = static_cast<const float *>(p.C) + cbase + static_cast<size_t>(grow) * p.ldc;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int gc = col0 + 4 * q;
-                if (gc < p.N) {  // N % 8 == 0: the whole group of 4 is in range
+                if (gc + 4 <= p.N) {  // 16-byte aligned: ldc % 4 == 0 and C 16-byte aligned
                     const float4 c4 = *reinterpret_cast<const float4 *>(crow + gc);
                     v[4 * q] = fmaf(p.beta, c4.x, v[4 * q]);
                     v[4 * q + 1] = fmaf(p.beta, c4.y, v[4 * q + 1]);
                     v[4 * q + 2] = fmaf(p.beta, c4.z, v[4 * q + 2]);
                     v[4 * q + 3] = fmaf(p.beta, c4.w, v[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (gc + i < p.N) v[4 * q + i] = fmaf(p.beta, crow[gc + i], v[4 * q + i]);
                 }
             }
         } else {
             // 16-bit C: groups of 8 columns are 16-byte aligned (N % 8 == 0)
-            const uint16_t *crow = static_cast<const uint16_t *>(p.C) + cbase + static_cast<size_t>(grow) * p.N;
+            const uint16_t *crow = static_cast<const uint16_t *>(p.C) + cbase + static_cast<size_t>(grow) * p.ldc;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int gc = col0 + 8 * q;
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j) {
                             const int gm = ch * 32 + j;
                             if (gm < p.M) {
-                                const size_t ci = cbase + static_cast<size_t>(gm) * p.N + gn;
+                                const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
                                 const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
                                 store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
                             }
@@ -617,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = 0; j < 32; ++j) {
                                     const int gm = ch * 32 + j;
                                     if (gm < p.M) {
-                                        const size_t ci = cbase + static_cast<size_t>(gm) * p.N + gn;
+                                        const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
                                         const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
                                         store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
                                     }
@@ -665,15 +671,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the MMA thread's commits arrive on both CTAs' "empty" and "accumulator
 // full" barriers (multicast); both CTAs' epilogue warps arrive on the even
 // CTA's "accumulator empty" barrier.
-template <int BN, int STAGES, int EPI>
+// X3: FP32-accuracy mode.  A and B arrive split into TF32 high and low parts
+// (A_hi + A_lo, B_hi + B_lo, B stored N x K); each stage holds both parts of
+// both operands, 32 k per 128-byte row, and the MMA thread issues
+// A_lo B_hi + A_hi B_lo + A_hi B_hi (kind::tf32) per k step.
+template <int BN, int STAGES, int EPI, bool X3 = false>
 struct HgemmPairCfg {
     static constexpr int kNBuf = EPI == 4 ? 2 : 1;    // 4 KB staging buffers per epilogue warp
     static constexpr int kThreadsPair = 64 + 32 * EPI;
-    static constexpr int kABytes = kBM * kBK * 2;  // this CTA's 128 rows
+    static constexpr int kKB = X3 ? 32 : kBK;      // k per stage: one 128-byte swizzle row
+    static constexpr int kABytes = kBM * 128;      // this CTA's 128 rows (one part)
     static constexpr int kBHalf = BN / 2;          // this CTA's columns of B
     static constexpr int kBBoxes = (kBHalf + 63) / 64;
-    static constexpr int kBBytes = kBBoxes * 64 * kBK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBBytes = X3 ? kBHalf * 128 : kBBoxes * 64 * kBK * 2;  // one part
+    static constexpr int kParts = X3 ? 2 : 1;
+    static constexpr int kAStage = kParts * kABytes;
+    static constexpr int kBStage = kParts * kBBytes;
+    static constexpr int kStageBytes = kAStage + kBStage;
     static constexpr int kCStageBytes = EPI * kNBuf * 32 * 32 * 4;
     static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
@@ -681,6 +695,7 @@ struct HgemmPairCfg {
     static_assert(BN % 32 == 0 && BN <= 256 && kBHalf % 16 == 0, "pair MMA N");
     static_assert(EPI == 4 || EPI == 8, "epilogue warps");
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
+    static_assert(kBBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
 };
 
 // Pair tile t (over the whole batch) -> (matrix index, first row of the
@@ -696,16 +711,17 @@ __device__ __forceinline__ void pair_tile_origin(const HgemmArgs &p, int t, int 
     n0 = ((t % group_tiles) / gsz) * bn;
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool X3>
 __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     hgemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                         const __grid_constant__ CUtensorMap tm_c, const HgemmArgs p) {
-    using Cfg = HgemmPairCfg<BN, STAGES, EPI>;
+                         const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_a2,
+                         const __grid_constant__ CUtensorMap tm_b2, const HgemmArgs p) {
+    using Cfg = HgemmPairCfg<BN, STAGES, EPI, X3>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * Cfg::kABytes;
-    uint8_t *sC = sB + STAGES * Cfg::kBBytes;
+    uint8_t *sA = smem;                               // STAGES x kAStage (A, or A_hi | A_lo)
+    uint8_t *sB = smem + STAGES * Cfg::kAStage;       // STAGES x kBStage (B, or B_hi | B_lo)
+    uint8_t *sC = sB + STAGES * Cfg::kBStage;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sC + Cfg::kCStageBytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
@@ -722,8 +738,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
     // Bytes each CTA stages per k block: its A rows and its half of B (64-column
-    // boxes when B is K x N; exactly BN/2 rows of 64 k when B is N x K).
-    const uint32_t stage_tx = Cfg::kABytes + (p.b_kmajor ? Cfg::kBHalf * kBK * 2 : Cfg::kBBytes);
+    // boxes when B is K x N; exactly BN/2 rows of 64 k when B is N x K); both
+    // parts of each in the FP32-accuracy mode.
+    const uint32_t stage_tx =
+        X3 ? Cfg::kStageBytes : Cfg::kABytes + (p.b_kmajor ? Cfg::kBHalf * kBK * 2 : Cfg::kBBytes);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -742,6 +760,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
         tma_prefetch_desc(&tm_c);
+        if (X3) {
+            tma_prefetch_desc(&tm_a2);
+            tma_prefetch_desc(&tm_b2);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_holder, Cfg::kTmemCols);
@@ -773,15 +795,20 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 }
                 if (leader) mbar_arrive_expect_tx(&full[stage], 2 * stage_tx);
                 const uint32_t full_even = mapa_shared(smem_u32(&full[stage]), 0);
-                const int k0 = kb * kBK;
-                tma_load_3d_pair(&tm_a, full_even, sA + stage * Cfg::kABytes, k0, my_m, za);
-                if (p.b_kmajor) {
-                    tma_load_3d_pair(&tm_b, full_even, sB + stage * Cfg::kBBytes, k0, my_n, zb);
+                const int k0 = kb * Cfg::kKB;
+                uint8_t *a_dst = sA + stage * Cfg::kAStage;
+                uint8_t *b_dst = sB + stage * Cfg::kBStage;
+                tma_load_3d_pair(&tm_a, full_even, a_dst, k0, my_m, za);
+                if constexpr (X3) {
+                    tma_load_3d_pair(&tm_a2, full_even, a_dst + Cfg::kABytes, k0, my_m, za);
+                    tma_load_3d_pair(&tm_b, full_even, b_dst, k0, my_n, zb);
+                    tma_load_3d_pair(&tm_b2, full_even, b_dst + Cfg::kBBytes, k0, my_n, zb);
+                } else if (p.b_kmajor) {
+                    tma_load_3d_pair(&tm_b, full_even, b_dst, k0, my_n, zb);
                 } else {
 #pragma unroll
                     for (int j = 0; j < Cfg::kBBoxes; ++j)
-                        tma_load_3d_pair(&tm_b, full_even, sB + stage * Cfg::kBBytes + j * 8192, my_n + 64 * j, k0,
-                                         zb);
+                        tma_load_3d_pair(&tm_b, full_even, b_dst + j * 8192, my_n + 64 * j, k0, zb);
                 }
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -796,43 +823,134 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         // ------------------------------------------------ MMA issuer (even CTA)
         // Descriptors of stage 0, moved by address / 16 per stage and k step.
         const uint64_t a_desc0 = umma_desc_sw128(smem_u32(sA), 16, 1024);
-        const uint64_t b_desc0 = p.b_kmajor ? umma_desc_sw128(smem_u32(sB), 16, 1024)
-                                            : umma_desc_sw128(smem_u32(sB), 8192, 1024);
-        const uint32_t b_kstep = p.b_kmajor ? 2u : 128u;
+        const bool b_kmajor = X3 || p.b_kmajor;
+        const uint64_t b_desc0 = b_kmajor ? umma_desc_sw128(smem_u32(sB), 16, 1024)
+                                          : umma_desc_sw128(smem_u32(sB), 8192, 1024);
+        const uint32_t b_kstep = b_kmajor ? 2u : 128u;
+        // The accumulator is handed to the epilogue once per tile, or in the
+        // FP32-accuracy mode once per chunk of kX3ChunkKB k blocks (the epilogue
+        // adds the chunks in FP32 registers).
+        const int kb_chunk = X3 ? kX3ChunkKB : p.kb_total;
+        const int nch = (p.kb_total + kb_chunk - 1) / kb_chunk;
         int stage = 0;
         uint32_t phase = 0;
         int local = 0;
-        for (int t = cid; t < p.units && !*abort_flag; t += ncl, ++local) {
-            const int buf = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
-            if (!mbar_wait(&tempty[buf], acc_phase ^ 1u)) {
-                flag_timeout(abort_flag, p.err);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-            bool ok = true;
-            for (int kb = 0; kb < p.kb_total; ++kb) {
-                if (!mbar_wait(&full[stage], phase)) {
+        bool ok = true;
+        for (int t = cid; ok && t < p.units && !*abort_flag; t += ncl) {
+            for (int c = 0; c < nch; ++c, ++local) {
+                const int buf = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait(&tempty[buf], acc_phase ^ 1u)) {
                     flag_timeout(abort_flag, p.err);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = a_desc0 + stage * (Cfg::kABytes >> 4);
-                const uint64_t bd = b_desc0 + stage * (Cfg::kBBytes >> 4);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                const int kb0 = c * kb_chunk, kb1 = min(p.kb_total, kb0 + kb_chunk);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase)) {
+                        flag_timeout(abort_flag, p.err);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = a_desc0 + stage * (Cfg::kAStage >> 4);
+                    const uint64_t bd = b_desc0 + stage * (Cfg::kBStage >> 4);
+                    if constexpr (X3) {
+                        // small products first: A_lo B_hi, A_hi B_lo, then A_hi B_hi (K = 8 each)
+                        const uint64_t al = ad + (Cfg::kABytes >> 4), bl = bd + (Cfg::kBBytes >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-                    umma_f16_pair(d_tmem, ad + 2u * kk, bd + b_kstep * kk, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                umma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                        for (int kk = 0; kk < 4; ++kk) {
+                            umma_tf32_pair(d_tmem, al + 2u * kk, bd + 2u * kk, p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                            umma_tf32_pair(d_tmem, ad + 2u * kk, bl + 2u * kk, p.idesc, 1u);
+                            umma_tf32_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, 1u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+                            umma_f16_pair(d_tmem, ad + 2u * kk, bd + b_kstep * kk, p.idesc,
+                                          (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(&tfull[buf], 0x3);  // both halves of the accumulator complete
+            }
+        }
+    } else if (X3 && warp >= 2) {
+        // ------------------------------------------------ epilogue, FP32-accuracy mode
+        // Eight warps: warp w reads TMEM lane quarter w % 4 and owns 4 of the
+        // 8 column groups of its rows ((w - 2) / 4 selects which), keeping
+        // their running sums in registers.  Each chunk accumulator (kX3ChunkKB
+        // k blocks, summed by the tensor core) is added in FP32 with
+        // round-to-nearest; the tensor core's own accumulation is truncated,
+        // so keeping its sums short keeps the total within FP32's error level
+        // for any K.
+        static_assert(!X3 || (EPI == 8 && BN == 256), "FP32-accuracy mode: 8 epilogue warps, 256 columns");
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        const int g0 = ((warp - 2) >> 2) * 4;  // first of this warp's 4 column groups
+        uint8_t *const stage_base = sC + (warp - 2) * (Cfg::kNBuf * 4096);
+        uint32_t n_staged = 0;
+        const int nch = (p.kb_total + kX3ChunkKB - 1) / kX3ChunkKB;
+        int local = 0;
+        bool ok = true;
+        for (int t = cid; ok && t < p.units && !*abort_flag; t += ncl) {
+            int m0, n0, bz;
+            pair_tile_origin(p, t, BN, m0, n0, bz);
+            const int my_m = m0 + static_cast<int>(rank) * kBM;
+            const size_t cbase = static_cast<size_t>(bz) * static_cast<size_t>(p.stride_c);
+            float tot[4][32];
+            for (int c = 0; c < nch; ++c, ++local) {
+                const int buf = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait(&tfull[buf], acc_phase)) {
+                    flag_timeout(abort_flag, p.err);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t t_row =
+                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+                for (int gh = 0; gh < 8; ++gh) {  // half groups of 16 columns (fewer live registers)
+                    const int gi = gh >> 1, j0 = (gh & 1) * 16;
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(t_row + (g0 + gi) * 32 + j0, r);
+                    tmem_wait_ld();
+                    if (c == 0) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) tot[gi][j0 + j] = __uint_as_float(r[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) tot[gi][j0 + j] += __uint_as_float(r[j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        mbar_arrive(&tempty[buf]);
+                    else
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
                 }
             }
             if (!ok) break;
-            umma_commit_pair_mc(&tfull[buf], 0x3);  // both halves of the accumulator complete
+            const int grow = my_m + row_in_tile;
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi) {
+                const int col0 = n0 + (g0 + gi) * 32;
+                epilogue_row_chunk(tot[gi], p, grow, col0, cbase);
+                store_row_chunk<Cfg::kNBuf>(tot[gi], p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0, bz);
+            }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue warps (both CTAs)
         // Warp w reads TMEM lane quarter w % 4.  With 8 epilogue warps two
@@ -940,12 +1058,12 @@ bool encode_3d(CUtensorMap *map, CUtensorMapDataType dt, int elem_bytes, const v
 
 // Store map of C: 32 x 32 boxes; FP32 rows of the box are 128 bytes (128-byte
 // swizzle), 16-bit rows 64 bytes (64-byte swizzle), matching store_row_chunk.
-bool encode_c(CUtensorMap *map, const TcGemm &g) {
+bool encode_c(CUtensorMap *map, const TcGemm &g, int ldc) {
     if (g.c_type == kOutF32)
-        return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.C, g.N, g.M, g.batch, g.N, g.stride_c, 32, 32);
+        return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.C, g.N, g.M, g.batch, ldc, g.stride_c, 32, 32);
     const CUtensorMapDataType dt =
         g.c_type == kOutF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    return encode_3d(map, dt, 2, g.C, g.N, g.M, g.batch, g.N, g.stride_c, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    return encode_3d(map, dt, 2, g.C, g.N, g.M, g.batch, ldc, g.stride_c, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Operand maps.  A: K x M per matrix, boxes of 64 k x `rows` rows.  B stored
@@ -976,11 +1094,12 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     return cudaPeekAtLastError();
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool X3 = false>
 cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const HgemmArgs &a,
-                              cudaStream_t stream, int *clusters_used) {
-    using Cfg = HgemmPairCfg<BN, STAGES, EPI>;
-    auto kern = hgemm_tc_pair_kernel<BN, STAGES, EPI>;
+                              cudaStream_t stream, int *clusters_used, const CUtensorMap *ta2 = nullptr,
+                              const CUtensorMap *tb2 = nullptr) {
+    using Cfg = HgemmPairCfg<BN, STAGES, EPI, X3>;
+    auto kern = hgemm_tc_pair_kernel<BN, STAGES, EPI, X3>;
     static int max_clusters = -1;  // per instantiation; one device type per process
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set);
@@ -1008,8 +1127,9 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     *clusters_used = clusters;
     HgemmArgs args = a;
-    args.idesc = umma_idesc_f16_f32(2 * kBM, BN, 0, a.b_kmajor ? 0 : 1) | a.idesc_fmt;
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
+    args.idesc = X3 ? umma_idesc_f16_f32(2 * kBM, BN, 0, 0) | kIdescTf32Operands
+                    : umma_idesc_f16_f32(2 * kBM, BN, 0, a.b_kmajor ? 0 : 1) | a.idesc_fmt;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, ta2 ? *ta2 : ta, tb2 ? *tb2 : tb, args);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
@@ -1032,6 +1152,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     a.bias = g.bias;
     a.act = g.act;
     a.C = g.C;
+    a.ldc = g.N;
     a.c_type = g.c_type;
     a.kb_total = (K + kBK - 1) / kBK;
     a.err = watchdog_word();
@@ -1110,7 +1231,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
             a.splits = 1;
             a.units = t2;
             CUtensorMap ta, tb, tc;
-            if (!encode_a(&ta, g, in_dt, kBM) || !encode_b(&tb, g, in_dt, best_bn / 2) || !encode_c(&tc, g))
+            if (!encode_a(&ta, g, in_dt, kBM) || !encode_b(&tb, g, in_dt, best_bn / 2) || !encode_c(&tc, g, g.N))
                 return cudaErrorNotSupported;
             int used = 0;
             cudaError_t e;
@@ -1118,13 +1239,13 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
             // buffer each, measured no faster: the epilogue is off the
             // critical path.)
             if (best_bn == 256) {
-                e = launch_hgemm_pair<256, 6, 4>(ta, tb, tc, a, stream, &used);
+                e = launch_hgemm_pair<256, 6, 4, false>(ta, tb, tc, a, stream, &used);
                 info->plan = "tc_pair_256x256";
             } else if (best_bn == 224) {
-                e = launch_hgemm_pair<224, 6, 4>(ta, tb, tc, a, stream, &used);
+                e = launch_hgemm_pair<224, 6, 4, false>(ta, tb, tc, a, stream, &used);
                 info->plan = "tc_pair_256x224";
             } else {
-                e = launch_hgemm_pair<192, 6, 4>(ta, tb, tc, a, stream, &used);
+                e = launch_hgemm_pair<192, 6, 4, false>(ta, tb, tc, a, stream, &used);
                 info->plan = "tc_pair_256x192";
             }
             info->launches = 1;
@@ -1158,7 +1279,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     if (!swap) {
         ok = ok && encode_a(&ta, g, in_dt, kBM);
         ok = ok && encode_b(&tb, g, in_dt, bn);
-        ok = ok && encode_c(&tc, g);
+        ok = ok && encode_c(&tc, g, g.N);
     } else {
         ok = ok && encode_a(&ta, g, in_dt, bn);
         ok = ok && encode_b(&tb, g, in_dt, kBM);
@@ -1185,6 +1306,115 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
         }
     }
     info->launches = 1;
+    return e;
+}
+
+// ------------------------------------------------------------------ FP32 through 3 x TF32
+// The FP32 product on the tensor cores: every FP32 operand x is split into a
+// TF32 high part h = tf32(x) and a TF32 low part l = tf32(x - h) (x - h is
+// exact in FP32), so x = h + l + e with |e| <= 2^-22 |x|, and
+//   a b ~= a_h b_h + a_h b_l + a_l b_h        (a_l b_l ~ 2^-22 |a b| dropped).
+// A pre-pass writes A_h, A_l (M x Kp) and B_h^T, B_l^T (N x Kp, so that both
+// MMA operands are K-major), Kp = K rounded up to 4 (16-byte rows), zero-filled
+// past K; the CTA-pair kernel then runs three kind::tf32 MMAs per k step.
+namespace {
+
+__global__ void __launch_bounds__(256) split_rows_tf32_kernel(const float *__restrict__ A, int lda, int M, int K,
+                                                              int Kp, float *__restrict__ hi, float *__restrict__ lo) {
+    for (int r = blockIdx.x; r < M; r += gridDim.x) {
+        const float *src = A + static_cast<size_t>(r) * lda;
+        float *h = hi + static_cast<size_t>(r) * Kp;
+        float *l = lo + static_cast<size_t>(r) * Kp;
+        for (int c = threadIdx.x; c < Kp; c += 256) {
+            const float x = c < K ? __ldcs(src + c) : 0.f;
+            const float xh = tf32_round(x);
+            h[c] = xh;
+            l[c] = tf32_round(x - xh);
+        }
+    }
+}
+
+// B (K x N, ldb) -> B_h^T, B_l^T (N x Kp) through 32 x 32 shared-memory tiles:
+// reads along n and writes along k are both coalesced.
+__global__ void __launch_bounds__(256) split_cols_tf32_kernel(const float *__restrict__ B, int ldb, int K, int N,
+                                                              int Kp, float *__restrict__ hi, float *__restrict__ lo) {
+    __shared__ float tile[32][33];
+    const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const int k = k0 + ty + j, n = n0 + tx;
+        tile[ty + j][tx] = (k < K && n < N) ? __ldcs(B + static_cast<size_t>(k) * ldb + n) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const int n = n0 + ty + j, k = k0 + tx;
+        if (n < N && k < Kp) {
+            const float x = tile[tx][ty + j];
+            const float xh = tf32_round(x);
+            hi[static_cast<size_t>(n) * Kp + k] = xh;
+            lo[static_cast<size_t>(n) * Kp + k] = tf32_round(x - xh);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t run_gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                                float beta, float *C, int ldc, cudaStream_t stream, CallInfo *info) {
+    const int sms = device_sm_count();
+    const int Kp = (K + 3) & ~3;
+    const size_t a_elems = static_cast<size_t>(M) * Kp, b_elems = static_cast<size_t>(N) * Kp;
+    float *ws = nullptr;
+    cudaError_t e = acquire_operand_scratch(stream, 2 * a_elems + 2 * b_elems, &ws);
+    if (e != cudaSuccess) return e;
+    float *a_hi = ws, *a_lo = ws + a_elems, *bt_hi = a_lo + a_elems, *bt_lo = bt_hi + b_elems;
+    split_rows_tf32_kernel<<<std::min(M, 8 * sms), 256, 0, stream>>>(A, lda, M, K, Kp, a_hi, a_lo);
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+    const dim3 tgrid((N + 31) / 32, (Kp + 31) / 32);
+    if (tgrid.y > 65535u) return cudaErrorNotSupported;
+    split_cols_tf32_kernel<<<tgrid, 256, 0, stream>>>(B, ldb, K, N, Kp, bt_hi, bt_lo);
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+
+    constexpr int BN = 256;
+    HgemmArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.C = C;
+    a.ldc = ldc;
+    a.c_type = kOutF32;
+    a.kb_total = (K + 31) / 32;
+    a.err = watchdog_word();
+    a.batch = 1;
+    a.za = a.zb = 0;
+    a.stride_c = static_cast<long long>(M) * ldc;
+    a.b_kmajor = 1;
+    a.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
+    a.tiles_n = (N + BN - 1) / BN;
+    const long long t2 = static_cast<long long>(a.tiles_m) * a.tiles_n;
+    if (t2 > (1LL << 26)) return cudaErrorNotSupported;
+    a.splits = 1;
+    a.units = static_cast<int>(t2);
+    TcGemm g;
+    g.M = M;
+    g.N = N;
+    g.C = C;
+    CUtensorMap ta, ta2, tb, tb2, tc;
+    const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (!encode_3d(&ta, f32, 4, a_hi, K, M, 1, Kp, 0, 32, kBM) || !encode_3d(&ta2, f32, 4, a_lo, K, M, 1, Kp, 0, 32, kBM) ||
+        !encode_3d(&tb, f32, 4, bt_hi, K, N, 1, Kp, 0, 32, BN / 2) ||
+        !encode_3d(&tb2, f32, 4, bt_lo, K, N, 1, Kp, 0, 32, BN / 2) || !encode_c(&tc, g, ldc))
+        return cudaErrorNotSupported;
+    int used = 0;
+    e = launch_hgemm_pair<BN, 3, 8, true>(ta, tb, tc, a, stream, &used, &ta2, &tb2);
+    info->plan = "tf32x3_pair_256x256";
+    info->launches = 3;
     return e;
 }
 
@@ -1244,6 +1474,7 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
     a.bias = bias;
     a.act = act;
     a.C = C;
+    a.ldc = N;
     a.kb_total = (K + kBK - 1) / kBK;
     a.err = watchdog_word();
     a.batch = 1;

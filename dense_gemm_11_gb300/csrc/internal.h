@@ -80,6 +80,11 @@ struct TcGemm {
 };
 cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info);
 
+// FP32 GEMM on the tensor cores with three TF32 products per k step (operands
+// split into high and low TF32 parts); C 16-byte aligned with ldc % 4 == 0.
+cudaError_t run_gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                                float beta, float *C, int ldc, cudaStream_t stream, CallInfo *info);
+
 // The same small-M (M <= 64) transposed split-K plan with its scratch in a
 // fixed device array (no allocation).  *reject = 1 if M > 64, 2 if the plan's
 // scratch exceeds the array; nothing is launched then.

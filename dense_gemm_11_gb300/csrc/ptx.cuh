@@ -293,6 +293,16 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "r"(taddr)
         : "memory");
 }
+// 16 columns: register r[j] = column base + j of this thread's lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- CTA pairs (clusters of 2)
@@ -359,6 +369,27 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same pair MMA of kind::tf32: A and B tiles hold FP32 words of which the
+// MMA uses the TF32 part (sign, 8 exponent bits, the top 10 mantissa bits);
+// K = 8 per instruction (32 bytes of each row, as for kind::f16).
+__device__ __forceinline__ void umma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// FP32 -> TF32, round to nearest (ties away from zero); the low 13 mantissa
+// bits of the result are zero.
+__device__ __forceinline__ float tf32_round(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
 // Arrive once on the mbarrier at this offset in every CTA of `cta_mask` when
 // all pair MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void umma_commit_pair_mc(uint64_t *bar, uint16_t cta_mask) {
@@ -395,5 +426,7 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16_f32(int M, int N, int a_mn
 // Operand-format bits for BF16 A and B (the same kind::f16 MMA; only the two
 // 3-bit format fields change, F16 = 0, BF16 = 1).
 constexpr uint32_t kIdescBf16Operands = (1u << 7) | (1u << 10);
+// Operand-format bits for TF32 A and B (kind::tf32: format code 2 in both fields).
+constexpr uint32_t kIdescTf32Operands = (2u << 7) | (2u << 10);
 
 }  // namespace gemm11

@@ -32,7 +32,7 @@ import numpy as np
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str            # "f32", "f16" or "bf16"
+    kind: str            # "f32", "f16", "bf16", or "f32x3" (FP32 through gemm_f32_3xtf32)
     M: int
     N: int
     K: int
@@ -83,6 +83,8 @@ def _registry():
         w[f"bf16_epi{i}"] = Workload(f"bf16_epi{i}", "bf16", m, n, k, 0.5, 0.0, "normal_k", 12 + i,
                                      bias=True, act=act,
                                      note=f"BF16 {'ReLU' if act == 2 else 'tanh-GELU'}(0.5*A*B+bias) {m}x{n}x{k}")
+    w["f32x3_4096"] = Workload("f32x3_4096", "f32x3", 4096, 4096, 4096, 1.0, 3.0, "uniform", 3,
+                               note="FP32 4096^3 on the tensor cores (3 x TF32), beta 3, C reset each run")
     w["f16_4096_out16"] = Workload("f16_4096_out16", "f16", 4096, 4096, 4096, 1.0, 0.0, "normal_k", 16,
                                    out="f16", note="FP16-in FP32-acc 4096^3, FP16 C")
     # Attention products per head (32 = batch 4 x 8 heads, sequence 2048, head
@@ -123,7 +125,7 @@ def round_to_bf16(x):
 
 
 def _cast_input(x, kind):
-    if kind == "f32":
+    if kind in ("f32", "f32x3"):
         return x.astype(np.float32)
     if kind == "f16":
         return x.astype(np.float16)

@@ -92,6 +92,31 @@ GEMM11_API int gemm_f32(int M, int N, int K, float alpha, const float *A, int ld
              float beta, float *C, int ldc, void *stream);
 
 /*
+ * gemm_f32_3xtf32 -- the operation, arguments and return codes of gemm_f32,
+ * computed on the tcgen05 tensor cores instead of the FP32 FMA units (opt in;
+ * gemm_f32 is unchanged).  Each FP32 operand x is split into a TF32 high
+ * part h = tf32(x) and a TF32 low part l = tf32(x - h), and each product is
+ * taken as a_h b_h + a_h b_l + a_l b_h, which drops terms of about
+ * 2^-21 |a b|.  The tensor core sums chunks of 128 k (its FP32 accumulation
+ * truncates, a bias that would grow with K); the chunk sums are added in
+ * FP32 with round-to-nearest on the CUDA cores.  Measured on GB300: at most
+ * 1.7e-6 S for same-sign data and 4e-7 S for mixed signs, for K from 256 to
+ * 16384 -- inside gemm_f32's bound |C - C_exact| <= 1e-5 S + 1e-6, but not
+ * bit-identical to gemm_f32.
+ * "SGEMM优化，从naive到warptiling" (Q9, the optimisations not made) lists
+ * TF32 / tensor cores; "第 11 章 Tiled GEMM" (section 11.7) puts the FP32
+ * CUDA-core peak at about 1/15 of the dense FP16 tensor-core peak.
+ *   Extra constraint: C 16-byte aligned and ldc % 4 == 0 (C is written by
+ *   TMA stores), otherwise GEMM_ERR_UNSUPPORTED; A and B may have any
+ *   alignment and leading dimension.  Scratch: 16 (M + N) K' bytes of
+ *   library-owned device memory per stream, K' = K rounded up to 4.  Inputs
+ *   within 2^-11 of the FP32 overflow threshold are outside the method (their
+ *   TF32 high part rounds to infinity).
+ */
+GEMM11_API int gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                               float beta, float *C, int ldc, void *stream);
+
+/*
  * gemm_f16_f32acc_epilogue -- FP16 inputs, FP32 accumulation on the tcgen05
  * tensor cores, fused epilogue:
  *   C[i*N + j] = act( alpha * sum_k A[i*K + k] * B[k*N + j] + beta * C[i*N + j] + bias[j] )

@@ -142,3 +142,13 @@ def test_status_strings(L):
 def test_watchdog_selftest_rejects_bad_limits_on_host(L):
     assert L.gemm_watchdog_selftest(0, None) == g.GEMM_ERR_INVALID_ARG
     assert L.gemm_watchdog_selftest(2001, None) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_3xtf32_rejects_bad_args(L):
+    f = g.gemm_f32_3xtf32_raw
+    assert f(-1, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4) == g.GEMM_ERR_INVALID_ARG
+    assert f(4, 4, 8, 1.0, FAKE, 7, FAKE, 4, 0.0, FAKE, 4) == g.GEMM_ERR_INVALID_ARG   # lda < K
+    assert f(4, 4, 4, 1.0, 0, 4, FAKE, 4, 0.0, FAKE, 4) == g.GEMM_ERR_INVALID_ARG
+    assert f(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE + 4, 4) == g.GEMM_ERR_UNSUPPORTED  # C not 16-byte aligned
+    assert f(4, 5, 4, 1.0, FAKE, 4, FAKE, 5, 0.0, FAKE, 5) == g.GEMM_ERR_UNSUPPORTED      # ldc % 4 != 0
+    assert f(0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4) == g.GEMM_OK
