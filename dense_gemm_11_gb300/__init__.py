@@ -37,9 +37,21 @@ GEMM_ACT_GELU_TANH = 3
 GEMM_DTYPE_F32 = 0
 GEMM_DTYPE_F16 = 1
 GEMM_DTYPE_BF16 = 2
+GEMM_PATH_F32 = 0
+GEMM_PATH_TC = 1
+
+
+class TuneEntry(ctypes.Structure):
+    """One row of the tuning table (gemm_tune_entry in include/gemm11.h)."""
+    _fields_ = [("path", ctypes.c_int), ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("variant", ctypes.c_int), ("bn", ctypes.c_int), ("splits", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: int(getattr(self, f)) for f, _ in self._fields_}
 
 EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_f16_f32acc_epilogue", "gemm_bf16_f32acc_epilogue",
                     "gemm_tc_f32acc_epilogue", "gemm_tc_strided_batched", "gemm_f16_f32acc_epilogue_noalloc",
+                    "gemm_tune_set", "gemm_tune_get",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count")
 
@@ -85,6 +97,10 @@ def lib():
                                                   c_int, c_void_p]
             L.gemm_f16_f32acc_epilogue_noalloc.restype = c_int
             L.gemm_f16_f32acc_epilogue_noalloc.argtypes = L.gemm_f16_f32acc_epilogue.argtypes
+            L.gemm_tune_set.restype = c_int
+            L.gemm_tune_set.argtypes = [ctypes.POINTER(TuneEntry), c_int]
+            L.gemm_tune_get.restype = c_int
+            L.gemm_tune_get.argtypes = [ctypes.POINTER(TuneEntry), c_int]
             L.gemm_status_string.restype = ctypes.c_char_p
             L.gemm_status_string.argtypes = [c_int]
             L.gemm_last_cuda_error.restype = c_int
@@ -339,6 +355,34 @@ def gemm_tc_batched(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, a
                                        ctypes.c_void_p(bias_ptr or None), int(act), _stream_handle(stream))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_tc_strided_batched")
+
+
+def tune_set(entries) -> None:
+    """Install a tuning table: an iterable of dicts (or TuneEntry) with keys
+    path, M, N, K, variant, bn, splits.  An empty iterable clears the table."""
+    rows = [e if isinstance(e, TuneEntry) else TuneEntry(**{k: int(e.get(k, 0)) for k, _ in TuneEntry._fields_})
+            for e in entries]
+    arr = (TuneEntry * max(1, len(rows)))(*rows)
+    st = lib().gemm_tune_set(arr, len(rows))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_tune_set")
+
+
+def tune_get() -> list:
+    """The installed tuning table as a list of dicts."""
+    n = lib().gemm_tune_get(None, 0)
+    arr = (TuneEntry * max(1, n))()
+    n = lib().gemm_tune_get(arr, n)
+    return [arr[i].as_dict() for i in range(n)]
+
+
+def load_tuning(path: str) -> int:
+    """Install the table stored by ``autotune`` in a JSON file; returns the entry count."""
+    import json
+    with open(path) as f:
+        doc = json.load(f)
+    tune_set(doc["entries"])
+    return len(doc["entries"])
 
 
 def watchdog_selftest(wait_ms: int = 20, stream=None) -> int:

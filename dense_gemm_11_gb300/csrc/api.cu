@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libgemm11.so: argument checks, degenerate shapes,
 // dispatch to the FP32 / FP16 paths, status codes, the per-(device, stream)
 // split-K scratch and the device watchdog word.
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <map>
@@ -33,6 +34,18 @@ __global__ void watchdog_probe_kernel(unsigned *err, unsigned long long limit_ns
 thread_local int t_last_cuda_error = 0;
 thread_local const char *t_last_plan = "none";
 thread_local int t_last_launches = 0;
+thread_local char t_plan_buf[96];
+
+// Record a finished call's plan for gemm_last_plan / gemm_last_launch_count.
+void record_plan(const gemm11::CallInfo &info) {
+    if (info.tuned) {
+        std::snprintf(t_plan_buf, sizeof(t_plan_buf), "%s+tuned", info.plan);
+        t_last_plan = t_plan_buf;
+    } else {
+        t_last_plan = info.plan;
+    }
+    t_last_launches = info.launches;
+}
 
 constexpr int kMaxDevices = 64;
 
@@ -150,7 +163,87 @@ cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **
 
 using namespace gemm11;
 
+// ------------------------------------------------------------------ tuning table
+namespace {
+
+struct TuneKey {
+    int path, M, N, K;
+    bool operator<(const TuneKey &o) const {
+        if (path != o.path) return path < o.path;
+        if (M != o.M) return M < o.M;
+        if (N != o.N) return N < o.N;
+        return K < o.K;
+    }
+};
+std::mutex g_tune_mutex;
+std::map<TuneKey, TunePlan> g_tune_table;
+std::atomic<bool> g_tune_any{false};  // lets every call skip the lock while the table is empty
+
+bool valid_tune_entry(const gemm_tune_entry &e) {
+    if (e.M < 0 || e.N < 0 || e.K < 0 || e.splits < 0 || e.splits > 32) return false;
+    if (e.path == GEMM_PATH_F32) return (e.variant == 1 && e.bn == 0) || (e.variant == 2 && e.bn == 0);
+    if (e.path != GEMM_PATH_TC) return false;
+    switch (e.variant) {
+        case 1: return e.bn == 0 || e.bn == 256 || e.bn == 224 || e.bn == 192;
+        case 2: return e.bn == 0 || e.bn == 256 || e.bn == 128;
+        case 3: return e.bn == 0 || e.bn == 32 || e.bn == 64;
+        default: return false;
+    }
+}
+
+}  // namespace
+
+namespace gemm11 {
+bool tune_lookup(int path, int M, int N, int K, TunePlan *out) {
+    if (!g_tune_any.load(std::memory_order_acquire)) return false;
+    std::lock_guard<std::mutex> lock(g_tune_mutex);
+    auto it = g_tune_table.find(TuneKey{path, M, N, K});
+    if (it == g_tune_table.end()) return false;
+    *out = it->second;
+    return true;
+}
+}  // namespace gemm11
+
 extern "C" {
+
+int gemm_tune_set(const gemm_tune_entry *entries, int n) {
+    if (n < 0 || (n > 0 && !entries)) return GEMM_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!valid_tune_entry(entries[i])) return GEMM_ERR_INVALID_ARG;
+    std::map<TuneKey, TunePlan> table;
+    for (int i = 0; i < n; ++i) {
+        const gemm_tune_entry &e = entries[i];
+        TunePlan tp;
+        tp.variant = e.variant;
+        tp.bn = e.bn;
+        tp.splits = e.splits;
+        table[TuneKey{e.path, e.M, e.N, e.K}] = tp;
+    }
+    std::lock_guard<std::mutex> lock(g_tune_mutex);
+    g_tune_table.swap(table);
+    g_tune_any.store(!g_tune_table.empty(), std::memory_order_release);
+    return GEMM_OK;
+}
+
+int gemm_tune_get(gemm_tune_entry *out, int capacity) {
+    std::lock_guard<std::mutex> lock(g_tune_mutex);
+    int i = 0;
+    for (const auto &kv : g_tune_table) {
+        if (out && i < capacity) {
+            gemm_tune_entry &e = out[i];
+            e.path = kv.first.path;
+            e.M = kv.first.M;
+            e.N = kv.first.N;
+            e.K = kv.first.K;
+            e.variant = kv.second.variant;
+            e.bn = kv.second.bn;
+            e.splits = kv.second.splits;
+        }
+        ++i;
+    }
+    return i;
+}
+
 
 int gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
              float *C, int ldc, void *stream) {
@@ -172,8 +265,7 @@ int gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const fl
     cudaError_t e = product ? run_gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, &info)
                             : run_scale_c(M, N, beta, C, ldc, nullptr, 0, s, &info);
     if (e != cudaSuccess) return fail_cuda(e);
-    t_last_plan = info.plan;
-    t_last_launches = info.launches;
+    record_plan(info);
     return GEMM_OK;
 }
 
@@ -200,8 +292,7 @@ int gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, c
                             : run_scale_c(M, N, beta, C, ldc, nullptr, 0, s, &info);
     if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return fail_cuda(e);
-    t_last_plan = info.plan;
-    t_last_launches = info.launches;
+    record_plan(info);
     return GEMM_OK;
 }
 
@@ -256,8 +347,7 @@ int gemm_tc_checked(const TcGemm &g, int ab_type, void *stream) {
         if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return fail_cuda(e);
-    t_last_plan = info.plan;
-    t_last_launches = info.launches;
+    record_plan(info);
     return GEMM_OK;
 }
 
@@ -345,8 +435,7 @@ int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const voi
         if (e == cudaSuccess && reject == 2) return GEMM_ERR_SCRATCH_LIMIT;
     }
     if (e != cudaSuccess) return fail_cuda(e);
-    t_last_plan = info.plan;
-    t_last_launches = info.launches;
+    record_plan(info);
     return GEMM_OK;
 }
 

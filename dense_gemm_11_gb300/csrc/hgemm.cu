@@ -1168,15 +1168,22 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     // matrices of a batch in one sequence); with fewer tiles than a third of
     // the SMs, K is split evenly and partial tiles are reduced in k order by
     // the last contributor to arrive (per 32-row slice), inside the kernel.
-    const bool swap = M <= 64;
+    // A tuned plan for this exact shape (single matrices only) replaces the
+    // rules below; a transposed plan that cannot hold M is ignored.
+    TunePlan tp;
+    bool tuned = g.batch == 1 && tune_lookup(1, M, N, K, &tp);
+    if (tuned && tp.variant == 3 && M > (tp.bn ? tp.bn : 64)) tuned = false;
+    info->tuned = tuned;
+    const bool swap = tuned ? tp.variant == 3 : M <= 64;
     int bn;
     if (swap) {
-        bn = M <= 32 ? 32 : 64;
+        bn = (tuned && tp.bn) ? tp.bn : (M <= 32 ? 32 : 64);
     } else {
         // Few tiles of 128 x 256: 128 x 128 tiles put twice as many SMs to work
         // streaming B (measured at 128 x 11008 x 4096: 36.5 us vs 48.8 us).
         const long long t256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256) * g.batch;
         bn = (N > 128 && t256 >= sms / 2) ? 256 : 128;
+        if (tuned && tp.variant == 2 && tp.bn) bn = tp.bn;
     }
     const int bn_tile = swap ? kBM : bn;
     a.tiles_m = swap ? 1 : (M + kBM - 1) / kBM;
@@ -1191,6 +1198,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     int splits = 1;
     if (tiles * 3 < sms) splits = std::max(1, std::min((sms * 2 / 3) / tiles, a.kb_total / 2));
     splits = std::min(splits, 32);
+    if (tuned && tp.variant != 1 && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, a.kb_total / 2)));
     a.splits = splits;
     a.units = tiles * splits;
     // Stream-K for the partial last wave is implemented (next_unit) but off:
@@ -1211,7 +1219,8 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     // tile width is picked from {256, 224, 192} by waves x time per tile,
     // time per tile ~ (BN + 64): 4096 columns split 19 x 224 give exactly
     // four pair tiles per SM pair on 152 SMs where 256 gives 3.4.
-    if (!swap && M > kBM && sms >= 2) {
+    const bool try_pair = tuned ? tp.variant == 1 : (!swap && M > kBM);
+    if (try_pair && sms >= 2) {
         const int pairs = sms / 2;
         const int rows2 = (M + 2 * kBM - 1) / (2 * kBM);
         int best_bn = 0;
@@ -1224,8 +1233,9 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
                 best_cost = cost;
             }
         }
+        if (tuned && tp.bn) best_bn = tp.bn;
         const int t2 = rows2 * ((N + best_bn - 1) / best_bn) * g.batch;
-        if (t2 * 2 >= pairs) {
+        if (tuned || t2 * 2 >= pairs) {
             a.tiles_m = rows2;
             a.tiles_n = (N + best_bn - 1) / best_bn;
             a.splits = 1;

@@ -26,6 +26,15 @@ cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **
 // Device address of the current device's watchdog word.
 unsigned *watchdog_word();
 
+// Tuned plan for one exact shape, installed through gemm_tune_set (see the
+// header for the meaning of the fields).  path 0: FP32 CUDA-core GEMM,
+// path 1: tensor-core GEMM (single matrix).  Returns false when no entry
+// matches; the planner then uses its own rules.
+struct TunePlan {
+    int variant = 0, bn = 0, splits = 0;
+};
+bool tune_lookup(int path, int M, int N, int K, TunePlan *out);
+
 int device_sm_count();  // multiprocessors of the current device
 int current_device_id();  // -1 if none
 
@@ -46,6 +55,7 @@ cudaError_t ensure_dynamic_smem(Kernel kern, int bytes, unsigned long long &done
 struct CallInfo {
     const char *plan = "none";
     int launches = 0;
+    bool tuned = false;  // the plan came from the tuning table
 };
 
 // ---- FP32 path (sgemm.cu) ----

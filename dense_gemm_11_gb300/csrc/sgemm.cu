@@ -866,7 +866,12 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
     // tiles of the last partial wave shared out by k slices (stream-K), so
     // every SM gets the same number of k slices.
     const int tiles_big = ((M + 127) / 128) * ((N + 255) / 256);
-    const bool big = tiles_big >= sms || static_cast<long long>(tiles_big) * KT >= 4LL * sms;
+    bool big = tiles_big >= sms || static_cast<long long>(tiles_big) * KT >= 4LL * sms;
+    TunePlan tp;
+    if (tune_lookup(0, M, N, K, &tp)) {  // a tuned plan for this exact shape
+        big = tp.variant == 1;
+        info->tuned = true;
+    }
     cudaError_t e;
     if (big) {
         a.tiles_m = (M + 127) / 128;
@@ -914,6 +919,7 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         int splits = 1;
         if (tiles < 4 * sms) splits = std::max(1, std::min((4 * sms + tiles - 1) / tiles, KT / 2));
         splits = std::min(splits, 16);
+        if (info->tuned && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, KT / 2)));
         a.splits = splits;
         if (splits > 1) {
             Scratch sc;

@@ -226,6 +226,51 @@ GEMM11_API int gemm_tc_strided_batched(int batch, int M, int N, int K, float alp
 GEMM11_API int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const void *A, const void *B,
                                                 float beta, float *C, const float *bias, int act, void *stream);
 
+/*
+ * Tuned plans.  The planners pick a kernel family, tile width and split-K
+ * factor from the shape by fixed rules; a tuning table replaces those rules
+ * for exact shapes.  The pages tune the same parameters per shape and per GPU
+ * ("SGEMM优化，从naive到warptiling", kernel 9 autotuning and Q10; the DeepGEMM
+ * essay "企业官网建设流程全解析", section 1.3, searches tile sizes for the
+ * fixed shapes of an inference service).  dense_gemm_11_gb300/autotune.py
+ * times the candidates on the GPU and writes such a table.
+ *   path     GEMM_PATH_F32: gemm_f32 (M > 1 and N > 1; the GEMV shapes are
+ *            not tunable); GEMM_PATH_TC: the tensor-core entry points for a
+ *            single matrix (any input/output type; batches are not looked up).
+ *   M, N, K  the exact shape.
+ *   variant  GEMM_PATH_F32: 1 = 128 x 256 persistent tiles with stream-K,
+ *              2 = 64 x 64 tiles with `splits` K slices (0: the planner's count).
+ *            GEMM_PATH_TC: 1 = CTA pairs, bn in {256, 224, 192};
+ *              2 = single-CTA 128-row tiles, bn in {256, 128}, `splits` K slices;
+ *              3 = transposed small-M product (needs M <= bn), bn in {32, 64},
+ *              `splits` K slices.
+ *   bn       tile width (0: the planner's choice within the family).
+ *   splits   split-K factor, 0..32 (0: the planner's rule; clipped to half
+ *            the number of 64-wide k blocks).
+ * An entry whose family cannot run the shape it names (variant 3 with
+ * M > bn) is ignored at call time.  Results are identical in value across
+ * plans only up to the accumulation order.
+ */
+typedef enum { GEMM_PATH_F32 = 0, GEMM_PATH_TC = 1 } gemm_tune_path;
+typedef struct {
+    int path, M, N, K;
+    int variant, bn, splits;
+} gemm_tune_entry;
+
+/*
+ * gemm_tune_set -- replace the process-wide tuning table with entries[0..n)
+ * (n = 0 clears it; later entries for the same path and shape win).  Returns
+ * GEMM_ERR_INVALID_ARG, leaving the table unchanged, if n < 0, entries is
+ * NULL with n > 0, or an entry has an unknown path or variant, a tile width
+ * outside its family's list, a negative size or splits outside 0..32.
+ * Thread-safe; takes effect for calls made after it returns.
+ */
+GEMM11_API int gemm_tune_set(const gemm_tune_entry *entries, int n);
+
+/* gemm_tune_get -- copy up to `capacity` entries of the table to `out`;
+ * returns the number of entries in the table. */
+GEMM11_API int gemm_tune_get(gemm_tune_entry *out, int capacity);
+
 /* Text for a gemm_status value (static storage, never NULL). */
 GEMM11_API const char *gemm_status_string(int status);
 

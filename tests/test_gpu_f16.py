@@ -163,3 +163,50 @@ def test_activation_accuracy_on_exact_preactivations(act):
     err = np.abs(got.astype(np.float64) - ref)
     bound = 1e-6 * np.abs(x) + 1e-7 if act != 2 else np.zeros_like(x)
     assert np.all(err <= bound), f"act {act} [{plan}]: max err {err.max():.3e} at x={x.flat[np.argmax(err - bound)]}"
+
+
+@pytest.mark.parametrize("variant,bn,splits", [(1, 256, 0), (1, 224, 0), (1, 192, 0), (2, 256, 1), (2, 128, 3),
+                                               (2, 256, 5), (3, 32, 1), (3, 64, 4)])
+def test_tuned_plans_are_exact(variant, bn, splits):
+    # Every plan a tuning table can force computes the same exact result on
+    # small integers (M = 24 fits every family, including the transposed one).
+    M, N, K = 24, 1000, 1024
+    d = inputs.make(M, N, K, kind="f16", dist="smallint", seed=45, beta=1.0)
+    try:
+        g.tune_set([dict(path=g.GEMM_PATH_TC, M=M, N=N, K=K, variant=variant, bn=bn, splits=splits)])
+        got, plan = run_f16(d, 1.0, 1.0)
+    finally:
+        g.tune_set([])
+    assert plan.endswith("+tuned"), plan
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=1.0, with_scale=False)
+    np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
+
+
+def test_tuned_plan_ignored_when_it_cannot_run():
+    M, N, K = 100, 264, 128  # M > 64: the transposed family cannot hold it
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=46)
+    try:
+        g.tune_set([dict(path=g.GEMM_PATH_TC, M=M, N=N, K=K, variant=3, bn=64, splits=2)])
+        got, plan = run_f16(d, 1.0, 0.0)
+    finally:
+        g.tune_set([])
+    assert "+tuned" not in plan
+    ref, S = oracle.gemm(d["A"], d["B"], None)
+    assert_within(got, ref, S, TOL_F16, plan)
+
+
+def test_autotune_writes_a_usable_table(tmp_path):
+    from dense_gemm_11_gb300 import autotune
+    out = tmp_path / "table.json"
+    doc = autotune.main(["--shape", "tc:48x2048x1024", "--shape", "f32:192x320x256", "--min-gain", "-1",
+                         "--out", str(out)])
+    assert len(doc["entries"]) == 2 and len(doc["reports"]) == 2
+    try:
+        assert g.load_tuning(str(out)) == 2
+        d = inputs.make(48, 2048, 1024, kind="f16", dist="smallint", seed=47)
+        got, plan = run_f16(d, 1.0, 0.0)
+        assert plan.endswith("+tuned")
+        ref, _ = oracle.gemm(d["A"], d["B"], None, with_scale=False)
+        np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
+    finally:
+        g.tune_set([])

@@ -191,3 +191,20 @@ def test_f32_two_streams():
     for d, t in ((d1, t1), (d2, t2)):
         ref, S = oracle.gemm(d["A"], d["B"], None, alpha=1.0, beta=0.0)
         assert_within(t[2].cpu().numpy(), ref, S, TOL_F32, "two streams")
+
+
+@pytest.mark.parametrize("variant,splits", [(1, 0), (2, 1), (2, 4), (2, 16)])
+def test_tuned_f32_plans_are_exact(variant, splits):
+    M, N, K = 300, 520, 1000
+    d = inputs.make(M, N, K, kind="f32", dist="smallint", seed=48, beta=1.0)
+    A, B, C = (torch.from_numpy(d[k]).to(DEV) for k in ("A", "B", "C"))
+    try:
+        g.tune_set([dict(path=g.GEMM_PATH_F32, M=M, N=N, K=K, variant=variant, bn=0, splits=splits)])
+        g.gemm_f32(A, B, C, alpha=1.0, beta=1.0)
+        torch.cuda.synchronize()
+        plan = g.last_plan()
+    finally:
+        g.tune_set([])
+    assert plan.endswith("+tuned"), plan
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=1.0, with_scale=False)
+    np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), ref, err_msg=plan)
