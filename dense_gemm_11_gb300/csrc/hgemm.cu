@@ -1191,12 +1191,12 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     const long long tiles_ll = static_cast<long long>(a.tiles_m) * a.tiles_n * g.batch;
     if (tiles_ll > (1LL << 26)) return cudaErrorNotSupported;  // keeps every unit index and counter in int
     const int tiles = static_cast<int>(tiles_ll);
-    // K is split only while the tiles fill less than a third of the SMs; the
-    // memory-bound small-M shapes stream B fastest from about half the SMs
-    // without the partial-tile round trip (measured: 16 x 4096 x 4096 is best
-    // at 3 splits of 32 tiles, 128 x 11008 x 4096 with no split of 86 tiles).
+    // K is split only while the tiles fill less than a third of the SMs, into
+    // at most one unit per SM (measured: 16 x 4096 x 4096 is best at 4
+    // splits of 32 tiles, 15.7 us; 128 x 11008 x 4096 with no split of 86
+    // tiles).
     int splits = 1;
-    if (tiles * 3 < sms) splits = std::max(1, std::min((sms * 2 / 3) / tiles, a.kb_total / 2));
+    if (tiles * 3 < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
     splits = std::min(splits, 32);
     if (tuned && tp.variant != 1 && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, a.kb_total / 2)));
     a.splits = splits;

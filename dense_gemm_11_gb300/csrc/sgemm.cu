@@ -862,11 +862,14 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
     }
 
     // Tile table.  128x256 CTAs (8 warps, one per SM) run persistently when
-    // there is enough work for every SM: whole tiles round-robin, and the
-    // tiles of the last partial wave shared out by k slices (stream-K), so
-    // every SM gets the same number of k slices.
+    // there are big tiles for at least ~80 % of the SMs: whole tiles
+    // round-robin, and the tiles of the last partial wave shared out by k
+    // slices (stream-K), so every SM gets the same number of k slices.
+    // Fewer big tiles run faster as 64x64 tiles (autotuner on GB300:
+    // 1024^3 51.2 vs 53.6 us, 1000 x 3000 x 777 102.8 vs 110.2 us;
+    // 2048^3 with 128 big tiles stays big: 295 vs 320 us).
     const int tiles_big = ((M + 127) / 128) * ((N + 255) / 256);
-    bool big = tiles_big >= sms || static_cast<long long>(tiles_big) * KT >= 4LL * sms;
+    bool big = 5 * tiles_big >= 4 * sms;
     TunePlan tp;
     if (tune_lookup(0, M, N, K, &tp)) {  // a tuned plan for this exact shape
         big = tp.variant == 1;
@@ -910,14 +913,17 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         else
             info->plan = repacked ? "sgemm_repack_128x256_vec16" : (vec ? "sgemm_128x256_vec16" : "sgemm_128x256_vec4b");
     } else {
-        // Small problems: 64x64 CTAs (4 warps of 32x32, 4x8 per thread), several
-        // per SM, with K split so that there are about four CTAs per SM, each
-        // split at least two 32-wide k slices.
+        // Small problems: 64x64 CTAs (4 warps of 32x32, 4x8 per thread), with
+        // K split so that there are about as many CTAs as SMs, each split at
+        // least two 32-wide k slices, and no split at all for K <= 128 (the
+        // partial-tile round trip costs more than it gains there).  Measured
+        // on GB300: 512^3 13.0 us at 2 splits (20.3 us at 8), 256^3 8.8 us at
+        // 4, 128^3 6.1 us unsplit (7.4 us at 2).
         a.tiles_m = (M + 63) / 64;
         a.tiles_n = (N + 63) / 64;
         const int tiles = a.tiles_m * a.tiles_n;
         int splits = 1;
-        if (tiles < 4 * sms) splits = std::max(1, std::min((4 * sms + tiles - 1) / tiles, KT / 2));
+        if (tiles < sms && KT > 4) splits = std::max(1, std::min((sms + tiles / 2) / tiles, KT / 2));
         splits = std::min(splits, 16);
         if (info->tuned && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, KT / 2)));
         a.splits = splits;
@@ -931,9 +937,10 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         e = vec ? launch_tiled<64, 64, 2, 2, 4, 8, 3, true, false>(a, stream)
                 : launch_tiled<64, 64, 2, 2, 4, 8, 3, false, false>(a, stream);
         if (splits > 1)
-            info->plan = vec ? "sgemm_64x64_vec16_splitk" : "sgemm_64x64_vec4b_splitk";
+            info->plan = repacked ? "sgemm_repack_64x64_vec16_splitk"
+                                  : (vec ? "sgemm_64x64_vec16_splitk" : "sgemm_64x64_vec4b_splitk");
         else
-            info->plan = vec ? "sgemm_64x64_vec16" : "sgemm_64x64_vec4b";
+            info->plan = repacked ? "sgemm_repack_64x64_vec16" : (vec ? "sgemm_64x64_vec16" : "sgemm_64x64_vec4b");
         info->launches = 1 + repacked;
     }
     return e;
