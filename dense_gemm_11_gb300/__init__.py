@@ -376,6 +376,11 @@ def tune_get() -> list:
     return [arr[i].as_dict() for i in range(n)]
 
 
+def default_tuning_path() -> str:
+    """The tuning table shipped for GB300 (written by ``autotune`` on one)."""
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "tuning", "gb300.json")
+
+
 def load_tuning(path: str) -> int:
     """Install the table stored by ``autotune`` in a JSON file; returns the entry count."""
     import json

@@ -182,3 +182,11 @@ def test_tuning_table_roundtrip_and_validation(L):
     finally:
         g.tune_set([])
     assert g.tune_get() == []
+
+
+def test_shipped_tuning_table_installs(L):
+    try:
+        n = g.load_tuning(g.default_tuning_path())
+        assert n == len(g.tune_get()) and n >= 0
+    finally:
+        g.tune_set([])
