@@ -372,11 +372,12 @@ def run_profile_case(case: str, repeats: int):
     import dense_gemm_11_gb300 as g
     from dense_gemm_11_gb300 import inputs
     dev = torch.device("cuda", 0)
-    if case == "sgemm":
+    if case in ("sgemm", "tf32x3"):
         d = inputs.make_workload(inputs.WORKLOADS["f32_sq4096"])
         A, B, C = (torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C"))
+        fn = g.gemm_f32 if case == "sgemm" else g.gemm_f32_3xtf32
         for _ in range(repeats):
-            g.gemm_f32(A, B, C, alpha=1.0, beta=3.0)
+            fn(A, B, C, alpha=1.0, beta=3.0)
     else:
         d = inputs.make_workload(inputs.WORKLOADS["f16_4096"])
         A, B = (torch.from_numpy(d[k]).to(dev) for k in ("A", "B"))
@@ -512,7 +513,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["sgemm", "hgemm"], default=None,
+    ap.add_argument("--profile-case", choices=["sgemm", "hgemm", "tf32x3"], default=None,
                     help="launch one 4096^3 GEMM of the workload a few times (for ncu) and exit")
     ap.add_argument("--repeats", type=int, default=2)
     ap.add_argument("--sweep", action="store_true", help="time every named workload, one JSON line each")

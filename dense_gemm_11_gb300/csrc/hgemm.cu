@@ -1217,10 +1217,12 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     }
     // CTA pairs: M > 128 with enough 256-row pair tiles for the SMs.  The
     // tile width is picked from {256, 224, 192} by the number of waves of
-    // pair tiles, then by the columns computed (padding): a wave takes the
-    // same time at all three widths (measured ~24 us per wave at K = 4096,
-    // within 1.5 %), so 4096 x 11008 x 4096 runs 43 x 256 in 10 waves
-    // (238 us) rather than 50 x 224 in 11 (266 us).
+    // pair tiles, then the narrowest: a tile takes nearly the same time at all
+    // three widths (each CTA loads the same 64-column B boxes per k block;
+    // measured ~24 us per wave at K = 4096), so 4096 x 11008 x 4096 runs
+    // 43 x 256 in 10 waves (238 us) rather than 50 x 224 in 11 (266 us),
+    // while 4096^3 runs 19 x 224 in 4 full waves (87 us; 256-wide tiles also
+    // take 4 waves, the last one 37 % full: 91 us).
     const bool try_pair = tuned ? tp.variant == 1 : (!swap && M > kBM);
     if (try_pair && sms >= 2) {
         const int pairs = sms / 2;
@@ -1230,8 +1232,8 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
         for (int cand : {256, 224, 192}) {
             const long long tn = (N + cand - 1) / cand;
             const long long t2 = static_cast<long long>(rows2) * tn * g.batch;
-            // waves first; among equal waves, fewer padded columns
-            const double cost = static_cast<double>((t2 + pairs - 1) / pairs) * 1e9 + static_cast<double>(tn * cand);
+            // waves first; among equal waves, the narrower tile
+            const double cost = static_cast<double>((t2 + pairs - 1) / pairs) * 1e9 + static_cast<double>(cand);
             if (best_bn == 0 || cost < best_cost - 1e-9) {
                 best_bn = cand;
                 best_cost = cost;
