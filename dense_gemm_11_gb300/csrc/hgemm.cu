@@ -891,7 +891,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         // round-to-nearest; the tensor core's own accumulation is truncated,
         // so keeping its sums short keeps the total within FP32's error level
         // for any K.
-        static_assert(!X3 || (EPI == 8 && BN == 256), "FP32-accuracy mode: 8 epilogue warps, 256 columns");
+        static_assert(!X3 || (EPI == 8 && BN / 32 <= 8), "FP32-accuracy mode: 8 epilogue warps, <= 256 columns");
+        constexpr int kGroups = BN / 32;  // 32-column groups of a tile; warp half h owns [4h, 4h + 4)
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
         const int g0 = ((warp - 2) >> 2) * 4;  // first of this warp's 4 column groups
@@ -920,6 +921,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
 #pragma unroll
                 for (int gh = 0; gh < 8; ++gh) {  // half groups of 16 columns (fewer live registers)
                     const int gi = gh >> 1, j0 = (gh & 1) * 16;
+                    if (g0 + gi >= kGroups) continue;
                     uint32_t r[16];
                     tmem_ld_32x32b_x16(t_row + (g0 + gi) * 32 + j0, r);
                     tmem_wait_ld();
@@ -944,6 +946,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             const int grow = my_m + row_in_tile;
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi) {
+                if (g0 + gi >= kGroups) continue;
                 const int col0 = n0 + (g0 + gi) * 32;
                 epilogue_row_chunk(tot[gi], p, grow, col0, cbase);
                 store_row_chunk<Cfg::kNBuf>(tot[gi], p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0, bz);
@@ -1395,7 +1398,20 @@ cudaError_t run_gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
     e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
 
-    constexpr int BN = 256;
+    // Pair tile width by the planner's rule for CTA pairs: fewest waves, then
+    // the narrowest of {256, 224, 192}.
+    const int pairs = std::max(1, sms / 2);
+    const int rows2 = (M + 2 * kBM - 1) / (2 * kBM);
+    int BN = 0;
+    long long best_waves = 0;
+    for (int cand : {256, 224, 192}) {
+        const long long t2c = static_cast<long long>(rows2) * ((N + cand - 1) / cand);
+        const long long waves = (t2c + pairs - 1) / pairs;
+        if (BN == 0 || waves <= best_waves) {
+            BN = cand;
+            best_waves = waves;
+        }
+    }
     HgemmArgs a{};
     a.M = M;
     a.N = N;
@@ -1428,8 +1444,16 @@ cudaError_t run_gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
         !encode_3d(&tb2, f32, 4, bt_lo, K, N, 1, Kp, 0, 32, BN / 2) || !encode_c(&tc, g, ldc))
         return cudaErrorNotSupported;
     int used = 0;
-    e = launch_hgemm_pair<BN, 3, 8, true>(ta, tb, tc, a, stream, &used, &ta2, &tb2);
-    info->plan = "tf32x3_pair_256x256";
+    if (BN == 256) {
+        e = launch_hgemm_pair<256, 3, 8, true>(ta, tb, tc, a, stream, &used, &ta2, &tb2);
+        info->plan = "tf32x3_pair_256x256";
+    } else if (BN == 224) {
+        e = launch_hgemm_pair<224, 3, 8, true>(ta, tb, tc, a, stream, &used, &ta2, &tb2);
+        info->plan = "tf32x3_pair_256x224";
+    } else {
+        e = launch_hgemm_pair<192, 3, 8, true>(ta, tb, tc, a, stream, &used, &ta2, &tb2);
+        info->plan = "tf32x3_pair_256x192";
+    }
     info->launches = 3;
     return e;
 }
