@@ -80,18 +80,28 @@ __host__ __device__ constexpr int tmem_cols_for(int bn) {
     return (2 * bn <= 32) ? 32 : (2 * bn <= 64) ? 64 : (2 * bn <= 128) ? 128 : (2 * bn <= 256) ? 256 : 512;
 }
 
-template <int BN, int STAGES, bool SWAP>
+// CSPLIT: the K splits of a tile are the CTAs of one thread-block cluster,
+// and the partial tiles are added through distributed shared memory: each
+// CTA puts its 128 x BN fp32 partial in its own shared memory, and CTA r of
+// the cluster sums rows [r * 128 / s, (r + 1) * 128 / s) of all s partials
+// (in split order) and writes them to C.  Two cluster-wide mbarriers per CTA
+// hand the partial buffer over: "ready" (every CTA's partial is written) and
+// "consumed" (every CTA has read this CTA's partial).  No global scratch,
+// atomics or memory fences.
+template <int BN, int STAGES, bool SWAP, bool CSPLIT = false>
 struct HgemmCfg {
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows of 128 B
     static constexpr int kBBytes = BN * kBK * 2;   // BN rows (or k-rows) of 128 B
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kCStageBytes = SWAP ? 0 : kEpiWarps * 2 * 32 * 32 * 4;  // 2 x 4 KB per warp
-    static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+    static constexpr int kCStageBytes =
+        CSPLIT ? kBM * BN * 4 : (SWAP ? 0 : kEpiWarps * 2 * 32 * 32 * 4);  // partial tile, or 2 x 4 KB per warp
+    static constexpr int kBarBytes = (2 * STAGES + 7) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
     static constexpr int kTmemCols = tmem_cols_for(BN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (and 32-column TMEM reads)");
     static_assert(SWAP || BN % 64 == 0, "B tile is loaded in 64-column boxes");
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
+    static_assert(!CSPLIT || SWAP, "cluster split-K is the transposed small-M variant's");
 };
 
 
@@ -314,11 +324,11 @@ __device__ __forceinline__ float epi_value(float acc, const HgemmArgs &p, float 
     return v;
 }
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, bool CSPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const HgemmArgs p) {
-    using Cfg = HgemmCfg<BN, STAGES, SWAP>;
+    using Cfg = HgemmCfg<BN, STAGES, SWAP, CSPLIT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;                                 // STAGES x 16 KB (MMA operand A)
@@ -330,7 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tfull = bars + 2 * STAGES;                // MMA -> epilogue, per accumulator
     uint64_t *tempty = bars + 2 * STAGES + 2;           // epilogue -> MMA, per accumulator
     uint64_t *mma_done = bars + 2 * STAGES + 4;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    uint64_t *part_ready = bars + 2 * STAGES + 5;     // CSPLIT: every CTA's partial written
+    uint64_t *part_consumed = bars + 2 * STAGES + 6;  // CSPLIT: every CTA has read this partial
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 7);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -347,6 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        if (CSPLIT) {
+            mbar_init(part_ready, p.splits * kEpiWarps * 32);
+            mbar_init(part_consumed, p.splits * kEpiWarps * 32);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -360,7 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (CSPLIT)
+        cluster_sync();  // every CTA's hand-over barriers exist before any remote arrive
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -488,8 +507,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             // or the raw partial to scratch (split K).
             // A unit leaves a partial tile when K is split evenly (splits > 1) or
             // when it covers only part of a stream-K tile (slot >= 0).
-            const bool partial = (p.splits > 1) || (c.slot >= 0);
             const size_t cbase = static_cast<size_t>(c.batch) * static_cast<size_t>(p.stride_c);
+            if constexpr (CSPLIT) {
+                // 1. this CTA's partial -> own shared memory, [column][row]
+                float *part = reinterpret_cast<float *>(sC);
+                if (local > 0 && !mbar_wait_cluster(part_consumed, (local - 1) & 1)) {
+                    flag_timeout(abort_flag, p.err);
+                    break;
+                }
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + ch * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) part[(ch * 32 + j) * kBM + row_in_tile] = __uint_as_float(r[j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                const int nsp = p.splits;
+                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), r));
+                // 2. rows [rank * R, rank * R + R) of the sum of all partials, in split order
+                if (!mbar_wait_cluster(part_ready, local & 1)) {
+                    flag_timeout(abort_flag, p.err);
+                    break;
+                }
+                const int R = kBM / nsp;                 // rows reduced by this CTA
+                const int et = threadIdx.x - 64;         // epilogue thread 0..127
+                const int rr = c.split * R + et % R;     // tile row = column n of C
+                const int ncol = BN / nsp;               // columns (rows m of C) per thread
+                const int j0 = (et / R) * ncol;
+                const uint32_t part_addr = smem_u32(part);
+                float acc[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) acc[jj] = 0.f;
+                for (int src = 0; src < nsp; ++src) {
+                    const uint32_t base = mapa_shared(part_addr, src);
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (jj < ncol) acc[jj] += ld_shared_cluster_f32(base + ((j0 + jj) * kBM + rr) * 4);
+                }
+                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_consumed), r));
+                const int gn = c.n0 + rr;
+                if (gn < p.N) {
+                    const float b = p.bias ? __ldg(p.bias + gn) : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int gm = j0 + jj;
+                        if (jj < ncol && gm < p.M) {
+                            const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
+                            const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
+                            store_out(p.C, ci, p.c_type, epi_value(acc[jj], p, cold, b));
+                        }
+                    }
+                }
+                continue;
+            }
+            const bool partial = (p.splits > 1) || (c.slot >= 0);
             float *part = nullptr;
             if (partial)
                 part = p.ws + (c.slot >= 0 ? static_cast<size_t>(c.slot)
@@ -634,6 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) p.counters[cnt_idx] = 0u;
                 }
             }
+        }
+        if (CSPLIT && local > 0 && !*abort_flag) {
+            // the peers must have read this CTA's last partial before it exits
+            if (!mbar_wait_cluster(part_consumed, (local - 1) & 1)) flag_timeout(abort_flag, p.err);
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -1079,11 +1158,11 @@ bool encode_b(CUtensorMap *map, const TcGemm &g, CUtensorMapDataType dt, uint32_
     return encode_3d(map, dt, 2, g.B, g.N, g.K, g.stride_b ? g.batch : 1, g.N, g.stride_b, 64, kBK);
 }
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, bool CSPLIT = false>
 cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const HgemmArgs &a,
                          int grid, cudaStream_t stream) {
-    using Cfg = HgemmCfg<BN, STAGES, SWAP>;
-    auto kern = hgemm_tc_kernel<BN, STAGES, SWAP>;
+    using Cfg = HgemmCfg<BN, STAGES, SWAP, CSPLIT>;
+    auto kern = hgemm_tc_kernel<BN, STAGES, SWAP, CSPLIT>;
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
@@ -1093,6 +1172,24 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     HgemmArgs args = a;
     const int b_mn = a.b_kmajor ? 0 : 1;
     args.idesc = (SWAP ? umma_idesc_f16_f32(kBM, BN, b_mn, 0) : umma_idesc_f16_f32(kBM, BN, 0, b_mn)) | a.idesc_fmt;
+    if constexpr (CSPLIT) {
+        // clusters of `splits` CTAs, one K split each (the grid is a multiple of it)
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(a.splits);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
+        if (e != cudaSuccess) return e;
+        return cudaPeekAtLastError();
+    }
     kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, tc, args);
     return cudaPeekAtLastError();
 }
@@ -1194,12 +1291,14 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     const long long tiles_ll = static_cast<long long>(a.tiles_m) * a.tiles_n * g.batch;
     if (tiles_ll > (1LL << 26)) return cudaErrorNotSupported;  // keeps every unit index and counter in int
     const int tiles = static_cast<int>(tiles_ll);
-    // K is split only while the tiles fill less than a third of the SMs, into
-    // at most one unit per SM (measured: 16 x 4096 x 4096 is best at 4
-    // splits of 32 tiles, 15.7 us; 128 x 11008 x 4096 with no split of 86
-    // tiles).
+    // K is split into at most one unit per SM while the tiles fill less than
+    // a third of the SMs -- half for the transposed plan, whose splits are
+    // added through distributed shared memory (measured: 16 x 4096 x 4096 is
+    // best at 4 splits of 32 tiles, 15.7 us; 32 x 8192 x 8192 at 2 splits of
+    // 64 tiles, 30.4 us against 41.7 us unsplit; 128 x 11008 x 4096 with no
+    // split of 86 tiles).
     int splits = 1;
-    if (tiles * 3 < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
+    if (swap ? tiles * 2 <= sms : tiles * 3 < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
     splits = std::min(splits, 32);
     if (tuned && tp.variant != 1 && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, a.kb_total / 2)));
     a.splits = splits;
@@ -1274,6 +1373,27 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     // (Stream-K over all SMs for these memory-bound M <= 128 shapes measured
     // slower: 45.8 us vs 35.6 us at 128 x 11008 x 4096, the partial-tile
     // round trip costs more than the extra SMs gain.)
+    // The transposed small-M plan splits K over the CTAs of a cluster and adds
+    // the partials through distributed shared memory (2, 4 or 8 splits).
+    if (swap && splits > 1) {
+        int cs = 1;
+        while (cs * 2 <= std::min(splits, 8)) cs *= 2;
+        a.splits = cs;
+        a.units = tiles * cs;
+        const int grid = std::min(a.units, (sms / cs) * cs);
+        CUtensorMap ta, tb;
+        if (!encode_a(&ta, g, in_dt, bn) || !encode_b(&tb, g, in_dt, kBM)) return cudaErrorNotSupported;
+        cudaError_t e;
+        if (bn == 32) {
+            e = launch_hgemm<32, 8, true, true>(ta, tb, tb, a, grid, stream);
+            info->plan = "tc_swap_n32_clusterk";
+        } else {
+            e = launch_hgemm<64, 8, true, true>(ta, tb, tb, a, grid, stream);
+            info->plan = "tc_swap_n64_clusterk";
+        }
+        info->launches = 1;
+        return e;
+    }
     if (splits > 1) {
         Scratch sc;
         cudaError_t e =

@@ -326,6 +326,37 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Wait for a phase of this CTA's mbarrier whose arrivals were released by
+// other CTAs of the cluster (cluster-scope acquire).  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(a, parity)) return true;
+        if ((it & 255u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+// Load a float from the shared memory of a CTA of the cluster (address from mapa).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
 // 2-D tiled load into this CTA's shared memory whose completion is counted on
 // an mbarrier that may live in the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap *map, uint32_t mbar_cluster_addr, void *smem_dst,

@@ -166,7 +166,8 @@ def test_activation_accuracy_on_exact_preactivations(act):
 
 
 @pytest.mark.parametrize("variant,bn,splits", [(1, 256, 0), (1, 224, 0), (1, 192, 0), (2, 256, 1), (2, 128, 3),
-                                               (2, 256, 5), (3, 32, 1), (3, 64, 4)])
+                                               (2, 256, 5), (3, 32, 1), (3, 64, 4), (3, 32, 2), (3, 64, 8),
+                                               (3, 32, 3)])
 def test_tuned_plans_are_exact(variant, bn, splits):
     # Every plan a tuning table can force computes the same exact result on
     # small integers (M = 24 fits every family, including the transposed one).
@@ -210,3 +211,14 @@ def test_autotune_writes_a_usable_table(tmp_path):
         np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
     finally:
         g.tune_set([])
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 4096), (1, 4096, 2048), (64, 1000, 3000), (33, 136, 8192)])
+def test_f16_cluster_split_k(M, N, K):
+    # Small M with few tiles: K is split over the CTAs of a cluster and the
+    # partials are added through distributed shared memory.
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=M + N + K, beta=0.5, bias=True)
+    got, plan = run_f16(d, 1.25, 0.5, d["bias"], 1)
+    assert "clusterk" in plan, plan
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.25, beta=0.5, bias=d["bias"], act=1)
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
