@@ -382,6 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything above (barriers, tensor memory, descriptor prefetch) may
+    // overlap the previous kernel of the stream; global memory only below.
+    pdl_wait();
+    pdl_launch_dependents();
 
     uint32_t armed = 0, armed_parity = 0;  // producer bookkeeping for the final drain
 
@@ -852,6 +856,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything above (barriers, tensor memory, descriptor prefetch) may
+    // overlap the previous kernel of the stream; global memory only below.
+    pdl_wait();
+    pdl_launch_dependents();
 
     uint32_t armed = 0, armed_parity = 0;
 
@@ -1172,25 +1180,26 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     HgemmArgs args = a;
     const int b_mn = a.b_kmajor ? 0 : 1;
     args.idesc = (SWAP ? umma_idesc_f16_f32(kBM, BN, b_mn, 0) : umma_idesc_f16_f32(kBM, BN, 0, b_mn)) | a.idesc_fmt;
-    if constexpr (CSPLIT) {
-        // clusters of `splits` CTAs, one K split each (the grid is a multiple of it)
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(a.splits);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
-        if (e != cudaSuccess) return e;
-        return cudaPeekAtLastError();
-    }
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, tc, args);
+    // Programmatic dependent launch: the prologue may overlap the previous
+    // kernel (the kernel waits in pdl_wait before touching global memory);
+    // with CSPLIT, clusters of `splits` CTAs, one K split each (the grid is a
+    // multiple of it).
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CSPLIT ? static_cast<unsigned>(a.splits) : 1u;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = CSPLIT ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
+    if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
 
@@ -1204,11 +1213,13 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // prologue may overlap the previous kernel
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(Cfg::kThreadsPair, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
@@ -1229,6 +1240,7 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     HgemmArgs args = a;
     args.idesc = X3 ? umma_idesc_f16_f32(2 * kBM, BN, 0, 0) | kIdescTf32Operands
                     : umma_idesc_f16_f32(2 * kBM, BN, 0, a.b_kmajor ? 0 : 1) | a.idesc_fmt;
+    cfg.numAttrs = 2;  // the occupancy query above used the cluster shape alone
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, ta2 ? *ta2 : ta, tb2 ? *tb2 : tb, args);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();

@@ -189,6 +189,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in the stream is still running.  pdl_wait blocks until
+// that kernel has completed and its memory operations are visible (so it must
+// come before this kernel's first global-memory access); pdl_launch_dependents
+// lets the next such kernel be scheduled (it still waits in its own pdl_wait).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
