@@ -1521,13 +1521,12 @@ cudaError_t run_gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
     cudaError_t e = acquire_operand_scratch(stream, 2 * a_elems + 2 * b_elems, &ws);
     if (e != cudaSuccess) return e;
     float *a_hi = ws, *a_lo = ws + a_elems, *bt_hi = a_lo + a_elems, *bt_lo = bt_hi + b_elems;
-    split_rows_tf32_kernel<<<std::min(M, 8 * sms), 256, 0, stream>>>(A, lda, M, K, Kp, a_hi, a_lo);
-    e = cudaPeekAtLastError();
+    e = launch_kernel(split_rows_tf32_kernel, dim3(std::min(M, 8 * sms)), dim3(256), 0, stream, A, lda, M, K, Kp, a_hi,
+                   a_lo);
     if (e != cudaSuccess) return e;
     const dim3 tgrid((N + 31) / 32, (Kp + 31) / 32);
     if (tgrid.y > 65535u) return cudaErrorNotSupported;
-    split_cols_tf32_kernel<<<tgrid, 256, 0, stream>>>(B, ldb, K, N, Kp, bt_hi, bt_lo);
-    e = cudaPeekAtLastError();
+    e = launch_kernel(split_cols_tf32_kernel, tgrid, dim3(256), 0, stream, B, ldb, K, N, Kp, bt_hi, bt_lo);
     if (e != cudaSuccess) return e;
 
     // Pair tile width by the planner's rule for CTA pairs: fewest waves, then

@@ -26,6 +26,23 @@ cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **
 // Device address of the current device's watchdog word.
 unsigned *watchdog_word();
 
+// Plain launch through cudaLaunchKernelEx with an error check.  (The grid
+// kernels here are not launched with programmatic stream serialization: their
+// CTAs are placed several per SM, and letting the next kernel's CTAs take
+// free slots early skewed that placement -- 1024^3 FP32 ran 51 -> 77 us.)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaPeekAtLastError();
+}
+
 // Tuned plan for one exact shape, installed through gemm_tune_set (see the
 // header for the meaning of the fields).  path 0: FP32 CUDA-core GEMM,
 // path 1: tensor-core GEMM (single matrix).  Returns false when no entry

@@ -741,8 +741,7 @@ cudaError_t launch_tiled(const SgemmArgs &a, cudaStream_t stream) {
     cudaError_t e = ensure_dynamic_smem(kern, T::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     dim3 grid = PERSIST ? dim3(a.grid_ctas, 1) : dim3(a.tiles_m * a.tiles_n, a.splits);
-    kern<<<grid, T::kThreads, T::kSmemBytes, stream>>>(a);
-    return cudaPeekAtLastError();
+    return launch_kernel(kern, grid, dim3(T::kThreads), T::kSmemBytes, stream, a);
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -758,10 +757,9 @@ cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float
     }
     const long long total = static_cast<long long>(M) * N;
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4LL * device_sm_count()));
-    scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc, bias, act);
     info->plan = "scale_c";
     info->launches = 1;
-    return cudaPeekAtLastError();
+    return launch_kernel(scale_c_kernel, dim3(blocks), dim3(256), 0, stream, M, N, beta, C, ldc, bias, act);
 }
 
 cudaError_t run_scale_c_batched(int batch, int M, int N, float beta, void *C, long long stride_c, int c_type,
@@ -773,10 +771,10 @@ cudaError_t run_scale_c_batched(int batch, int M, int N, float beta, void *C, lo
     }
     const long long total = static_cast<long long>(batch) * M * N;
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4LL * device_sm_count()));
-    scale_c_batched_kernel<<<blocks, 256, 0, stream>>>(M, N, total, beta, C, stride_c, c_type, bias, act);
     info->plan = "scale_c_batched";
     info->launches = 1;
-    return cudaPeekAtLastError();
+    return launch_kernel(scale_c_batched_kernel, dim3(blocks), dim3(256), 0, stream, M, N, total, beta, C, stride_c,
+                      c_type, bias, act);
 }
 
 cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
@@ -784,16 +782,15 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
     const int sms = device_sm_count();
     if (N == 1) {
         const int vec = aligned16(A) && (lda % 4 == 0) && ldb == 1 && aligned16(B);
-        if (vec) {
-            sgemv_rows_block_kernel<<<(M + kRowsPerCta - 1) / kRowsPerCta, 256, 0, stream>>>(M, K, alpha, A, lda, B,
-                                                                                           beta, C, ldc);
-            info->plan = "sgemv_rows_block";
-        } else {
-            sgemv_rows_kernel<<<(M + 7) / 8, 256, 0, stream>>>(M, K, alpha, A, lda, B, ldb, beta, C, ldc, 0);
-            info->plan = "sgemv_rows";
-        }
         info->launches = 1;
-        return cudaPeekAtLastError();
+        if (vec) {
+            info->plan = "sgemv_rows_block";
+            return launch_kernel(sgemv_rows_block_kernel, dim3((M + kRowsPerCta - 1) / kRowsPerCta), dim3(256), 0, stream,
+                              M, K, alpha, A, lda, B, beta, C, ldc);
+        }
+        info->plan = "sgemv_rows";
+        return launch_kernel(sgemv_rows_kernel, dim3((M + 7) / 8), dim3(256), 0, stream, M, K, alpha, A, lda, B, ldb, beta,
+                          C, ldc, 0);
     }
     if (M == 1) {
         const int vec = aligned16(B) && (ldb % 4 == 0);
@@ -806,12 +803,10 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             cudaError_t e = acquire_scratch(stream, static_cast<size_t>(col_blocks) * splits * 128, col_blocks, &sc);
             if (e != cudaSuccess) return e;
         }
-        dim3 grid(col_blocks, splits);
-        sgemv_cols_kernel<<<grid, 256, 0, stream>>>(N, K, alpha, A, B, ldb, beta, C, vec, splits, sc.partials,
-                                                    sc.counters);
         info->plan = splits > 1 ? "sgemv_cols_splitk" : "sgemv_cols";
         info->launches = 1;
-        return cudaPeekAtLastError();
+        return launch_kernel(sgemv_cols_kernel, dim3(col_blocks, splits), dim3(256), 0, stream, N, K, alpha, A, B, ldb, beta,
+                          C, vec, splits, sc.partials, sc.counters);
     }
 
     SgemmArgs a{};
@@ -844,14 +839,16 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         if (e != cudaSuccess) return e;
         const int blocks = 8 * sms;
         if (!a_ok) {
-            repack_rows_kernel<<<blocks, 256, 0, stream>>>(A, M, K, lda, ops, lda2);
+            e = launch_kernel(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, A, M, K, lda, ops, lda2);
+            if (e != cudaSuccess) return e;
             a.A = ops;
             a.lda = lda2;
             ++repacked;
         }
         if (!b_ok) {
             float *B2 = ops + a_floats;  // 256-byte aligned
-            repack_rows_kernel<<<blocks, 256, 0, stream>>>(B, K, N, ldb, B2, ldb2);
+            e = launch_kernel(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, B, K, N, ldb, B2, ldb2);
+            if (e != cudaSuccess) return e;
             a.B = B2;
             a.ldb = ldb2;
             ++repacked;
@@ -903,8 +900,7 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
                 : launch_tiled<128, 256, 2, 4, 8, 16, 3, false, true>(a, stream);
         if (e != cudaSuccess) return e;
         if (a.sk_tiles > 0) {
-            sgemm_streamk_fixup_kernel<128, 256><<<dim3(a.sk_tiles, 128 / 8), 256, 0, stream>>>(a);
-            e = cudaPeekAtLastError();
+            e = launch_kernel(sgemm_streamk_fixup_kernel<128, 256>, dim3(a.sk_tiles, 128 / 8), dim3(256), 0, stream, a);
         }
         info->launches = (a.sk_tiles > 0 ? 2 : 1) + repacked;
         if (a.sk_tiles > 0)
