@@ -148,3 +148,16 @@ def test_batched_alpha_zero_scales_every_matrix():
     torch.cuda.synchronize()
     assert g.last_plan() == "scale_c_batched"
     np.testing.assert_array_equal(C.cpu().numpy(), np.maximum(-2.0 * C0, 0.0))
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("b_trans", [False, True])
+def test_batched_small_m_cluster_split(out, b_trans):
+    # Decode-like batch: 4 matrices of 8 x 2048 x 4096 -> 64 tiles, K split
+    # over clusters; 16-bit or FP32 C with beta and bias.
+    batch, M, N, K = 4, 8, 2048, 4096
+    d = inputs.make_batched(batch, M, N, K, kind="bf16", seed=37, beta=1.5, bias=True, b_trans=b_trans)
+    got, C0, plan = run_batched(d, "bf16", out, 0.5, 1.5, b_trans, act=3)
+    assert "clusterk" in plan, plan
+    ref, S = oracle_batch(d, C0, 0.5, 1.5, b_trans, act=3)
+    assert_within(got, ref, S, TOL_F16, f"{out} trans={b_trans} [{plan}]", out=out)
