@@ -146,7 +146,11 @@ def _mat(t, name, dtype):
         raise ValueError(f"{name} must be 2-D")
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} needs unit column stride")
-    return t.data_ptr(), max(t.stride(0), 1) if t.shape[0] > 1 else max(t.shape[1], 1)
+    # a single row has no row stride of its own: report the tensor's when it is
+    # a valid one (a view keeps its parent's, which may be 16-byte aligned)
+    if t.shape[0] > 1 or t.stride(0) >= t.shape[1]:
+        return t.data_ptr(), max(t.stride(0), 1)
+    return t.data_ptr(), max(t.shape[1], 1)
 
 
 def gemm_f32_raw(M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream_ptr=0) -> int:

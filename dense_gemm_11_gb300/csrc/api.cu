@@ -281,8 +281,10 @@ int gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, c
     if (!C) return GEMM_ERR_INVALID_ARG;
     const bool product = (K > 0) && (alpha != 0.f);
     if (product && (!A || !B)) return GEMM_ERR_INVALID_ARG;
-    // C is written by TMA stores: 16-byte aligned base and rows.
-    if (product && (((reinterpret_cast<uintptr_t>(C) & 15u) != 0) || (ldc % 4) != 0)) return GEMM_ERR_UNSUPPORTED;
+    // C is written by TMA stores: 16-byte aligned base and rows (a single row
+    // has no row stride to align).
+    if (product && (((reinterpret_cast<uintptr_t>(C) & 15u) != 0) || (M > 1 && (ldc % 4) != 0)))
+        return GEMM_ERR_UNSUPPORTED;
     DeviceState *ds = device_state();
     if (!ds) return fail_cuda(cudaErrorInvalidDevice);
     if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);

@@ -1572,7 +1572,8 @@ cudaError_t run_gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
     const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     if (!encode_3d(&ta, f32, 4, a_hi, K, M, 1, Kp, 0, 32, kBM) || !encode_3d(&ta2, f32, 4, a_lo, K, M, 1, Kp, 0, 32, kBM) ||
         !encode_3d(&tb, f32, 4, bt_hi, K, N, 1, Kp, 0, 32, BN / 2) ||
-        !encode_3d(&tb2, f32, 4, bt_lo, K, N, 1, Kp, 0, 32, BN / 2) || !encode_c(&tc, g, ldc))
+        !encode_3d(&tb2, f32, 4, bt_lo, K, N, 1, Kp, 0, 32, BN / 2) ||
+        !encode_c(&tc, g, M == 1 ? (N + 3) & ~3 : ldc))  // one row: any 16-byte row stride describes it
         return cudaErrorNotSupported;
     int used = 0;
     if (BN == 256) {

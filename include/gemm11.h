@@ -106,8 +106,8 @@ GEMM11_API int gemm_f32(int M, int N, int K, float alpha, const float *A, int ld
  * "SGEMM优化，从naive到warptiling" (Q9, the optimisations not made) lists
  * TF32 / tensor cores; "第 11 章 Tiled GEMM" (section 11.7) puts the FP32
  * CUDA-core peak at about 1/15 of the dense FP16 tensor-core peak.
- *   Extra constraint: C 16-byte aligned and ldc % 4 == 0 (C is written by
- *   TMA stores), otherwise GEMM_ERR_UNSUPPORTED; A and B may have any
+ *   Extra constraint: C 16-byte aligned and, when M > 1, ldc % 4 == 0 (C is
+ *   written by TMA stores), otherwise GEMM_ERR_UNSUPPORTED; A and B may have any
  *   alignment and leading dimension.  Scratch: 16 (M + N) K' bytes of
  *   library-owned device memory per stream, K' = K rounded up to 4.  Inputs
  *   within 2^-11 of the FP32 overflow threshold are outside the method (their
