@@ -1365,18 +1365,24 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
                 return cudaErrorNotSupported;
             int used = 0;
             cudaError_t e;
-            // (8 epilogue warps, two per TMEM lane quarter with one staging
-            // buffer each, measured no faster: the epilogue is off the
-            // critical path.)
+            // Short K (at most 8 k blocks per tile): the tile's MMA takes less
+            // time than its epilogue, so 8 epilogue warps (two per TMEM lane
+            // quarter, alternate 32-column chunks, one staging buffer each)
+            // drain the accumulators; with long K the epilogue is hidden behind
+            // the next tile's MMA and 4 warps measured as fast.
+            const bool epi8 = a.kb_total <= 8;
             if (best_bn == 256) {
-                e = launch_hgemm_pair<256, 6, 4, false>(ta, tb, tc, a, stream, &used);
-                info->plan = "tc_pair_256x256";
+                e = epi8 ? launch_hgemm_pair<256, 6, 8, false>(ta, tb, tc, a, stream, &used)
+                         : launch_hgemm_pair<256, 6, 4, false>(ta, tb, tc, a, stream, &used);
+                info->plan = epi8 ? "tc_pair_256x256_epi8" : "tc_pair_256x256";
             } else if (best_bn == 224) {
-                e = launch_hgemm_pair<224, 6, 4, false>(ta, tb, tc, a, stream, &used);
-                info->plan = "tc_pair_256x224";
+                e = epi8 ? launch_hgemm_pair<224, 6, 8, false>(ta, tb, tc, a, stream, &used)
+                         : launch_hgemm_pair<224, 6, 4, false>(ta, tb, tc, a, stream, &used);
+                info->plan = epi8 ? "tc_pair_256x224_epi8" : "tc_pair_256x224";
             } else {
-                e = launch_hgemm_pair<192, 6, 4, false>(ta, tb, tc, a, stream, &used);
-                info->plan = "tc_pair_256x192";
+                e = epi8 ? launch_hgemm_pair<192, 6, 8, false>(ta, tb, tc, a, stream, &used)
+                         : launch_hgemm_pair<192, 6, 4, false>(ta, tb, tc, a, stream, &used);
+                info->plan = epi8 ? "tc_pair_256x192_epi8" : "tc_pair_256x192";
             }
             info->launches = 1;
             return e;

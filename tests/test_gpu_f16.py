@@ -222,3 +222,21 @@ def test_f16_cluster_split_k(M, N, K):
     assert "clusterk" in plan, plan
     ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.25, beta=0.5, bias=d["bias"], act=1)
     assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+
+
+@pytest.mark.parametrize("M,N,K,act", [(2048, 4096, 256, 1), (1000, 4000, 512, 3), (4100, 4104, 64, 0), (513, 4104, 128, 2)])
+def test_f16_short_k_pair_eight_epilogue_warps(M, N, K, act):
+    d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=M + K, beta=-0.5, bias=True)
+    got, plan = run_f16(d, 0.75, -0.5, d["bias"], act)
+    assert "pair" in plan and plan.endswith("epi8"), plan
+    rows = sample_rows(M, seed=49)
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=0.75, beta=-0.5, bias=d["bias"], act=act, rows=rows)
+    assert_within(got[rows], ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+
+
+def test_f16_short_k_pair_exact():
+    d = inputs.make(1024, 2048, 512, kind="f16", dist="smallint", seed=50, beta=1.0)
+    got, plan = run_f16(d, 1.0, 1.0)
+    assert plan.endswith("epi8"), plan
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=1.0, with_scale=False)
+    np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
