@@ -120,3 +120,24 @@ def test_out16_matches_f32_output_rounded():
         np.testing.assert_array_equal(C16.float().cpu().numpy().astype(np.float64),
                                       oracle.round_to(out, C32.cpu().numpy().astype(np.float64)),
                                       err_msg=f"{out} [{g.last_plan()}]")
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 512), (1024, 3072, 256), (4096, 11008, 512)])
+def test_out16_pair_64_column_stores(out, M, N, K):
+    # CTA-pair tiles 256 or 192 wide store a 16-bit C in 32 x 64 boxes.
+    d = inputs.make(M, N, K, kind="bf16", dist="normal_k", seed=M + N, beta=0.5, bias=True)
+    got, C0, plan = run_tc(d, "bf16", out, 1.25, 0.5, d["bias"], 3)
+    assert plan.startswith("tc_pair_256x256") or plan.startswith("tc_pair_256x192"), plan
+    rows = sample_rows(M, seed=51)
+    ref, S = oracle.gemm(d["A"], d["B"], C0, alpha=1.25, beta=0.5, bias=d["bias"], act=3, rows=rows)
+    assert_within(got[rows], ref, S, TOL_F16, f"{out} {M}x{N}x{K} [{plan}]", out=out)
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+def test_out16_pair_64_column_stores_exact(out):
+    d = inputs.make(1024, 3072, 256, kind="f16", dist="smallint", seed=52, beta=2.0)
+    got, C0, plan = run_tc(d, "f16", out, 1.0, 2.0)
+    assert "pair" in plan, plan
+    ref, _ = oracle.gemm(d["A"], d["B"], C0, alpha=1.0, beta=2.0, with_scale=False)
+    np.testing.assert_array_equal(got, oracle.round_to(out, ref), err_msg=plan)
