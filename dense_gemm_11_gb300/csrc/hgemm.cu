@@ -1102,14 +1102,16 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
 #pragma unroll 1
                 for (int u = ch_first; u < BN / 64; u += ch_step) {
                     uint4 w[8];
+                    // both chunks' tensor-memory loads in flight before one wait
+                    uint32_t r2[2][32];
+                    tmem_ld_32x32b_x32(t_row + (2 * u) * 32, r2[0]);
+                    tmem_ld_32x32b_x32(t_row + (2 * u + 1) * 32, r2[1]);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(t_row + (2 * u + h) * 32, r);
-                        tmem_wait_ld();
                         float v[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r2[h][j]);
                         epilogue_row_chunk(v, p, grow, n0 + (2 * u + h) * 32, cbase);
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
