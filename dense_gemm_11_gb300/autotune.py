@@ -47,7 +47,23 @@ def candidates(path: int, M: int, N: int, K: int):
     out += [(2, bn, s) for bn in (256, 128) for s in SPLITS if s <= max(1, kb // 2)]
     if M <= 64:
         out += [(3, bn, s) for bn in (32, 64) if M <= bn for s in SPLITS if s <= max(1, kb // 2)]
+    # cluster split-K (2..8 CTAs per tile); the library ignores an entry whose
+    # CTAs do not all fit on the GPU, so only shapes with few tiles qualify
+    tiles_m = (M + 127) // 128
+    for bn in (256, 192, 128):
+        t = tiles_m * ((N + bn - 1) // bn)
+        out += [(4, bn, s) for s in range(2, 9) if s <= kb // 2 and t * s <= sm_count()]
     return out
+
+
+def sm_count() -> int:
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return 152
 
 
 class _Timed:

@@ -187,6 +187,7 @@ bool valid_tune_entry(const gemm_tune_entry &e) {
         case 1: return e.bn == 0 || e.bn == 256 || e.bn == 224 || e.bn == 192;
         case 2: return e.bn == 0 || e.bn == 256 || e.bn == 128;
         case 3: return e.bn == 0 || e.bn == 32 || e.bn == 64;
+        case 4: return (e.bn == 0 || e.bn == 256 || e.bn == 192 || e.bn == 128) && (e.splits == 0 || (e.splits >= 2 && e.splits <= 8));
         default: return false;
     }
 }

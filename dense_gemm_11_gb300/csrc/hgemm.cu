@@ -89,20 +89,26 @@ __host__ __device__ constexpr int tmem_cols_for(int bn) {
 // hand the partial buffer over: "ready" (every CTA's partial is written) and
 // "consumed" (every CTA has read this CTA's partial).  No global scratch,
 // atomics or memory fences.
+// Not transposed (SWAP false), every CTA computes exactly one unit and its
+// partial overwrites the operand ring, which is idle once the unit's MMAs
+// have completed; the host launches one CTA per unit.
 template <int BN, int STAGES, bool SWAP, bool CSPLIT = false>
 struct HgemmCfg {
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows of 128 B
     static constexpr int kBBytes = BN * kBK * 2;   // BN rows (or k-rows) of 128 B
     static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr bool kPartInRing = CSPLIT && !SWAP;
     static constexpr int kCStageBytes =
-        CSPLIT ? kBM * BN * 4 : (SWAP ? 0 : kEpiWarps * 2 * 32 * 32 * 4);  // partial tile, or 2 x 4 KB per warp
+        kPartInRing ? BN * 4  // the tile's bias slice
+                    : (CSPLIT ? kBM * BN * 4 : (SWAP ? 0 : kEpiWarps * 2 * 32 * 32 * 4));  // partial tile, or 2 x 4 KB per warp
     static constexpr int kBarBytes = (2 * STAGES + 7) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
     static constexpr int kTmemCols = tmem_cols_for(BN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (and 32-column TMEM reads)");
     static_assert(SWAP || BN % 64 == 0, "B tile is loaded in 64-column boxes");
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
-    static_assert(!CSPLIT || SWAP, "cluster split-K is the transposed small-M variant's");
+    static_assert(!kPartInRing || STAGES * kStageBytes >= kBM * BN * 4, "the partial tile fits in the operand ring");
+    static_assert(!kPartInRing || BN % 64 == 0, "partial rows are 32-column groups of 8 swizzled 16-byte chunks");
 };
 
 
@@ -183,15 +189,35 @@ __device__ __forceinline__ void flag_timeout(volatile int *abort_flag, unsigned 
     atomicOr(err, kWatchdogTimeout);
 }
 
-// Epilogue value for one element.
+// Bias of the 32-column chunks a warp will process, in its order: lane l
+// holds the bias of column n0 + 32 chunk(i) + l in b[i] (0 past N or without
+// bias).  Loaded before the epilogue waits for the accumulator, so the
+// loads' latency (an L2 round trip per chunk otherwise) hides behind the
+// main loop; the epilogue broadcasts b[0] by shuffles, then rotates b.
+template <int NCH, typename ChunkOf>
+__device__ __forceinline__ void load_bias_lanes(const HgemmArgs &p, int n0, int lane, ChunkOf chunk_of,
+                                                float (&b)[NCH]) {
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int n = n0 + chunk_of(i) * 32 + lane;
+        b[i] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
+    }
+}
+template <int NCH>
+__device__ __forceinline__ void rotate_bias_lanes(float (&b)[NCH]) {
+#pragma unroll
+    for (int i = 0; i + 1 < NCH; ++i) b[i] = b[i + 1];
+}
+
 // Epilogue of one row chunk: v[j] holds the accumulator of C[grow][col0 + j],
 // j < 32.  Each optional term is one uniform pass over the chunk (the flags
 // are kernel arguments), so the common alpha-only case is 32 multiplies:
 // v = act(alpha * acc + beta * C + bias).  N % 8 == 0 and 16-byte aligned
-// C rows let in-range groups of 4 columns use 128-bit loads (bias too when
-// it is 16-byte aligned).
+// C rows let in-range groups of 4 columns use 128-bit loads.  The bias of
+// column col0 + lane arrives in this lane's `blane` (the whole warp calls
+// this together).
 __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmArgs &p, int grow, int col0,
-                                                   size_t cbase) {
+                                                   size_t cbase, float blane) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
     if (p.beta != 0.f && grow < p.M) {
@@ -228,23 +254,8 @@ __device__ __forceinline__ void epilogue_row_chunk(float (&v)[32], const HgemmAr
         }
     }
     if (p.bias) {
-        if ((reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int gc = col0 + 4 * q;
-                if (gc < p.N) {
-                    const float4 b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + gc));
-                    v[4 * q] += b4.x;
-                    v[4 * q + 1] += b4.y;
-                    v[4 * q + 2] += b4.z;
-                    v[4 * q + 3] += b4.w;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
-        }
+        for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, blane, j);
     }
     // One uniform pass per activation (the branch is taken once per chunk).
     // The GELU forms run as a rolled loop over four groups of 8 that rotates
@@ -353,6 +364,84 @@ __device__ __forceinline__ float epi_value(float acc, const HgemmArgs &p, float 
     return v;
 }
 
+// Cluster split-K, not transposed: CTA `c.split` of the cluster sums rows
+// [r0, r1) = [split * 128 / NSP, (split + 1) * 128 / NSP) of the NSP partial
+// tiles (row-major, chunk-swizzled as written by the epilogue) in split order
+// and writes act(alpha * sum + beta * C + bias).  The 128 epilogue threads
+// take consecutive 4-column groups (coalesced C accesses); each round keeps
+// U groups x NSP remote loads in flight (the loop is latency-bound
+// otherwise), with the groups' C loads issued ahead of them.  `sbias` holds
+// the tile's bias slice (shared memory).
+template <int BN, int NSP>
+__device__ __forceinline__ void csplit_reduce_rows(const HgemmArgs &p, const UnitCoord &c, uint32_t part_addr,
+                                                   size_t cbase, int et, const float *sbias) {
+    constexpr int kGroups = BN / 4;
+    constexpr int U = NSP <= 2 ? 8 : 16 / NSP;
+    const int r0 = c.split * kBM / NSP, r1 = (c.split + 1) * kBM / NSP;
+    const int total = (r1 - r0) * kGroups;
+    uint32_t base[NSP];
+#pragma unroll
+    for (int sidx = 0; sidx < NSP; ++sidx) base[sidx] = mapa_shared(part_addr, sidx);
+    for (int e0 = et; e0 < total; e0 += kEpiWarps * 32 * U) {
+        uint32_t off[U];
+        size_t ci[U];
+        bool live[U];
+        float cold[U][4], b[U][4];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + kEpiWarps * 32 * u;
+            const int row = r0 + e / kGroups, g = e % kGroups;
+            off[u] = static_cast<uint32_t>(row * BN + (g >> 3) * 32 + (((g & 7) ^ (row & 7)) << 2)) * 4u;
+            const int gm = c.m0 + row, gn = c.n0 + 4 * g;
+            live[u] = e < total && gm < p.M && gn < p.N;  // N % 8 == 0: the whole group is inside
+            ci[u] = cbase + static_cast<size_t>(gm) * p.ldc + gn;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cold[u][i] = b[u][i] = 0.f;
+            if (live[u] && p.beta != 0.f) {
+                if (p.c_type == kOutF32) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.C) + ci[u]);
+                    cold[u][0] = c4.x, cold[u][1] = c4.y, cold[u][2] = c4.z, cold[u][3] = c4.w;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cold[u][i] = load_out(p.C, ci[u] + i, p.c_type);
+                }
+            }
+            if (live[u] && p.bias) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(sbias + 4 * g);
+                b[u][0] = b4.x, b[u][1] = b4.y, b[u][2] = b4.z, b[u][3] = b4.w;
+            }
+        }
+        float4 t[U][NSP];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int sidx = 0; sidx < NSP; ++sidx)
+                if (e0 + kEpiWarps * 32 * u < total) t[u][sidx] = ld_shared_cluster_v4(base[sidx] + off[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (!live[u]) continue;
+            float v[4] = {t[u][0].x, t[u][0].y, t[u][0].z, t[u][0].w};
+#pragma unroll
+            for (int sidx = 1; sidx < NSP; ++sidx) {
+                v[0] += t[u][sidx].x;
+                v[1] += t[u][sidx].y;
+                v[2] += t[u][sidx].z;
+                v[3] += t[u][sidx].w;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = epi_value(v[i], p, cold[u][i], b[u][i]);
+            if (p.c_type == kOutF32) {
+                *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + ci[u]) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                uint2 w;
+                w.x = pack2_out16(v[0], v[1], p.c_type);
+                w.y = pack2_out16(v[2], v[3], p.c_type);
+                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.C) + ci[u]) = w;
+            }
+        }
+    }
+}
+
 template <int BN, int STAGES, bool SWAP, bool CSPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -398,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
-        if (!SWAP) tma_prefetch_desc(&tm_c);
+        if (!SWAP && !CSPLIT) tma_prefetch_desc(&tm_c);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, Cfg::kTmemCols);
@@ -424,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         for (int idx = 0; !*abort_flag; ++idx) {
             UnitCoord c;
-            if (!next_unit(p, idx, kBnTile, SWAP, c)) break;
+            if ((Cfg::kPartInRing && idx > 0) || !next_unit(p, idx, kBnTile, SWAP, c)) break;
             for (int kb = c.kb0; kb < c.kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u)) {
                     flag_timeout(abort_flag, p.err);
@@ -479,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int local = 0;
         for (int idx = 0; !*abort_flag; ++idx, ++local) {
             UnitCoord c;
-            if (!next_unit(p, idx, kBnTile, SWAP, c)) break;
+            if ((Cfg::kPartInRing && idx > 0) || !next_unit(p, idx, kBnTile, SWAP, c)) break;
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait(&tempty[buf], acc_phase ^ 1u)) {
@@ -527,9 +616,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         int local = 0;
         for (int idx = 0; !*abort_flag; ++idx, ++local) {
             UnitCoord c;
-            if (!next_unit(p, idx, kBnTile, SWAP, c)) break;
+            if ((Cfg::kPartInRing && idx > 0) || !next_unit(p, idx, kBnTile, SWAP, c)) break;
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
+            // The unit's bias, loaded while its main loop runs: per lane and
+            // chunk (not transposed), this thread's column n (transposed), or
+            // the tile's slice in shared memory (cluster split, not transposed).
+            float blane[BN / 32];
+            float b_n = 0.f;
+            float *const sbias = reinterpret_cast<float *>(sC);
+            const int et = threadIdx.x - 64;  // epilogue thread 0..127
+            if constexpr (Cfg::kPartInRing) {
+                if (p.bias)
+                    for (int j = et; j < BN; j += kEpiWarps * 32)
+                        sbias[j] = c.n0 + j < p.N ? __ldg(p.bias + c.n0 + j) : 0.f;
+            } else if constexpr (CSPLIT) {
+                const int gn = c.n0 + c.split * (kBM / p.splits) + et % (kBM / p.splits);
+                b_n = (p.bias && gn < p.N) ? __ldg(p.bias + gn) : 0.f;
+            } else if constexpr (SWAP) {
+                const int gn = c.n0 + row_in_tile;
+                b_n = (p.bias && gn < p.N) ? __ldg(p.bias + gn) : 0.f;
+            } else {
+                load_bias_lanes(p, c.n0, lane, [](int i) { return i; }, blane);
+            }
             if (!mbar_wait(&tfull[buf], acc_phase)) {
                 flag_timeout(abort_flag, p.err);
                 break;
@@ -541,6 +650,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A unit leaves a partial tile when K is split evenly (splits > 1) or
             // when it covers only part of a stream-K tile (slot >= 0).
             const size_t cbase = static_cast<size_t>(c.batch) * static_cast<size_t>(p.stride_c);
+            if constexpr (Cfg::kPartInRing) {
+                // 1. this CTA's partial -> the idle operand ring, [row][column]
+                //    with the 16-byte chunks of each 32-column group swizzled by
+                //    the row (chunk c of row r at c ^ (r & 7)): conflict-free
+                //    writes per quarter warp, and each reader walks one row.
+                //    The next chunk's tensor-memory load is in flight while
+                //    this one is written.
+                float *part = reinterpret_cast<float *>(sA);
+                fence_proxy_async_smem();  // after the async-proxy (TMA, MMA) use of the ring
+                auto put = [&](const uint32_t (&r)[32], int ch) {
+                    float4 *dst = reinterpret_cast<float4 *>(part + row_in_tile * BN + ch * 32);
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        dst[c4 ^ (row_in_tile & 7)] =
+                            make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
+                                        __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]));
+                };
+                {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(t_row, ra);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int ch = 0; ch < BN / 32; ch += 2) {
+                        tmem_ld_32x32b_x32(t_row + (ch + 1) * 32, rb);
+                        put(ra, ch);
+                        tmem_wait_ld();
+                        if (ch + 2 < BN / 32) tmem_ld_32x32b_x32(t_row + (ch + 2) * 32, ra);
+                        put(rb, ch + 1);
+                        tmem_wait_ld();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                const int nsp = p.splits;
+                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), r));
+                if (!mbar_wait_cluster(part_ready, 0)) {
+                    flag_timeout(abort_flag, p.err);
+                    break;
+                }
+                // 2. rows [r0, r1) of the tile, summed over the partials in split order
+                switch (nsp) {
+                    case 2: csplit_reduce_rows<BN, 2>(p, c, smem_u32(part), cbase, et, sbias); break;
+                    case 3: csplit_reduce_rows<BN, 3>(p, c, smem_u32(part), cbase, et, sbias); break;
+                    case 4: csplit_reduce_rows<BN, 4>(p, c, smem_u32(part), cbase, et, sbias); break;
+                    case 5: csplit_reduce_rows<BN, 5>(p, c, smem_u32(part), cbase, et, sbias); break;
+                    case 6: csplit_reduce_rows<BN, 6>(p, c, smem_u32(part), cbase, et, sbias); break;
+                    case 7: csplit_reduce_rows<BN, 7>(p, c, smem_u32(part), cbase, et, sbias); break;
+                    default: csplit_reduce_rows<BN, 8>(p, c, smem_u32(part), cbase, et, sbias); break;
+                }
+                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_consumed), r));
+                continue;
+            }
             if constexpr (CSPLIT) {
                 // 1. this CTA's partial -> own shared memory, [column][row]
                 float *part = reinterpret_cast<float *>(sC);
@@ -567,7 +729,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int R = kBM / nsp;                 // rows reduced by this CTA
-                const int et = threadIdx.x - 64;         // epilogue thread 0..127
                 const int rr = c.split * R + et % R;     // tile row = column n of C
                 const int ncol = BN / nsp;               // columns (rows m of C) per thread
                 const int j0 = (et / R) * ncol;
@@ -584,14 +745,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_consumed), r));
                 const int gn = c.n0 + rr;
                 if (gn < p.N) {
-                    const float b = p.bias ? __ldg(p.bias + gn) : 0.f;
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         const int gm = j0 + jj;
                         if (jj < ncol && gm < p.M) {
                             const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
                             const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                            store_out(p.C, ci, p.c_type, epi_value(acc[jj], p, cold, b));
+                            store_out(p.C, ci, p.c_type, epi_value(acc[jj], p, cold, b_n));
                         }
                     }
                 }
@@ -620,20 +780,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (!SWAP) {
                     const int grow = c.m0 + row_in_tile;
                     const int col0 = c.n0 + ch * 32;
-                    epilogue_row_chunk(v, p, grow, col0, cbase);
+                    epilogue_row_chunk(v, p, grow, col0, cbase, blane[0]);
+                    rotate_bias_lanes(blane);
                     store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
                 } else {
                     // transposed: this thread owns column n of C, registers walk rows m
                     const int gn = c.n0 + row_in_tile;
                     if (gn < p.N) {
-                        const float b = p.bias ? __ldg(p.bias + gn) : 0.f;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const int gm = ch * 32 + j;
                             if (gm < p.M) {
                                 const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
                                 const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                                store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
+                                store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b_n));
                             }
                         }
                     }
@@ -721,19 +881,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (!SWAP) {
                             const int grow = c.m0 + row_in_tile;
                             const int col0 = c.n0 + ch * 32;
-                            epilogue_row_chunk(v, p, grow, col0, cbase);
+                            epilogue_row_chunk(v, p, grow, col0, cbase, blane[0]);
+                            rotate_bias_lanes(blane);
                             store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
                         } else {
                             const int gn = c.n0 + row_in_tile;
                             if (gn < p.N) {
-                                const float b = p.bias ? __ldg(p.bias + gn) : 0.f;
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) {
                                     const int gm = ch * 32 + j;
                                     if (gm < p.M) {
                                         const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
                                         const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                                        store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b));
+                                        store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b_n));
                                     }
                                 }
                             }
@@ -1060,11 +1220,13 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             }
             if (!ok) break;
             const int grow = my_m + row_in_tile;
+            float blane[4];  // loaded here: the running sums hold most registers during the loop above
+            load_bias_lanes(p, n0, lane, [&](int i) { return g0 + i; }, blane);
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi) {
                 if (g0 + gi >= kGroups) continue;
                 const int col0 = n0 + (g0 + gi) * 32;
-                epilogue_row_chunk(tot[gi], p, grow, col0, cbase);
+                epilogue_row_chunk(tot[gi], p, grow, col0, cbase, blane[gi]);
                 store_row_chunk<Cfg::kNBuf>(tot[gi], p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0, bz);
             }
         }
@@ -1090,6 +1252,17 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             const size_t cbase = static_cast<size_t>(bz) * static_cast<size_t>(p.stride_c);
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
+            // bias of this warp's chunks, loaded while the tile's main loop runs
+            constexpr int kStep = EPI / 4;  // ch_step
+            constexpr int kNchPlain = (BN / 32 + kStep - 1) / kStep;
+            constexpr int kNchUnits = 2 * ((BN / 64 + kStep - 1) / kStep);  // 64-column units, two chunks each
+            constexpr int kNch = kNchPlain > kNchUnits ? kNchPlain : kNchUnits;
+            float blane[kNch];
+            if (p.c64)
+                load_bias_lanes(p, n0, lane, [&](int i) { return 2 * (ch_first + (i >> 1) * ch_step) + (i & 1); },
+                                blane);
+            else
+                load_bias_lanes(p, n0, lane, [&](int i) { return ch_first + i * ch_step; }, blane);
             if (!mbar_wait(&tfull[buf], acc_phase)) {
                 flag_timeout(abort_flag, p.err);
                 break;
@@ -1112,7 +1285,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r2[h][j]);
-                        epilogue_row_chunk(v, p, grow, n0 + (2 * u + h) * 32, cbase);
+                        epilogue_row_chunk(v, p, grow, n0 + (2 * u + h) * 32, cbase, blane[0]);
+                        rotate_bias_lanes(blane);
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
                             w[h * 4 + c8].x = pack2_out16(v[8 * c8], v[8 * c8 + 1], p.c_type);
@@ -1134,7 +1308,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epilogue_row_chunk(v, p, grow, col0, cbase);
+                    epilogue_row_chunk(v, p, grow, col0, cbase, blane[0]);
+                    rotate_bias_lanes(blane);
                     store_row_chunk<Cfg::kNBuf>(v, p, &tm_c, stage_base, n_staged, lane, my_m + q * 32, col0, bz);
                 }
             }
@@ -1263,6 +1438,43 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     return cudaPeekAtLastError();
 }
 
+// Clusters of `cs` CTAs of hgemm_tc_kernel<BN, STAGES, false, true> that the
+// GPU holds at once (cached per cluster size; one device type per process).
+template <int BN, int STAGES>
+int cluster_split_capacity(int cs) {
+    static int cap[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    if (cs < 1 || cs > 8) return 0;
+    if (cap[cs] >= 0) return cap[cs];
+    using Cfg = HgemmCfg<BN, STAGES, false, true>;
+    auto kern = hgemm_tc_kernel<BN, STAGES, false, true>;
+    static unsigned long long smem_set = 0;
+    if (ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs * device_sm_count(), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    cap[cs] = n;
+    return n;
+}
+
+int cluster_split_capacity_for(int bn, int cs) {
+    if (bn == 256) return cluster_split_capacity<256, 4>(cs);
+    if (bn == 192) return cluster_split_capacity<192, 5>(cs);
+    return cluster_split_capacity<128, 6>(cs);
+}
+
 template <int BN, int STAGES, int EPI, bool X3 = false>
 cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const HgemmArgs &a,
                               cudaStream_t stream, int *clusters_used, const CUtensorMap *ta2 = nullptr,
@@ -1306,6 +1518,44 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     return cudaPeekAtLastError();
 }
 
+// Cluster split-K for few 128-row tiles (not transposed): of the tile widths
+// {256, 192, 128} and cluster sizes 2..8 whose CTAs all run at once (one per
+// SM), the one that streams the fewest operand bytes per CTA -- these shapes
+// are bound by what each SM can have in flight -- plus a share for the
+// partial reduction.  Without a tuned entry only when whole 128 x 128 tiles
+// would leave at least half the SMs idle (measured: 128 x 11008 x 4096, 86
+// tiles, is fastest unsplit; 64 tiles of 96 x 8192 x 8192 gain 20 % split);
+// with one, its width and size (0: any) are taken if they can run.  Returns
+// false when no split qualifies.
+bool pick_cluster_split(int tiles_m, int N, int batch, int kb_total, int sms, const TunePlan *tp, int *bn_out,
+                        int *cs_out) {
+    auto cost = [](long long kb_per_cta, int w, int cs) {
+        return kb_per_cta * (kBM + w) * 128 + 3LL * kBM * w * 4 / 10;
+    };
+    const long long tiles128 = static_cast<long long>(tiles_m) * ((N + 127) / 128) * batch;
+    if (!tp && tiles128 * 2 > sms) return false;
+    long long best = -1;
+    int best_bn = 0, best_cs = 0;
+    for (int w : {256, 192, 128}) {
+        if (tp && tp->bn && tp->bn != w) continue;
+        const long long t = static_cast<long long>(tiles_m) * ((N + w - 1) / w) * batch;
+        for (int cs = 2; cs <= 8 && cs <= kb_total / 2; ++cs) {
+            if (tp && tp->splits && tp->splits != cs) continue;
+            if (t * cs > sms) break;
+            if (t > cluster_split_capacity_for(w, cs)) continue;
+            const long long c = cost((kb_total + cs - 1) / cs, w, cs);
+            if (best < 0 || c < best) {
+                best = c;
+                best_bn = w;
+                best_cs = cs;
+            }
+        }
+    }
+    *bn_out = best_bn;
+    *cs_out = best_cs;
+    return best_cs > 0;
+}
+
 }  // namespace
 
 cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
@@ -1345,6 +1595,10 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     TunePlan tp;
     bool tuned = g.batch == 1 && tune_lookup(1, M, N, K, &tp);
     if (tuned && tp.variant == 3 && M > (tp.bn ? tp.bn : 64)) tuned = false;
+    int csplit_bn = 0, csplit_cs = 0;
+    if (tuned && tp.variant == 4 &&
+        !pick_cluster_split((M + kBM - 1) / kBM, N, g.batch, a.kb_total, sms, &tp, &csplit_bn, &csplit_cs))
+        tuned = false;
     info->tuned = tuned;
     const bool swap = tuned ? tp.variant == 3 : M <= 64;
     int bn;
@@ -1372,7 +1626,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     int splits = 1;
     if (swap ? tiles * 2 <= sms : tiles * 3 < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
     splits = std::min(splits, 32);
-    if (tuned && tp.variant != 1 && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, a.kb_total / 2)));
+    if (tuned && (tp.variant == 2 || tp.variant == 3) && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, a.kb_total / 2)));
     a.splits = splits;
     a.units = tiles * splits;
     // Stream-K for the partial last wave is implemented (next_unit) but off:
@@ -1453,6 +1707,34 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     // (Stream-K over all SMs for these memory-bound M <= 128 shapes measured
     // slower: 45.8 us vs 35.6 us at 128 x 11008 x 4096, the partial-tile
     // round trip costs more than the extra SMs gain.)
+    // Fewer 128 x 128 tiles than SMs, not transposed: split K over the CTAs of
+    // a cluster and add the partials through distributed shared memory
+    // (128 x 11008 x 4096: 43 tiles of 128 x 256 in clusters of 3, 129 CTAs
+    // of ~1 MB each, instead of 86 CTAs of 2 MB).
+    const bool use_csplit = tuned ? tp.variant == 4
+                                  : (!swap && pick_cluster_split(a.tiles_m, N, g.batch, a.kb_total, sms, nullptr,
+                                                                 &csplit_bn, &csplit_cs));
+    if (use_csplit) {
+        a.tiles_n = (N + csplit_bn - 1) / csplit_bn;
+        const int t = a.tiles_m * a.tiles_n * g.batch;
+        a.splits = csplit_cs;
+        a.units = t * csplit_cs;  // one CTA per unit; all of them fit at once
+        CUtensorMap ta, tb;
+        if (!encode_a(&ta, g, in_dt, kBM) || !encode_b(&tb, g, in_dt, csplit_bn)) return cudaErrorNotSupported;
+        cudaError_t e;
+        if (csplit_bn == 256) {
+            e = launch_hgemm<256, 4, false, true>(ta, tb, tb, a, a.units, stream);
+            info->plan = "tc_128x256_clusterk";
+        } else if (csplit_bn == 192) {
+            e = launch_hgemm<192, 5, false, true>(ta, tb, tb, a, a.units, stream);
+            info->plan = "tc_128x192_clusterk";
+        } else {
+            e = launch_hgemm<128, 6, false, true>(ta, tb, tb, a, a.units, stream);
+            info->plan = "tc_128x128_clusterk";
+        }
+        info->launches = 1;
+        return e;
+    }
     // The transposed small-M plan splits K over the CTAs of a cluster and adds
     // the partials through distributed shared memory (2, 4 or 8 splits).
     if (swap && splits > 1) {

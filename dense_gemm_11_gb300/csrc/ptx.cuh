@@ -366,6 +366,14 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
     return v;
 }
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
 // 2-D tiled load into this CTA's shared memory whose completion is counted on
 // an mbarrier that may live in the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap *map, uint32_t mbar_cluster_addr, void *smem_dst,

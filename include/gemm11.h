@@ -243,12 +243,17 @@ GEMM11_API int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha
  *            GEMM_PATH_TC: 1 = CTA pairs, bn in {256, 224, 192};
  *              2 = single-CTA 128-row tiles, bn in {256, 128}, `splits` K slices;
  *              3 = transposed small-M product (needs M <= bn), bn in {32, 64},
- *              `splits` K slices.
+ *              `splits` K slices;
+ *              4 = single-CTA 128-row tiles whose K is split over the 2..8
+ *              CTAs of a thread-block cluster (partials added in distributed
+ *              shared memory), bn in {256, 192, 128}, splits = cluster size
+ *              in 2..8 or 0; every CTA of the launch must fit on the GPU at
+ *              once (one per SM), else the entry is ignored.
  *   bn       tile width (0: the planner's choice within the family).
  *   splits   split-K factor, 0..32 (0: the planner's rule; clipped to half
  *            the number of 64-wide k blocks).
  * An entry whose family cannot run the shape it names (variant 3 with
- * M > bn) is ignored at call time.  Results are identical in value across
+ * M > bn, variant 4 with too many CTAs) is ignored at call time.  Results are identical in value across
  * plans only up to the accumulation order.
  */
 typedef enum { GEMM_PATH_F32 = 0, GEMM_PATH_TC = 1 } gemm_tune_path;

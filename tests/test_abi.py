@@ -157,16 +157,21 @@ def test_3xtf32_rejects_bad_args(L):
 def test_tuning_table_roundtrip_and_validation(L):
     rows = [dict(path=g.GEMM_PATH_TC, M=4096, N=4096, K=4096, variant=1, bn=224, splits=0),
             dict(path=g.GEMM_PATH_TC, M=16, N=4096, K=4096, variant=3, bn=32, splits=3),
+            dict(path=g.GEMM_PATH_TC, M=128, N=11008, K=4096, variant=4, bn=192, splits=2),
             dict(path=g.GEMM_PATH_F32, M=512, N=512, K=512, variant=2, bn=0, splits=8),
             dict(path=g.GEMM_PATH_TC, M=16, N=4096, K=4096, variant=2, bn=128, splits=4)]  # later entry wins
     try:
         g.tune_set(rows)
         got = {(e["path"], e["M"], e["N"], e["K"]): e for e in g.tune_get()}
-        assert len(got) == 3
+        assert len(got) == 4
+        assert got[(1, 128, 11008, 4096)]["variant"] == 4 and got[(1, 128, 11008, 4096)]["bn"] == 192
         assert got[(1, 16, 4096, 4096)]["variant"] == 2 and got[(1, 16, 4096, 4096)]["splits"] == 4
         assert got[(0, 512, 512, 512)]["splits"] == 8
         bad = [dict(path=2, M=1, N=1, K=1, variant=1),                       # unknown path
-               dict(path=g.GEMM_PATH_TC, M=1, N=8, K=8, variant=4),          # unknown variant
+               dict(path=g.GEMM_PATH_TC, M=1, N=8, K=8, variant=5),          # unknown variant
+               dict(path=g.GEMM_PATH_TC, M=1, N=8, K=8, variant=4, bn=64),   # width outside the family
+               dict(path=g.GEMM_PATH_TC, M=1, N=8, K=8, variant=4, splits=9),  # cluster larger than 8
+               dict(path=g.GEMM_PATH_TC, M=1, N=8, K=8, variant=4, splits=1),
                dict(path=g.GEMM_PATH_TC, M=1, N=8, K=8, variant=1, bn=128),  # width outside the family
                dict(path=g.GEMM_PATH_TC, M=1, N=8, K=8, variant=3, bn=256),
                dict(path=g.GEMM_PATH_F32, M=1, N=8, K=8, variant=1, bn=64),
@@ -176,7 +181,7 @@ def test_tuning_table_roundtrip_and_validation(L):
             with pytest.raises(g.GemmError) as e:
                 g.tune_set(rows[:1] + [b])
             assert e.value.status == g.GEMM_ERR_INVALID_ARG
-            assert len(g.tune_get()) == 3  # unchanged
+            assert len(g.tune_get()) == 4  # unchanged
         assert L.gemm_tune_set(None, 1) == g.GEMM_ERR_INVALID_ARG
         assert L.gemm_tune_set(None, -1) == g.GEMM_ERR_INVALID_ARG
     finally:
