@@ -364,6 +364,48 @@ __device__ __forceinline__ float epi_value(float acc, const HgemmArgs &p, float 
     return v;
 }
 
+// Cluster split-K of the transposed small-M product: CTA `c.split` sums tile
+// row rr = split * R + et % R (R = 128 / NSP; column n of C) of the NSP
+// partials ([accumulator column][row] in each CTA's shared memory) over the
+// NCOL = BN / NSP accumulator columns j0 + jj (rows m of C) this thread owns,
+// in split order; then releases the partials (every CTA's "consumed"
+// barrier) and writes act(alpha * sum + beta * C + bias).  Compile-time NSP
+// keeps the once-per-unit code short (instruction fetch is a visible cost
+// of a path each CTA runs once).
+template <int BN, int NSP>
+__device__ __forceinline__ void swap_csplit_reduce(const HgemmArgs &p, const UnitCoord &c, uint32_t part_addr,
+                                                   uint32_t consumed_addr, size_t cbase, int et, float b_n) {
+    constexpr int R = kBM / NSP, NCOL = BN / NSP;
+    static_assert(kBM % NSP == 0 && BN % NSP == 0, "power-of-two cluster sizes");
+    const int rr = c.split * R + et % R;
+    const int j0 = (et / R) * NCOL;
+    float acc[NCOL];
+#pragma unroll
+    for (int jj = 0; jj < NCOL; ++jj) acc[jj] = 0.f;
+#pragma unroll
+    for (int src = 0; src < NSP; ++src) {
+        const uint32_t base = mapa_shared(part_addr, src) + static_cast<uint32_t>(j0 * kBM + rr) * 4u;
+        float t[NCOL];
+#pragma unroll
+        for (int jj = 0; jj < NCOL; ++jj) t[jj] = ld_shared_cluster_f32(base + jj * kBM * 4);
+#pragma unroll
+        for (int jj = 0; jj < NCOL; ++jj) acc[jj] += t[jj];
+    }
+#pragma unroll
+    for (int r = 0; r < NSP; ++r) mbar_arrive_cluster(mapa_shared(consumed_addr, r));
+    const int gn = c.n0 + rr;
+    if (gn >= p.N) return;
+#pragma unroll
+    for (int jj = 0; jj < NCOL; ++jj) {
+        const int gm = j0 + jj;
+        if (gm < p.M) {
+            const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
+            const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
+            store_out(p.C, ci, p.c_type, epi_value(acc[jj], p, cold, b_n));
+        }
+    }
+}
+
 // Cluster split-K, not transposed: CTA `c.split` of the cluster sums rows
 // [r0, r1) = [split * 128 / NSP, (split + 1) * 128 / NSP) of the NSP partial
 // tiles (row-major, chunk-swizzled as written by the epilogue) in split order
@@ -728,33 +770,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     flag_timeout(abort_flag, p.err);
                     break;
                 }
-                const int R = kBM / nsp;                 // rows reduced by this CTA
-                const int rr = c.split * R + et % R;     // tile row = column n of C
-                const int ncol = BN / nsp;               // columns (rows m of C) per thread
-                const int j0 = (et / R) * ncol;
-                const uint32_t part_addr = smem_u32(part);
-                float acc[32];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) acc[jj] = 0.f;
-                for (int src = 0; src < nsp; ++src) {
-                    const uint32_t base = mapa_shared(part_addr, src);
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj)
-                        if (jj < ncol) acc[jj] += ld_shared_cluster_f32(base + ((j0 + jj) * kBM + rr) * 4);
-                }
-                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_consumed), r));
-                const int gn = c.n0 + rr;
-                if (gn < p.N) {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int gm = j0 + jj;
-                        if (jj < ncol && gm < p.M) {
-                            const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
-                            const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                            store_out(p.C, ci, p.c_type, epi_value(acc[jj], p, cold, b_n));
-                        }
-                    }
-                }
+                // sizes 2, 4 or 8 (the planner's powers of two)
+                if (nsp == 2)
+                    swap_csplit_reduce<BN, 2>(p, c, smem_u32(part), smem_u32(part_consumed), cbase, et, b_n);
+                else if (nsp == 4)
+                    swap_csplit_reduce<BN, 4>(p, c, smem_u32(part), smem_u32(part_consumed), cbase, et, b_n);
+                else
+                    swap_csplit_reduce<BN, 8>(p, c, smem_u32(part), smem_u32(part_consumed), cbase, et, b_n);
                 continue;
             }
             const bool partial = (p.splits > 1) || (c.slot >= 0);
