@@ -71,10 +71,6 @@ struct HgemmArgs {
     long long stride_c;
     int b_kmajor;  // 1: B is stored N x K (the product uses its transpose), 0: K x N
     int c64;       // 16-bit C stored in 32 x 64 boxes (128-byte rows; pair kernel, tile width % 64 == 0)
-    // stream-K schedule (non-transposed, splits == 1): the first dp_tiles
-    // tiles of the raster are whole units, the last sk_tiles are shared out
-    // by k blocks over the grid; partial tiles go to 2 slots per CTA.
-    int streamk, dp_tiles, sk_tiles;
 };
 
 __host__ __device__ constexpr int tmem_cols_for(int bn) {
@@ -114,7 +110,6 @@ struct HgemmCfg {
 
 struct UnitCoord {
     int tile, split, m0, n0, kb0, kb1, batch;
-    int slot;  // stream-K partial slot, -1 when the unit finishes its tile
 };
 
 // Tile number (over the whole batch) -> matrix index and tile origin.
@@ -142,45 +137,15 @@ __device__ __forceinline__ UnitCoord decode_unit(const HgemmArgs &p, int u, int 
     tile_origin(p, c.tile, bn_tile, swap, c);
     c.kb0 = static_cast<int>(static_cast<long long>(p.kb_total) * c.split / p.splits);
     c.kb1 = static_cast<int>(static_cast<long long>(p.kb_total) * (c.split + 1) / p.splits);
-    c.slot = -1;
     return c;
 }
 
-// The idx-th unit of this CTA; false past the last one.  All three warp
-// roles walk the same sequence.  Stream-K: CTA c owns k blocks
-// [c*I/G, (c+1)*I/G) of the I = sk_tiles * kb_total blocks of the stream-K
-// tiles (at most two tiles, since sk_tiles < G), then data-parallel tiles
-// c, c + G, ...
+// The idx-th unit of this CTA (units u = blockIdx.x + idx * gridDim.x);
+// false past the last one.  All three warp roles walk the same sequence.
 __device__ __forceinline__ bool next_unit(const HgemmArgs &p, int idx, int bn_tile, bool swap, UnitCoord &c) {
-    if (!p.streamk) {
-        const int u = blockIdx.x + idx * gridDim.x;
-        if (u >= p.units) return false;
-        c = decode_unit(p, u, bn_tile, swap);
-        return true;
-    }
-    const int G = gridDim.x, cta = blockIdx.x;
-    const long long KB = p.kb_total;
-    const long long I = static_cast<long long>(p.sk_tiles) * KB;
-    const long long b = cta * I / G, e = (cta + 1) * I / G;
-    const int nsk = (p.sk_tiles > 0 && b < e) ? static_cast<int>((e - 1) / KB - b / KB + 1) : 0;
-    int tile;
-    if (idx < nsk) {
-        const int ts = static_cast<int>(b / KB) + idx;
-        const long long t0 = static_cast<long long>(ts) * KB;
-        tile = p.dp_tiles + ts;
-        c.kb0 = static_cast<int>(max(b, t0) - t0);
-        c.kb1 = static_cast<int>(min(e, t0 + KB) - t0);
-        c.slot = (c.kb0 == 0 && c.kb1 == p.kb_total) ? -1 : 2 * cta + idx;
-    } else {
-        tile = cta + (idx - nsk) * G;
-        if (tile >= p.dp_tiles) return false;
-        c.kb0 = 0;
-        c.kb1 = p.kb_total;
-        c.slot = -1;
-    }
-    c.tile = tile;
-    c.split = 0;
-    tile_origin(p, tile, bn_tile, swap, c);
+    const int u = blockIdx.x + idx * gridDim.x;
+    if (u >= p.units) return false;
+    c = decode_unit(p, u, bn_tile, swap);
     return true;
 }
 
@@ -688,9 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
             // Pass 1: TMEM -> registers.  Either the finished epilogue (no split)
-            // or the raw partial to scratch (split K).
-            // A unit leaves a partial tile when K is split evenly (splits > 1) or
-            // when it covers only part of a stream-K tile (slot >= 0).
+            // or the raw partial to scratch (K split over CTAs, splits > 1).
             const size_t cbase = static_cast<size_t>(c.batch) * static_cast<size_t>(p.stride_c);
             if constexpr (Cfg::kPartInRing) {
                 // 1. this CTA's partial -> the idle operand ring, [row][column]
@@ -779,11 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     swap_csplit_reduce<BN, 8>(p, c, smem_u32(part), smem_u32(part_consumed), cbase, et, b_n);
                 continue;
             }
-            const bool partial = (p.splits > 1) || (c.slot >= 0);
+            const bool partial = p.splits > 1;
             float *part = nullptr;
-            if (partial)
-                part = p.ws + (c.slot >= 0 ? static_cast<size_t>(c.slot)
-                                           : static_cast<size_t>(c.tile) * p.splits + c.split) * (kBM * BN);
+            if (partial) part = p.ws + (static_cast<size_t>(c.tile) * p.splits + c.split) * (kBM * BN);
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 uint32_t r[32];
@@ -828,21 +789,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (partial) {
                 // The last contributor to arrive on this 32-row slice of the
-                // tile adds all contributions in k order (even splits: split
-                // index; stream-K: the owning CTAs c0..c1 in order).
-                int n_contrib, c0 = 0, cnt_idx;
-                long long I = 0;
-                if (c.slot >= 0) {
-                    const long long KB = p.kb_total;
-                    I = static_cast<long long>(p.sk_tiles) * KB;
-                    const long long f = static_cast<long long>(c.tile - p.dp_tiles) * KB;
-                    c0 = static_cast<int>(((f + 1) * gridDim.x - 1) / I);
-                    n_contrib = static_cast<int>(((f + KB) * gridDim.x - 1) / I) - c0 + 1;
-                    cnt_idx = (c.tile - p.dp_tiles) * 4 + q;
-                } else {
-                    n_contrib = p.splits;
-                    cnt_idx = c.tile * 4 + q;
-                }
+                // tile adds all contributions in k order (split index).
+                const int n_contrib = p.splits;
+                const int cnt_idx = c.tile * 4 + q;
                 __threadfence();
                 __syncwarp();
                 unsigned last = 0;
@@ -851,16 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (last) {
                     __threadfence();
                     auto contrib = [&](int i) -> const float * {
-                        size_t slot;
-                        if (c.slot >= 0) {
-                            const int cc = c0 + i;
-                            const int ts = c.tile - p.dp_tiles;
-                            slot = 2 * static_cast<size_t>(cc) +
-                                   static_cast<size_t>(ts - static_cast<int>((cc * I / gridDim.x) / p.kb_total));
-                        } else {
-                            slot = static_cast<size_t>(c.tile) * p.splits + i;
-                        }
-                        return p.ws + slot * (kBM * BN);
+                        return p.ws + (static_cast<size_t>(c.tile) * p.splits + i) * (kBM * BN);
                     };
 #pragma unroll 1
                     for (int ch = 0; ch < BN / 32; ++ch) {
@@ -1651,20 +1591,10 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     if (tuned && (tp.variant == 2 || tp.variant == 3) && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, a.kb_total / 2)));
     a.splits = splits;
     a.units = tiles * splits;
-    // Stream-K for the partial last wave is implemented (next_unit) but off:
-    // on GB300 at 4096^3 it measured slower (126 us vs 110 us) than whole
-    // tiles, because the last arriver's reduction of ~2.7 partial tiles is
-    // latency-bound inside one CTA.
-    constexpr bool kUseStreamK = false;
-    if (kUseStreamK && !swap && tiles >= sms) {
-        const int rem = tiles % sms;
-        const long long share = static_cast<long long>(rem) * a.kb_total / sms;  // k blocks per CTA
-        if (rem != 0 && share >= 2 && a.kb_total / share + 2 <= 64) {
-            a.streamk = 1;
-            a.dp_tiles = tiles - rem;
-            a.sk_tiles = rem;
-        }
-    }
+    // (Stream-K for the partial last wave measured slower on GB300 at
+    // 4096^3, 126 us vs 110 us for whole tiles: the last arriver's reduction
+    // of ~2.7 partial tiles is latency-bound inside one CTA.  CTA pairs with
+    // the tile width chosen by waves replaced it.)
     // CTA pairs: M > 128 with enough 256-row pair tiles for the SMs.  The
     // tile width is picked from {256, 224, 192} by the number of waves of
     // pair tiles, then the narrowest: a tile takes nearly the same time at all
@@ -1786,15 +1716,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
         a.ws = sc.partials;
         a.counters = sc.counters;
     }
-    const int grid = a.streamk ? sms : std::min(a.units, sms);
-    if (a.streamk) {
-        Scratch sc;
-        cudaError_t e = acquire_scratch(stream, static_cast<size_t>(2) * grid * kBM * bn,
-                                        static_cast<size_t>(a.sk_tiles) * 4, &sc);
-        if (e != cudaSuccess) return e;
-        a.ws = sc.partials;
-        a.counters = sc.counters;
-    }
+    const int grid = std::min(a.units, sms);
 
     CUtensorMap ta, tb, tc;
     std::memset(&tc, 0, sizeof(tc));
@@ -1814,10 +1736,10 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     if (!swap) {
         if (bn == 256) {
             e = launch_hgemm<256, 4, false>(ta, tb, tc, a, grid, stream);
-            info->plan = a.streamk ? "tc_128x256_streamk" : (splits > 1 ? "tc_128x256_splitk" : "tc_128x256");
+            info->plan = splits > 1 ? "tc_128x256_splitk" : "tc_128x256";
         } else {
             e = launch_hgemm<128, 6, false>(ta, tb, tc, a, grid, stream);
-            info->plan = a.streamk ? "tc_128x128_streamk" : (splits > 1 ? "tc_128x128_splitk" : "tc_128x128");
+            info->plan = splits > 1 ? "tc_128x128_splitk" : "tc_128x128";
         }
     } else {
         if (bn == 32) {
