@@ -344,29 +344,39 @@ __device__ __forceinline__ void swap_csplit_reduce(const HgemmArgs &p, const Uni
     static_assert(kBM % NSP == 0 && BN % NSP == 0, "power-of-two cluster sizes");
     const int rr = c.split * R + et % R;
     const int j0 = (et / R) * NCOL;
-    float acc[NCOL];
-#pragma unroll
-    for (int jj = 0; jj < NCOL; ++jj) acc[jj] = 0.f;
+    // every source's loads in flight before the first add (one remote latency)
+    float t[NSP][NCOL];
 #pragma unroll
     for (int src = 0; src < NSP; ++src) {
         const uint32_t base = mapa_shared(part_addr, src) + static_cast<uint32_t>(j0 * kBM + rr) * 4u;
-        float t[NCOL];
 #pragma unroll
-        for (int jj = 0; jj < NCOL; ++jj) t[jj] = ld_shared_cluster_f32(base + jj * kBM * 4);
-#pragma unroll
-        for (int jj = 0; jj < NCOL; ++jj) acc[jj] += t[jj];
+        for (int jj = 0; jj < NCOL; ++jj) t[src][jj] = ld_shared_cluster_f32(base + jj * kBM * 4);
     }
-#pragma unroll
-    for (int r = 0; r < NSP; ++r) mbar_arrive_cluster(mapa_shared(consumed_addr, r));
-    const int gn = c.n0 + rr;
-    if (gn >= p.N) return;
+    float acc[NCOL];
 #pragma unroll
     for (int jj = 0; jj < NCOL; ++jj) {
+        acc[jj] = t[0][jj];
+#pragma unroll
+        for (int src = 1; src < NSP; ++src) acc[jj] += t[src][jj];
+    }
+    // one arrival per warp on each CTA's barrier (lane r -> CTA r), after
+    // the warp's loads (the warp barrier orders them before the release)
+    __syncwarp();
+    if ((threadIdx.x & 31) < NSP) mbar_arrive_cluster(mapa_shared(consumed_addr, threadIdx.x & 31));
+    const int gn = c.n0 + rr;
+    if (gn >= p.N) return;
+    // a rolled loop (the values rotate through acc[0]): this code runs once
+    // per CTA, and fetching unrolled straight-line code costs more than it saves
+#pragma unroll 1
+    for (int jj = 0; jj < NCOL; ++jj) {
+        const float a = acc[0];
+#pragma unroll
+        for (int i = 0; i + 1 < NCOL; ++i) acc[i] = acc[i + 1];
         const int gm = j0 + jj;
         if (gm < p.M) {
             const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
             const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-            store_out(p.C, ci, p.c_type, epi_value(acc[jj], p, cold, b_n));
+            store_out(p.C, ci, p.c_type, epi_value(a, p, cold, b_n));
         }
     }
 }
@@ -485,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(mma_done, 1);
         if (CSPLIT) {
-            mbar_init(part_ready, p.splits * kEpiWarps * 32);
-            mbar_init(part_consumed, p.splits * kEpiWarps * 32);
+            mbar_init(part_ready, p.splits * kEpiWarps);  // one arrival per epilogue warp of each CTA
+            mbar_init(part_consumed, p.splits * kEpiWarps);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -508,8 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     // Everything above (barriers, tensor memory, descriptor prefetch) may
-    // overlap the previous kernel of the stream; global memory only below.
-    pdl_wait();
+    // overlap the previous kernel of the stream, and so may each role's work
+    // up to its first global-memory access: the producer waits for the
+    // previous kernel (pdl_wait) just before its first TMA load, the epilogue
+    // warps before their first load; the MMA warp touches no global memory.
     pdl_launch_dependents();
 
     uint32_t armed = 0, armed_parity = 0;  // producer bookkeeping for the final drain
@@ -527,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+                if (idx == 0 && kb == c.kb0) pdl_wait();  // the operands may come from the previous kernel
                 const int k0 = kb * kBK;
                 uint8_t *a_dst = sA + stage * Cfg::kABytes;
                 uint8_t *b_dst = sB + stage * Cfg::kBBytes;
@@ -621,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *const stage_base = sC + (warp - 2) * 8192;
         uint32_t n_staged = 0;
         int local = 0;
+        pdl_wait();  // before the first bias, C or scratch access
         for (int idx = 0; !*abort_flag; ++idx, ++local) {
             UnitCoord c;
             if ((Cfg::kPartInRing && idx > 0) || !next_unit(p, idx, kBnTile, SWAP, c)) break;
@@ -687,10 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before();
-                __syncwarp();
+                __syncwarp();  // also orders the warp's partial (and bias) writes before the arrivals
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 const int nsp = p.splits;
-                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), r));
+                if (lane < nsp) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), lane));
                 if (!mbar_wait_cluster(part_ready, 0)) {
                     flag_timeout(abort_flag, p.err);
                     break;
@@ -705,7 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     case 7: csplit_reduce_rows<BN, 7>(p, c, smem_u32(part), cbase, et, sbias); break;
                     default: csplit_reduce_rows<BN, 8>(p, c, smem_u32(part), cbase, et, sbias); break;
                 }
-                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_consumed), r));
+                __syncwarp();
+                if (lane < nsp) mbar_arrive_cluster(mapa_shared(smem_u32(part_consumed), lane));
                 continue;
             }
             if constexpr (CSPLIT) {
@@ -724,10 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) part[(ch * 32 + j) * kBM + row_in_tile] = __uint_as_float(r[j]);
                 }
                 tc_fence_before();
-                __syncwarp();
+                __syncwarp();  // also orders the warp's partial writes before the arrivals
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 const int nsp = p.splits;
-                for (int r = 0; r < nsp; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), r));
+                if (lane < nsp) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), lane));
                 // 2. rows [rank * R, rank * R + R) of the sum of all partials, in split order
                 if (!mbar_wait_cluster(part_ready, local & 1)) {
                     flag_timeout(abort_flag, p.err);
