@@ -88,15 +88,21 @@ __host__ __device__ constexpr int tmem_cols_for(int bn) {
 // Not transposed (SWAP false), every CTA computes exactly one unit and its
 // partial overwrites the operand ring, which is idle once the unit's MMAs
 // have completed; the host launches one CTA per unit.
-template <int BN, int STAGES, bool SWAP, bool CSPLIT = false>
+// EPI: epilogue warps (4, or 8 for the whole-tile non-transposed plan whose
+// tiles fit one per CTA, so that the epilogue is not hidden behind another
+// tile's main loop: two warps per TMEM lane quarter take alternate 32-column
+// chunks, one 4 KB staging buffer each).
+template <int BN, int STAGES, bool SWAP, bool CSPLIT = false, int EPI = 4>
 struct HgemmCfg {
+    static constexpr int kThreads = 64 + 32 * EPI;
+    static constexpr int kNBuf = EPI == 4 ? 2 : 1;  // 4 KB staging buffers per epilogue warp
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows of 128 B
     static constexpr int kBBytes = BN * kBK * 2;   // BN rows (or k-rows) of 128 B
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr bool kPartInRing = CSPLIT && !SWAP;
     static constexpr int kCStageBytes =
         kPartInRing ? BN * 4  // the tile's bias slice
-                    : (CSPLIT ? kBM * BN * 4 : (SWAP ? 0 : kEpiWarps * 2 * 32 * 32 * 4));  // partial tile, or 2 x 4 KB per warp
+                    : (CSPLIT ? kBM * BN * 4 : (SWAP ? 0 : EPI * kNBuf * 32 * 32 * 4));  // partial tile, or staging
     static constexpr int kBarBytes = (2 * STAGES + 7) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
     static constexpr int kTmemCols = tmem_cols_for(BN);
@@ -105,6 +111,7 @@ struct HgemmCfg {
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
     static_assert(!kPartInRing || STAGES * kStageBytes >= kBM * BN * 4, "the partial tile fits in the operand ring");
     static_assert(!kPartInRing || BN % 64 == 0, "partial rows are 32-column groups of 8 swizzled 16-byte chunks");
+    static_assert(EPI == 4 || (EPI == 8 && !SWAP && !CSPLIT), "8 epilogue warps: whole non-transposed tiles only");
 };
 
 
@@ -385,85 +392,99 @@ __device__ __forceinline__ void swap_csplit_reduce(const HgemmArgs &p, const Uni
 // [r0, r1) = [split * 128 / NSP, (split + 1) * 128 / NSP) of the NSP partial
 // tiles (row-major, chunk-swizzled as written by the epilogue) in split order
 // and writes act(alpha * sum + beta * C + bias).  The 128 epilogue threads
-// take consecutive 4-column groups (coalesced C accesses); each round keeps
-// U groups x NSP remote loads in flight (the loop is latency-bound
-// otherwise), with the groups' C loads issued ahead of them.  `sbias` holds
-// the tile's bias slice (shared memory).
+// take consecutive 4-column groups (coalesced C accesses) in a rolled loop
+// that keeps the next group's remote loads in flight while it finishes the
+// current one: this runs once per CTA, and unrolled straight-line code spent
+// more time in instruction fetch than in the work.  `sbias` holds the
+// tile's bias slice (shared memory).
 template <int BN, int NSP>
 __device__ __forceinline__ void csplit_reduce_rows(const HgemmArgs &p, const UnitCoord &c, uint32_t part_addr,
                                                    size_t cbase, int et, const float *sbias) {
     constexpr int kGroups = BN / 4;
-    constexpr int U = NSP <= 2 ? 8 : 16 / NSP;
+    constexpr int kStep = kEpiWarps * 32;
     const int r0 = c.split * kBM / NSP, r1 = (c.split + 1) * kBM / NSP;
     const int total = (r1 - r0) * kGroups;
+    // the own partial through ordinary shared loads (the cluster path carries
+    // only ~16 B per clock per SM), the peers' through distributed shared memory
     uint32_t base[NSP];
 #pragma unroll
     for (int sidx = 0; sidx < NSP; ++sidx) base[sidx] = mapa_shared(part_addr, sidx);
-    for (int e0 = et; e0 < total; e0 += kEpiWarps * 32 * U) {
-        uint32_t off[U];
-        size_t ci[U];
-        bool live[U];
-        float cold[U][4], b[U][4];
+    const int own = c.split;
+    auto load_part = [&](int sidx, uint32_t off) -> float4 {
+        if (sidx == own) {
+            float4 v;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                         : "r"(part_addr + off)
+                         : "memory");
+            return v;
+        }
+        return ld_shared_cluster_v4(base[sidx] + off);
+    };
+    auto offset = [&](int e) {
+        const int row = r0 + e / kGroups, g = e % kGroups;
+        return static_cast<uint32_t>(row * BN + (g >> 3) * 32 + (((g & 7) ^ (row & 7)) << 2)) * 4u;
+    };
+    float4 nxt[NSP];
+    if (et < total) {
+        const uint32_t off = offset(et);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = e0 + kEpiWarps * 32 * u;
-            const int row = r0 + e / kGroups, g = e % kGroups;
-            off[u] = static_cast<uint32_t>(row * BN + (g >> 3) * 32 + (((g & 7) ^ (row & 7)) << 2)) * 4u;
-            const int gm = c.m0 + row, gn = c.n0 + 4 * g;
-            live[u] = e < total && gm < p.M && gn < p.N;  // N % 8 == 0: the whole group is inside
-            ci[u] = cbase + static_cast<size_t>(gm) * p.ldc + gn;
+        for (int sidx = 0; sidx < NSP; ++sidx) nxt[sidx] = load_part(sidx, off);
+    }
+#pragma unroll 1
+    for (int e = et; e < total; e += kStep) {
+        float4 cur[NSP];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) cold[u][i] = b[u][i] = 0.f;
-            if (live[u] && p.beta != 0.f) {
-                if (p.c_type == kOutF32) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.C) + ci[u]);
-                    cold[u][0] = c4.x, cold[u][1] = c4.y, cold[u][2] = c4.z, cold[u][3] = c4.w;
-                } else {
+        for (int sidx = 0; sidx < NSP; ++sidx) cur[sidx] = nxt[sidx];
+        if (e + kStep < total) {
+            const uint32_t off = offset(e + kStep);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) cold[u][i] = load_out(p.C, ci[u] + i, p.c_type);
-                }
-            }
-            if (live[u] && p.bias) {
-                const float4 b4 = *reinterpret_cast<const float4 *>(sbias + 4 * g);
-                b[u][0] = b4.x, b[u][1] = b4.y, b[u][2] = b4.z, b[u][3] = b4.w;
+            for (int sidx = 0; sidx < NSP; ++sidx) nxt[sidx] = load_part(sidx, off);
+        }
+        float v[4] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w};
+#pragma unroll
+        for (int sidx = 1; sidx < NSP; ++sidx) {
+            v[0] += cur[sidx].x;
+            v[1] += cur[sidx].y;
+            v[2] += cur[sidx].z;
+            v[3] += cur[sidx].w;
+        }
+        const int row = r0 + e / kGroups, g = e % kGroups;
+        const int gm = c.m0 + row, gn = c.n0 + 4 * g;
+        if (gm >= p.M || gn >= p.N) continue;  // N % 8 == 0: the whole group is inside
+        const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
+        float cold[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p.beta != 0.f) {
+            if (p.c_type == kOutF32) {
+                const float4 c4 = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.C) + ci);
+                cold[0] = c4.x, cold[1] = c4.y, cold[2] = c4.z, cold[3] = c4.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cold[i] = load_out(p.C, ci + i, p.c_type);
             }
         }
-        float4 t[U][NSP];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int sidx = 0; sidx < NSP; ++sidx)
-                if (e0 + kEpiWarps * 32 * u < total) t[u][sidx] = ld_shared_cluster_v4(base[sidx] + off[u]);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (!live[u]) continue;
-            float v[4] = {t[u][0].x, t[u][0].y, t[u][0].z, t[u][0].w};
-#pragma unroll
-            for (int sidx = 1; sidx < NSP; ++sidx) {
-                v[0] += t[u][sidx].x;
-                v[1] += t[u][sidx].y;
-                v[2] += t[u][sidx].z;
-                v[3] += t[u][sidx].w;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = epi_value(v[i], p, cold[u][i], b[u][i]);
-            if (p.c_type == kOutF32) {
-                *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + ci[u]) = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-                uint2 w;
-                w.x = pack2_out16(v[0], v[1], p.c_type);
-                w.y = pack2_out16(v[2], v[3], p.c_type);
-                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.C) + ci[u]) = w;
-            }
+        float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.bias) b4 = *reinterpret_cast<const float4 *>(sbias + 4 * g);
+        v[0] = epi_value(v[0], p, cold[0], b4.x);
+        v[1] = epi_value(v[1], p, cold[1], b4.y);
+        v[2] = epi_value(v[2], p, cold[2], b4.z);
+        v[3] = epi_value(v[3], p, cold[3], b4.w);
+        if (p.c_type == kOutF32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + ci) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            uint2 w;
+            w.x = pack2_out16(v[0], v[1], p.c_type);
+            w.y = pack2_out16(v[2], v[3], p.c_type);
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.C) + ci) = w;
         }
     }
 }
 
-template <int BN, int STAGES, bool SWAP, bool CSPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, bool SWAP, bool CSPLIT, int EPI = 4>
+__global__ void __launch_bounds__(64 + 32 * EPI, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const HgemmArgs p) {
-    using Cfg = HgemmCfg<BN, STAGES, SWAP, CSPLIT>;
+    using Cfg = HgemmCfg<BN, STAGES, SWAP, CSPLIT, EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;                                 // STAGES x 16 KB (MMA operand A)
@@ -491,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], kEpiWarps);
+            mbar_init(&tempty[b], EPI);
         }
         mbar_init(mma_done, 1);
         if (CSPLIT) {
@@ -628,10 +649,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue warps
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
-        // Two 4 KB staging buffers per warp used alternately (running chunk
-        // count), so a chunk's shared-memory writes only wait for the TMA
-        // store issued two chunks earlier.
-        uint8_t *const stage_base = sC + (warp - 2) * 8192;
+        // Four warps: two 4 KB staging buffers per warp used alternately
+        // (running chunk count), so a chunk's shared-memory writes only wait
+        // for the TMA store issued two chunks earlier.  Eight warps: one
+        // buffer each, and warp half h takes the chunks ch = h (mod 2).
+        const int ch_first = (warp - 2) >> 2, ch_step = EPI / 4;
+        uint8_t *const stage_base = sC + (warp - 2) * (Cfg::kNBuf * 4096);
         uint32_t n_staged = 0;
         int local = 0;
         pdl_wait();  // before the first bias, C or scratch access
@@ -643,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The unit's bias, loaded while its main loop runs: per lane and
             // chunk (not transposed), this thread's column n (transposed), or
             // the tile's slice in shared memory (cluster split, not transposed).
-            float blane[BN / 32];
+            float blane[(BN / 32 + EPI / 4 - 1) / (EPI / 4)];
             float b_n = 0.f;
             float *const sbias = reinterpret_cast<float *>(sC);
             const int et = threadIdx.x - 64;  // epilogue thread 0..127
@@ -658,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int gn = c.n0 + row_in_tile;
                 b_n = (p.bias && gn < p.N) ? __ldg(p.bias + gn) : 0.f;
             } else {
-                load_bias_lanes(p, c.n0, lane, [](int i) { return i; }, blane);
+                load_bias_lanes(p, c.n0, lane, [&](int i) { return ch_first + i * ch_step; }, blane);
             }
             if (!mbar_wait(&tfull[buf], acc_phase)) {
                 flag_timeout(abort_flag, p.err);
@@ -757,11 +780,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     swap_csplit_reduce<BN, 8>(p, c, smem_u32(part), smem_u32(part_consumed), cbase, et, b_n);
                 continue;
             }
-            const bool partial = p.splits > 1;
+            const bool partial = EPI == 4 && p.splits > 1;  // the planner splits only with 4 warps
             float *part = nullptr;
             if (partial) part = p.ws + (static_cast<size_t>(c.tile) * p.splits + c.split) * (kBM * BN);
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = ch_first; ch < BN / 32; ch += ch_step) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_row + ch * 32, r);
                 tmem_wait_ld();
@@ -780,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int col0 = c.n0 + ch * 32;
                     epilogue_row_chunk(v, p, grow, col0, cbase, blane[0]);
                     rotate_bias_lanes(blane);
-                    store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
+                    store_row_chunk<Cfg::kNBuf>(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
                 } else {
                     // transposed: this thread owns column n of C, registers walk rows m
                     const int gn = c.n0 + row_in_tile;
@@ -860,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int col0 = c.n0 + ch * 32;
                             epilogue_row_chunk(v, p, grow, col0, cbase, blane[0]);
                             rotate_bias_lanes(blane);
-                            store_row_chunk(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
+                            store_row_chunk<Cfg::kNBuf>(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
                         } else {
                             const int gn = c.n0 + row_in_tile;
                             if (gn < p.N) {
@@ -1378,11 +1401,11 @@ bool encode_b(CUtensorMap *map, const TcGemm &g, CUtensorMapDataType dt, uint32_
     return encode_3d(map, dt, 2, g.B, g.N, g.K, g.stride_b ? g.batch : 1, g.N, g.stride_b, 64, kBK);
 }
 
-template <int BN, int STAGES, bool SWAP, bool CSPLIT = false>
+template <int BN, int STAGES, bool SWAP, bool CSPLIT = false, int EPI = 4>
 cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const HgemmArgs &a,
                          int grid, cudaStream_t stream) {
-    using Cfg = HgemmCfg<BN, STAGES, SWAP, CSPLIT>;
-    auto kern = hgemm_tc_kernel<BN, STAGES, SWAP, CSPLIT>;
+    using Cfg = HgemmCfg<BN, STAGES, SWAP, CSPLIT, EPI>;
+    auto kern = hgemm_tc_kernel<BN, STAGES, SWAP, CSPLIT, EPI>;
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
@@ -1405,7 +1428,7 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
     attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1495,23 +1518,26 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     return cudaPeekAtLastError();
 }
 
-// Cluster split-K for few 128-row tiles (not transposed): of the tile widths
-// {256, 192, 128} and cluster sizes 2..8 whose CTAs all run at once (one per
-// SM), the one that streams the fewest operand bytes per CTA -- these shapes
-// are bound by what each SM can have in flight -- plus a share for the
-// partial reduction.  Without a tuned entry only when whole 128 x 128 tiles
-// would leave at least half the SMs idle (measured: 128 x 11008 x 4096, 86
-// tiles, is fastest unsplit; 64 tiles of 96 x 8192 x 8192 gain 20 % split);
-// with one, its width and size (0: any) are taken if they can run.  Returns
+// Cluster split-K for few 128-row tiles (not transposed).  A time model
+// fitted to GB300 measurements: a CTA streams its operand bytes at ~100 GB/s
+// (the bytes each SM keeps in flight bound it, not HBM, while the SMs are
+// few); a split adds ~5 us of hand-over and reduction (peers' skew, the
+// barriers, the reduction loop with its epilogue) plus the partial's remote
+// reads at ~30 GB/s (distributed shared memory, ~16 B per clock per SM).
+// Without a tuned entry: only when whole 128 x 128 tiles leave at least half
+// the SMs idle, and only when the best split beats the whole tiles by 10 %
+// (128 x 4096 x 4096: 4 x 128-wide, 19.6 -> 13.6 us; 96 x 8192 x 2048 and
+// 100 x 8192 x 1024 stay whole: 12.9 and 8.4 us, split 15.4 and 12.7 us).  With a tuned
+// entry, its width and size (0: any) are taken if they can run.  Returns
 // false when no split qualifies.
 bool pick_cluster_split(int tiles_m, int N, int batch, int kb_total, int sms, const TunePlan *tp, int *bn_out,
                         int *cs_out) {
-    auto cost = [](long long kb_per_cta, int w, int cs) {
-        return kb_per_cta * (kBM + w) * 128 + 3LL * kBM * w * 4 / 10;
-    };
+    constexpr double kStreamBps = 100e9, kRemoteBps = 30e9, kHandover = 5e-6;
+    auto stream_s = [&](int kb, int w) { return static_cast<double>(kb) * (kBM + w) * 128 / kStreamBps; };
     const long long tiles128 = static_cast<long long>(tiles_m) * ((N + 127) / 128) * batch;
     if (!tp && tiles128 * 2 > sms) return false;
-    long long best = -1;
+    const double whole = stream_s(kb_total, 128);
+    double best = -1.0;
     int best_bn = 0, best_cs = 0;
     for (int w : {256, 192, 128}) {
         if (tp && tp->bn && tp->bn != w) continue;
@@ -1520,7 +1546,8 @@ bool pick_cluster_split(int tiles_m, int N, int batch, int kb_total, int sms, co
             if (tp && tp->splits && tp->splits != cs) continue;
             if (t * cs > sms) break;
             if (t > cluster_split_capacity_for(w, cs)) continue;
-            const long long c = cost((kb_total + cs - 1) / cs, w, cs);
+            const double c = stream_s((kb_total + cs - 1) / cs, w) + kHandover +
+                             (cs - 1.0) / cs * kBM * w * 4 / kRemoteBps;
             if (best < 0 || c < best) {
                 best = c;
                 best_bn = w;
@@ -1528,6 +1555,7 @@ bool pick_cluster_split(int tiles_m, int N, int batch, int kb_total, int sms, co
             }
         }
     }
+    if (!tp && best >= 0.9 * whole) return false;
     *bn_out = best_bn;
     *cs_out = best_cs;
     return best_cs > 0;
@@ -1749,12 +1777,17 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
 
     cudaError_t e;
     if (!swap) {
+        // Whole tiles, one per CTA: nothing hides a tile's epilogue, so 8
+        // epilogue warps share it.
+        const bool epi8 = splits == 1 && a.units <= sms;
         if (bn == 256) {
-            e = launch_hgemm<256, 4, false>(ta, tb, tc, a, grid, stream);
-            info->plan = splits > 1 ? "tc_128x256_splitk" : "tc_128x256";
+            e = epi8 ? launch_hgemm<256, 4, false, false, 8>(ta, tb, tc, a, grid, stream)
+                     : launch_hgemm<256, 4, false>(ta, tb, tc, a, grid, stream);
+            info->plan = splits > 1 ? "tc_128x256_splitk" : (epi8 ? "tc_128x256_epi8" : "tc_128x256");
         } else {
-            e = launch_hgemm<128, 6, false>(ta, tb, tc, a, grid, stream);
-            info->plan = splits > 1 ? "tc_128x128_splitk" : "tc_128x128";
+            e = epi8 ? launch_hgemm<128, 6, false, false, 8>(ta, tb, tc, a, grid, stream)
+                     : launch_hgemm<128, 6, false>(ta, tb, tc, a, grid, stream);
+            info->plan = splits > 1 ? "tc_128x128_splitk" : (epi8 ? "tc_128x128_epi8" : "tc_128x128");
         }
     } else {
         if (bn == 32) {

@@ -36,10 +36,12 @@ def run(d, alpha, beta, act=0, in_kind="f16", out="f32", b_trans=False):
     return C.float().cpu().numpy().astype(np.float64), C0, g.last_plan()
 
 
-@pytest.mark.parametrize("M,N,K,split", [(128, 4096, 4096, True), (256, 4096, 4096, True), (100, 3000, 1000, True),
-                                         (96, 8192, 2048, True), (128, 11008, 4096, False)])
+@pytest.mark.parametrize("M,N,K,split", [(128, 4096, 4096, True), (256, 4096, 4096, True), (128, 2048, 8192, True),
+                                         (100, 3000, 1000, False), (96, 8192, 2048, False),
+                                         (128, 11008, 4096, False)])
 def test_planner_splits_few_tiles_over_a_cluster(M, N, K, split):
-    # split while whole 128 x 128 tiles would leave half the SMs idle
+    # split while whole 128 x 128 tiles would leave half the SMs idle and each
+    # would stream long enough to repay the hand-over (K = 1000 / 2048: no)
     d = inputs.make_batched(1, M, N, K, kind="f16", seed=M + N, beta=0.0, bias=True)
     got, _, plan = run(d, 0.5, 0.0, act=1)
     assert ("clusterk" in plan) == split, plan
