@@ -18,9 +18,9 @@ graph keeps its own split-K scratch).  Every graph is replayed once to drop
 the clear losers, then the planner's graph and the finalists are replayed in
 interleaved rounds and each keeps the median: GPU clock and temperature drift
 over a tuning run by several percent, and interleaving puts that drift on
-every candidate alike.  An entry is written only when the best candidate beats
-the planner's own choice by more than ``--min-gain`` (default 3 %: two graphs of the same plan differ
-by up to ~3 % on a GB300).
+every candidate alike.  An entry is written only when the best candidate is a
+different plan and beats the planner's own choice by more than ``--min-gain`` (default 3 %: two graphs
+of the same plan differ by up to ~4 % on a GB300).
 """
 from __future__ import annotations
 
@@ -166,7 +166,10 @@ def tune_shape(path: int, M: int, N: int, K: int, *, min_gain: float = 0.03, rou
     if verbose:
         print(f"path {path} {M}x{N}x{K}: planner {planner_plan} {planner.ms * 1e3:.1f} us, "
               f"best {best_plan} {best_t.ms * 1e3:.1f} us ({gain * 100:+.1f} %)", flush=True)
-    return (best_entry if gain > min_gain else None), report
+    # the planner's own plan under a table entry only measures graph-to-graph
+    # drift (a negative min_gain writes the best candidate whatever it is)
+    same_plan = min_gain >= 0 and best_plan.replace("+tuned", "") == planner_plan
+    return (best_entry if gain > min_gain and not same_plan else None), report
 
 
 def _parse_shape(text: str):
