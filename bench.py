@@ -403,14 +403,59 @@ def source_sha(sources):
     return h.hexdigest()[:16]
 
 
+def _workload_call(w, d, dev, nsets):
+    """Device copies (nsets sets of A, B, C) of a named workload's arrays and
+    call(t, stream=None), the library call the workload names."""
+    import torch
+
+    import dense_gemm_11_gb300 as g
+    in_t = torch.bfloat16 if w.kind == "bf16" else None
+    out_t = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out]
+    general = w.kind != "f32" and (w.batch > 1 or w.b_trans or w.out != "f32")
+    sets = []
+    for _ in range(nsets):
+        t = {k: torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")}
+        if in_t is not None:  # bf16 values travel as float32 arrays
+            t["A"], t["B"] = t["A"].to(in_t), t["B"].to(in_t)
+        t["C"] = t["C"].to(out_t)
+        if general and w.batch == 1 and not w.b_trans:
+            t = {k: v.unsqueeze(0) for k, v in t.items()}
+        sets.append(t)
+    bias = torch.from_numpy(d["bias"]).to(dev) if "bias" in d else None
+
+    def call(t, st=None):
+        st = torch.cuda.current_stream(dev) if st is None else st
+        if general:
+            g.gemm_tc_batched(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias, act=w.act,
+                              b_trans=w.b_trans, stream=st)
+        elif w.kind == "f32":
+            g.gemm_f32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
+        elif w.kind == "f32x3":
+            g.gemm_f32_3xtf32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
+        elif w.kind == "bf16":
+            g.gemm_bf16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
+                                        act=w.act, stream=st)
+        else:
+            g.gemm_f16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
+                                       act=w.act, stream=st)
+
+    return sets, call
+
+
 def run_profile_case(case: str, repeats: int):
-    """One GEMM of the bench workload, launched `repeats` times, for ncu captures."""
+    """One GEMM launched `repeats` times, for ncu captures: the bench's FP32
+    SGEMM ("sgemm"), its FP16 GEMM ("hgemm"), FP32 through 3 x TF32 at
+    4096^3 ("tf32x3"), or any named workload of inputs.WORKLOADS."""
     import torch
 
     import dense_gemm_11_gb300 as g
     from dense_gemm_11_gb300 import inputs
     dev = torch.device("cuda", 0)
-    if case in ("sgemm", "tf32x3"):
+    if case in inputs.WORKLOADS:
+        sets, call = _workload_call(inputs.WORKLOADS[case], inputs.make_workload(inputs.WORKLOADS[case]), dev, 1)
+        for _ in range(repeats):
+            call(sets[0])
+    elif case in ("sgemm", "tf32x3"):
         d = inputs.make_workload(inputs.WORKLOADS["f32_sq4096"])
         A, B, C = (torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C"))
         fn = g.gemm_f32 if case == "sgemm" else g.gemm_f32_3xtf32
@@ -453,36 +498,8 @@ def run_sweep(reps: int, only=None):
         d = inputs.make_workload(w)
         set_bytes = sum(d[k].nbytes for k in ("A", "B", "C"))
         nbuf = max(1, min(16, -(-3 * l2_bytes // set_bytes)))
-        in_t = torch.bfloat16 if w.kind == "bf16" else None
-        out_t = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out]
-        general = w.kind != "f32" and (w.batch > 1 or w.b_trans or w.out != "f32")
-        sets = []
-        for _ in range(nbuf):
-            t = {k: torch.from_numpy(d[k]).to(dev) for k in ("A", "B", "C")}
-            if in_t is not None:  # bf16 values travel as float32 arrays
-                t["A"], t["B"] = t["A"].to(in_t), t["B"].to(in_t)
-            t["C"] = t["C"].to(out_t)
-            if general and w.batch == 1 and not w.b_trans:
-                t = {k: v.unsqueeze(0) for k, v in t.items()}
-            sets.append(t)
+        sets, call = _workload_call(w, d, dev, nbuf)
         C0 = sets[0]["C"].clone()
-        bias = torch.from_numpy(d["bias"]).to(dev) if "bias" in d else None
-
-        def call(t, st=None):
-            st = torch.cuda.current_stream(dev) if st is None else st
-            if general:
-                g.gemm_tc_batched(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias, act=w.act,
-                                  b_trans=w.b_trans, stream=st)
-            elif w.kind == "f32":
-                g.gemm_f32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
-            elif w.kind == "f32x3":
-                g.gemm_f32_3xtf32(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=st)
-            elif w.kind == "bf16":
-                g.gemm_bf16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
-                                            act=w.act, stream=st)
-            else:
-                g.gemm_f16_f32acc_epilogue(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, bias=bias,
-                                           act=w.act, stream=st)
 
         times = []
         for r in range(reps + 3):
@@ -551,8 +568,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["sgemm", "hgemm", "tf32x3"], default=None,
-                    help="launch one 4096^3 GEMM of the workload a few times (for ncu) and exit")
+    ap.add_argument("--profile-case", default=None,
+                    help="launch one GEMM a few times (for ncu) and exit: sgemm, hgemm or tf32x3 (the 4096^3 "
+                         "bench GEMMs) or a workload name of inputs.WORKLOADS")
     ap.add_argument("--repeats", type=int, default=2)
     ap.add_argument("--sweep", action="store_true", help="time every named workload, one JSON line each")
     ap.add_argument("--workloads", default="", help="comma-separated workload names for --sweep (default: all)")
