@@ -1442,9 +1442,10 @@ cudaError_t launch_hgemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
 // GPU holds at once (cached per cluster size; one device type per process).
 template <int BN, int STAGES>
 int cluster_split_capacity(int cs) {
-    static int cap[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    static int cap[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // atomic accesses: planners may run concurrently
     if (cs < 1 || cs > 8) return 0;
-    if (cap[cs] >= 0) return cap[cs];
+    const int known = __atomic_load_n(&cap[cs], __ATOMIC_ACQUIRE);
+    if (known >= 0) return known;
     using Cfg = HgemmCfg<BN, STAGES, false, true>;
     auto kern = hgemm_tc_kernel<BN, STAGES, false, true>;
     static unsigned long long smem_set = 0;
@@ -1465,7 +1466,7 @@ int cluster_split_capacity(int cs) {
         (void)cudaGetLastError();
         n = 0;
     }
-    cap[cs] = n;
+    __atomic_store_n(&cap[cs], n, __ATOMIC_RELEASE);
     return n;
 }
 
@@ -1481,7 +1482,7 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
                               const CUtensorMap *tb2 = nullptr) {
     using Cfg = HgemmPairCfg<BN, STAGES, EPI, X3>;
     auto kern = hgemm_tc_pair_kernel<BN, STAGES, EPI, X3>;
-    static int max_clusters = -1;  // per instantiation; one device type per process
+    static int max_clusters = -1;  // per instantiation; one device type per process; atomic accesses
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, Cfg::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
@@ -1498,15 +1499,15 @@ cudaError_t launch_hgemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, cons
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_clusters < 0) {
+    int clusters_max = __atomic_load_n(&max_clusters, __ATOMIC_ACQUIRE);
+    if (clusters_max < 0) {
         cfg.gridDim = dim3(2 * device_sm_count(), 1, 1);
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&clusters_max, kern, &cfg);
         if (e != cudaSuccess) return e;
-        max_clusters = n;
+        __atomic_store_n(&max_clusters, clusters_max, __ATOMIC_RELEASE);
     }
-    if (max_clusters < 1) return cudaErrorNotSupported;
-    const int clusters = std::min(a.units, max_clusters);
+    if (clusters_max < 1) return cudaErrorNotSupported;
+    const int clusters = std::min(a.units, clusters_max);
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     *clusters_used = clusters;
     HgemmArgs args = a;
