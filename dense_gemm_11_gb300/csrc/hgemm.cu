@@ -1,8 +1,10 @@
-// hgemm.cu -- FP16-input / FP32-accumulate GEMM on the 5th-generation tensor
-// cores (tcgen05) of sm_103a, with the bias / scale / GELU epilogue fused.
+// hgemm.cu -- FP16/BF16-input / FP32-accumulate GEMM on the 5th-generation
+// tensor cores (tcgen05) of sm_103a, with the bias / scale / activation
+// epilogue fused; also strided batches (B optionally stored N x K) and the
+// FP32-accuracy product through three TF32 products.
 //
-//   C = act(alpha * A x B + beta * C + bias),  A: M x K fp16 row-major,
-//   B: K x N fp16 row-major, C: M x N fp32 row-major, bias: N fp32.
+//   C = act(alpha * A x B + beta * C + bias),  A: M x K row-major,
+//   B: K x N (or N x K) row-major, C: M x N fp32/fp16/bf16, bias: N fp32.
 //
 // The DeepGEMM essay "企业官网建设流程全解析" describes the Hopper version of
 // this pipeline: TMA tiles into a 4-stage shared-memory ring guarded by
@@ -22,12 +24,16 @@
 //   * the epilogue reads TMEM with tcgen05.ld, applies alpha, beta*C, bias
 //     and GELU in registers, stages the 32x32 fp32 block in swizzled shared
 //     memory and writes it with a TMA store (edges clipped by the tensor map);
+//   * M > 128: CTA pairs (tcgen05.mma.cta_group::2) compute 256-row tiles,
+//     each CTA staging its 128 rows of A and half of B;
 //   * small M (<= 64): the product is computed transposed, C^T = B^T A^T, so
 //     that N fills the 128-row side of the MMA and M becomes its N side;
-//   * too few tiles for the SMs: K is split, partial tiles go to a scratch
-//     buffer, and the last epilogue warp to finish a 32-row slice of a tile
-//     (atomic arrival count) adds the slices in split order and runs the
-//     epilogue -- deterministic, and no CTA waits for another.
+//   * too few tiles for the SMs: K is split over the CTAs of a thread-block
+//     cluster and the partial tiles are added in split order through
+//     distributed shared memory (no global scratch); the no-allocation entry
+//     and tuned plans can also split K through a scratch buffer, where the
+//     last epilogue warp to finish a 32-row slice of a tile (atomic arrival
+//     count) adds the slices in split order -- deterministic either way.
 // Every mbarrier wait is bounded; a timeout sets the watchdog word and the
 // CTA unwinds (waits for its TMA copies and MMAs, frees TMEM, returns).
 #include <algorithm>
@@ -1591,13 +1597,14 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     a.b_kmajor = g.b_trans ? 1 : 0;
 
     // Tile table.  M <= 64: transposed product with MMA N = M rounded up to
-    // 32 or 64.  Otherwise 128 x 256 tiles (128 x 128 when N <= 128).  Every
-    // CTA is persistent and takes whole tiles round-robin (tiles of all
-    // matrices of a batch in one sequence); with fewer tiles than a third of
-    // the SMs, K is split evenly and partial tiles are reduced in k order by
-    // the last contributor to arrive (per 32-row slice), inside the kernel.
-    // A tuned plan for this exact shape (single matrices only) replaces the
-    // rules below; a transposed plan that cannot hold M is ignored.
+    // 32 or 64 (K split over a cluster when its tiles fill at most half the
+    // SMs).  M > 128 with enough pair tiles: CTA pairs.  Otherwise 128-row
+    // tiles, 128 x 256 (128 x 128 when that puts more SMs to work), K split
+    // over a cluster when a time model says it pays (pick_cluster_split).
+    // Every CTA is persistent and takes whole tiles round-robin (tiles of all
+    // matrices of a batch in one sequence).  A tuned plan for this exact
+    // shape (single matrices only) replaces the rules below; a plan that
+    // cannot run the shape is ignored.
     TunePlan tp;
     bool tuned = g.batch == 1 && tune_lookup(1, M, N, K, &tp);
     if (tuned && tp.variant == 3 && M > (tp.bn ? tp.bn : 64)) tuned = false;
