@@ -1630,14 +1630,14 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     const long long tiles_ll = static_cast<long long>(a.tiles_m) * a.tiles_n * g.batch;
     if (tiles_ll > (1LL << 26)) return cudaErrorNotSupported;  // keeps every unit index and counter in int
     const int tiles = static_cast<int>(tiles_ll);
-    // K is split into at most one unit per SM while the tiles fill less than
-    // a third of the SMs -- half for the transposed plan, whose splits are
-    // added through distributed shared memory (measured: 16 x 4096 x 4096 is
-    // best at 4 splits of 32 tiles, 15.7 us; 32 x 8192 x 8192 at 2 splits of
-    // 64 tiles, 30.4 us against 41.7 us unsplit; 128 x 11008 x 4096 with no
-    // split of 86 tiles).
+    // Transposed plan: K is split into at most one unit per SM while the
+    // tiles fill at most half the SMs, the splits added through distributed
+    // shared memory (measured: 16 x 4096 x 4096 is best at 4 splits of 32
+    // tiles; 32 x 8192 x 8192 at 2 splits of 64 tiles, 30.4 us against 41.7 us
+    // unsplit).  Not transposed, K is split only over a cluster, when
+    // pick_cluster_split expects it to pay (below), or by a tuned entry.
     int splits = 1;
-    if (swap ? tiles * 2 <= sms : tiles * 3 < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
+    if (swap && tiles * 2 <= sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
     splits = std::min(splits, 32);
     if (tuned && (tp.variant == 2 || tp.variant == 3) && tp.splits > 0) splits = std::max(1, std::min(tp.splits, std::max(1, a.kb_total / 2)));
     a.splits = splits;
