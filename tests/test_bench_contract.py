@@ -1,0 +1,53 @@
+"""The benchmark's JSON line as the harness reads it, on CPU: the reference
+arm (the CPU oracle on a bounded row sample) prints one line with every key
+of the contract, and under torchrun only rank 0 prints."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*args, env=None):
+    e = dict(os.environ)
+    e.update(env or {})
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                       timeout=600, env=e, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [json.loads(line) for line in r.stdout.splitlines() if line.startswith("{")]
+
+
+@pytest.fixture(scope="module")
+def reference_line():
+    lines = run_bench("--impl", "reference", "--steps", "1", "--warmup", "0")
+    assert len(lines) == 1
+    return lines[0]
+
+
+def test_reference_line_has_the_contract_keys(reference_line):
+    r = reference_line
+    assert r["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in r, key
+    assert r["value"] > 0 and r["ms_per_step"] > 0
+    assert r["unit"] == "TFLOPS" and r["higher_is_better"] is True and r["n_gpus"] == 1
+    assert r["warmup"] >= 3  # the timing rules' minimum, applied even when asked for fewer
+    assert r["vs_baseline"] is None and r["data"] == "synthetic" and r["scaling"] == "weak"
+    assert "workload" in r["config"]
+
+
+def test_reference_line_describes_its_cpu_baseline(reference_line):
+    cb = reference_line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["unit"] == "TFLOPS"
+    assert cb["value"] == reference_line["value"] and isinstance(cb["sample"], str) and cb["sample"]
+    e2e = reference_line["e2e"]
+    assert e2e == {"value": reference_line["value"], "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    assert run_bench("--impl", "reference", "--steps", "1", env={"RANK": "1", "WORLD_SIZE": "2"}) == []
