@@ -51,3 +51,22 @@ def test_reference_line_describes_its_cpu_baseline(reference_line):
 
 def test_reference_arm_prints_on_rank_zero_only():
     assert run_bench("--impl", "reference", "--steps", "1", env={"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+@pytest.mark.gpu
+def test_our_line_has_roofline_e2e_launches_and_clocks():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    lines = run_bench("--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    assert len(lines) == 1
+    r = lines[0]
+    assert r["value"] > 0 and r["n_gpus"] == 1 and r["steps"] == 3
+    rf = r["roofline"]
+    assert rf["bound"] in ("alu", "tensor", "hbm") and rf["unit"] in ("TFLOP/s", "GB/s")
+    assert rf["peak"] > 0 and abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    assert rf["traffic"] is None or rf["traffic"] > 0
+    e2e = r["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert r["gpu_launches"] >= 2 * r["steps"]  # at least one launch per GEMM of every timed step
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(r["clocks"])
