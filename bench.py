@@ -181,6 +181,11 @@ def run_ours(args, rank, world, local_rank):
     hbm_gbs, tc_peak, tc_sustained, peak_src = _peaks()
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
+    # the tensor core's dense rate per SM, measured (untimed; see gemm_tc_rate_probe)
+    try:
+        tc_rate = g.tc_rate_probe()
+    except g.GemmError:
+        tc_rate = None
 
     w32, w16 = inputs.WORKLOADS["f32_sq4096"], inputs.WORKLOADS["f16_4096"]
     d32, d16 = inputs.make_workload(w32), inputs.make_workload(w16)
@@ -357,8 +362,9 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 x {clocks.get('sm_max_mhz') or 2070.0} MHz"},
         "roofline_tensor": {"bound": "tensor", "achieved": ach16, "peak": tc_peak, "unit": "TFLOP/s",
                             "frac": ach16 / tc_peak, "traffic": traffic.get("hgemm"),
-                            "kernel": "hgemm_tc_kernel (tcgen05 f16)",
-                            "peak_source": f"{peak_src} bf16 burst (fp16 runs at the bf16 rate)"},
+                            "kernel": f"tcgen05 f16 GEMM, plan {plans.get('gemm_f16')}",
+                            "peak_source": f"{peak_src} bf16 burst (fp16 runs at the bf16 rate)",
+                            **_nominal_tensor_peak(tc_rate, sms, clocks.get("sm_max_mhz") or 2070.0, ach16)},
         "e2e": {"value": replica_throughput(FLOPS_STEP, world, e2e_ms), "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipelining": "two device buffer sets, three streams: inputs of step i+1 and results of "
@@ -372,6 +378,15 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def _nominal_tensor_peak(rate, sms, mhz, achieved):
+    """#SM x the measured dense FLOP per clock per SM x the maximum SM clock."""
+    if not rate:
+        return {"nominal_peak": None}
+    nominal = rate * sms * mhz * 1e6 / 1e12
+    return {"nominal_peak": nominal, "frac_of_nominal": achieved / nominal,
+            "nominal_source": f"{sms} SMs x {rate:.0f} FLOP/clock/SM (tcgen05 rate probe) x {mhz:.0f} MHz"}
 
 
 def _traffic_from_profiles():

@@ -53,7 +53,7 @@ EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_f16_f32acc_epilogue", "
                     "gemm_tc_f32acc_epilogue", "gemm_tc_strided_batched", "gemm_f16_f32acc_epilogue_noalloc",
                     "gemm_tune_set", "gemm_tune_get",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
-                    "gemm_last_plan", "gemm_last_launch_count")
+                    "gemm_last_plan", "gemm_last_launch_count", "gemm_tc_rate_probe")
 
 _lock = threading.Lock()
 _lib = None
@@ -113,6 +113,8 @@ def lib():
             L.gemm_last_plan.argtypes = []
             L.gemm_last_launch_count.restype = c_int
             L.gemm_last_launch_count.argtypes = []
+            L.gemm_tc_rate_probe.restype = c_int
+            L.gemm_tc_rate_probe.argtypes = [c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
             _lib = L
     return _lib
 
@@ -397,6 +399,16 @@ def load_tuning(path: str) -> int:
 def watchdog_selftest(wait_ms: int = 20, stream=None) -> int:
     """Enqueue the watchdog probe (a wait that must time out after wait_ms); returns the status."""
     return int(lib().gemm_watchdog_selftest(int(wait_ms), _stream_handle(stream)))
+
+
+def tc_rate_probe(iters: int = 4096, stream=None) -> float:
+    """The tensor core's dense FP16/BF16 rate per SM in FLOP per clock,
+    measured by timing back-to-back MMAs on every SM (median over the SMs)."""
+    out = ctypes.c_double(0.0)
+    st = lib().gemm_tc_rate_probe(int(iters), ctypes.byref(out), _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_tc_rate_probe")
+    return float(out.value)
 
 
 def check(stream=None) -> int:

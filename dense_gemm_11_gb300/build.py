@@ -11,7 +11,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libgemm11.so")
-SOURCES = ["api.cu", "sgemm.cu", "hgemm.cu"]
+SOURCES = ["api.cu", "sgemm.cu", "hgemm.cu", "probe.cu"]
 HEADERS = ["internal.h", "ptx.cuh", os.path.join("..", "..", "include", "gemm11.h")]
 
 NVCC_FLAGS = [

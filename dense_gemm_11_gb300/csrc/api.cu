@@ -500,6 +500,19 @@ int gemm_watchdog_selftest(int wait_ms, void *stream) {
     return GEMM_OK;
 }
 
+int gemm_tc_rate_probe(int iters, double *flop_per_clock_per_sm, void *stream) {
+    if (iters < 1 || iters > (1 << 20) || !flop_per_clock_per_sm) return GEMM_ERR_INVALID_ARG;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    const cudaError_t e = run_tc_rate_probe(iters, flop_per_clock_per_sm, static_cast<cudaStream_t>(stream));
+    t_last_plan = "tc_rate_probe";
+    t_last_launches = 1;
+    if (e == cudaErrorLaunchTimeout) return GEMM_ERR_TIMEOUT;
+    if (e != cudaSuccess) return fail_cuda(e);
+    return GEMM_OK;
+}
+
 const char *gemm_last_plan(void) { return t_last_plan; }
 
 int gemm_last_launch_count(void) { return t_last_launches; }

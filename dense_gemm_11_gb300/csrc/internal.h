@@ -130,4 +130,9 @@ cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float
 cudaError_t run_scale_c_batched(int batch, int M, int N, float beta, void *C, long long stride_c, int c_type,
                                 const float *bias, int act, cudaStream_t stream, CallInfo *info);
 
+// The tensor core's dense kind::f16 rate (FLOP per SM clock), measured by
+// timing back-to-back 128 x 256 x 16 MMAs on every SM (probe.cu); synchronous
+// on `stream`.  cudaErrorLaunchTimeout if no SM finished within the bounded wait.
+cudaError_t run_tc_rate_probe(int iters, double *flop_per_clock_per_sm, cudaStream_t stream);
+
 }  // namespace gemm11

@@ -303,6 +303,23 @@ GEMM11_API int gemm_check(void *stream);
 GEMM11_API int gemm_watchdog_selftest(int wait_ms, void *stream);
 
 /*
+ * gemm_tc_rate_probe -- diagnostic: the tensor core's dense FP16/BF16 rate
+ * per SM, measured.  One CTA per SM issues `iters` x 4 back-to-back
+ * tcgen05.mma instructions of shape 128 x 256 x 16 (BF16 operands resident in
+ * shared memory, FP32 accumulator in tensor memory; no global-memory
+ * traffic) and times them with the SM cycle counter; *flop_per_clock_per_sm
+ * receives the median over the SMs of 2 * 128 * 256 * 16 * 4 * iters /
+ * cycles.  #SM x this rate x the SM clock is the nominal dense peak that the
+ * FP16 path's throughput is quoted against besides the measured cuBLAS rate.
+ * Synchronous on `stream` (it allocates and frees a small device buffer).
+ * iters in 1..2^20 (a few thousand take about a millisecond).  Returns
+ * GEMM_OK, GEMM_ERR_INVALID_ARG (iters out of range, NULL output),
+ * GEMM_ERR_TIMEOUT (no SM completed within the bounded wait) or
+ * GEMM_ERR_CUDA.
+ */
+GEMM11_API int gemm_tc_rate_probe(int iters, double *flop_per_clock_per_sm, void *stream);
+
+/*
  * Introspection for tests and benchmarks: the name of the kernel plan the
  * calling thread's last successful call used (static storage), and how many
  * kernels that call launched.

@@ -34,3 +34,4 @@ def test_watchdog_timeout_is_reported_and_cleared():
 def test_watchdog_selftest_rejects_bad_limits():
     assert g.watchdog_selftest(0) == g.GEMM_ERR_INVALID_ARG
     assert g.watchdog_selftest(5000) == g.GEMM_ERR_INVALID_ARG
+
