@@ -35,6 +35,7 @@
 //    section 8.3 question 2 discusses these GEMV-like shapes).
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -503,7 +504,10 @@ __global__ void __launch_bounds__(256) sgemm_streamk_fixup_kernel(const SgemmArg
 
 // ------------------------------------------------------------------ GEMV
 // N == 1: y_i = alpha * sum_k A[i, k] * x_k + beta * y_i, one warp per row,
-// x_k = B[k * incx], y_i = C[i * incy].  A streams once from HBM.
+// x_k = B[k * incx], y_i = C[i * incy].  A streams once from HBM.  vec: A's
+// rows are 16-byte aligned (lda % 4 == 0) and read as float4; x is read as
+// float4 too when contiguous (incx == 1, 16-byte aligned), else element by
+// element (a column of a row-major B).
 __global__ void __launch_bounds__(256) sgemv_rows_kernel(int M, int K, float alpha, const float *__restrict__ A,
                                                          int lda, const float *__restrict__ x, int incx,
                                                          float beta, float *y, int incy, int vec) {
@@ -520,7 +524,12 @@ __global__ void __launch_bounds__(256) sgemv_rows_kernel(int M, int K, float alp
 #pragma unroll 16
         for (int c = lane; c < K4; c += 32) {
             const float4 av = __ldcs(a4 + c);
-            const float4 xv = __ldg(x4 + c);
+            const float4 xv =
+                incx == 1 ? __ldg(x4 + c)
+                          : make_float4(__ldg(x + static_cast<size_t>(4 * c) * incx),
+                                        __ldg(x + static_cast<size_t>(4 * c + 1) * incx),
+                                        __ldg(x + static_cast<size_t>(4 * c + 2) * incx),
+                                        __ldg(x + static_cast<size_t>(4 * c + 3) * incx));
             s0 = fmaf(av.x, xv.x, s0);
             s1 = fmaf(av.y, xv.y, s1);
             s2 = fmaf(av.z, xv.z, s2);
@@ -873,28 +882,60 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         info->tuned = true;
     }
     cudaError_t e;
+    // Edge strip (the pages' main tiles plus separate edge kernels): when the
+    // last 256-wide tile column would hold at most 64 real columns, the big
+    // tiles cover the first N0 = N - r columns and the r-column strip runs
+    // after them -- as a matrix-vector product when r = 1, else as 64x64
+    // tiles -- instead of a column of mostly empty 128 x 256 tiles
+    // (4095 x 4097 x 4099: 544 -> 512 big tiles).
+    const int strip = (big && N > 256 && N % 256 != 0 && N % 256 <= 64) ? N % 256 : 0;
+    const int N0 = N - strip;
     if (big) {
+        a.N = N0;
         a.tiles_m = (M + 127) / 128;
-        a.tiles_n = (N + 255) / 256;
+        a.tiles_n = (N0 + 255) / 256;
         a.splits = 1;
         a.persistent = 1;
-        const int rem = tiles_big % sms;
-        a.dp_tiles = tiles_big - rem;
+        const int tiles_main = a.tiles_m * a.tiles_n;
+        const int rem = tiles_main % sms;
+        a.dp_tiles = tiles_main - rem;
         a.sk_tiles = rem;
         const long long share = static_cast<long long>(rem) * KT / sms;  // k slices per CTA
         // too few k slices to share out (or too many CTAs per tile for the
         // fixup's owner list): whole tiles only
         if (rem != 0 && (share < 2 || KT / share + 2 > 64)) {
-            a.dp_tiles = tiles_big;
+            a.dp_tiles = tiles_main;
             a.sk_tiles = 0;
         }
-        a.grid_ctas = a.sk_tiles > 0 ? sms : std::min(sms, tiles_big);
-        if (a.sk_tiles > 0) {
+        a.grid_ctas = a.sk_tiles > 0 ? sms : std::min(sms, tiles_main);
+        // A strip of r > 1 columns runs as 64x64 tiles with split K; its
+        // partials follow the big tiles' stream-K partials in one scratch
+        // request made before anything is launched (a request that grows the
+        // buffer synchronises the stream).
+        SgemmArgs s2 = a;
+        if (strip > 1) {
+            s2.N = strip;
+            s2.B = a.B + N0;
+            s2.C = C + N0;
+            s2.c_vec = aligned16(s2.C) && (ldc % 4 == 0);
+            s2.tiles_m = (M + 63) / 64;
+            s2.tiles_n = 1;
+            s2.persistent = 0;
+            s2.dp_tiles = s2.sk_tiles = s2.grid_ctas = 0;
+            int splits = 1;
+            if (s2.tiles_m < sms && KT > 4) splits = std::max(1, std::min((sms + s2.tiles_m / 2) / s2.tiles_m, KT / 2));
+            s2.splits = std::min(splits, 16);
+        }
+        const size_t main_floats = a.sk_tiles > 0 ? static_cast<size_t>(2) * a.grid_ctas * 128 * 256 : 0;
+        const size_t strip_floats = (strip > 1 && s2.splits > 1) ? static_cast<size_t>(s2.tiles_m) * s2.splits * 64 * 64 : 0;
+        if (main_floats + strip_floats > 0) {
             Scratch sc;
-            e = acquire_scratch(stream, static_cast<size_t>(2) * a.grid_ctas * 128 * 256, 0, &sc);
+            e = acquire_scratch(stream, main_floats + strip_floats, strip_floats > 0 ? s2.tiles_m : 0, &sc);
             if (e != cudaSuccess) return e;
             a.ws = sc.partials;
             a.counters = sc.counters;
+            s2.ws = sc.partials + main_floats;
+            s2.counters = sc.counters;
         }
         e = vec ? launch_tiled<128, 256, 2, 4, 8, 16, 3, true, true>(a, stream)
                 : launch_tiled<128, 256, 2, 4, 8, 16, 3, false, true>(a, stream);
@@ -902,12 +943,30 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         if (a.sk_tiles > 0) {
             e = launch_kernel(sgemm_streamk_fixup_kernel<128, 256>, dim3(a.sk_tiles, 128 / 8), dim3(256), 0, stream, a);
         }
+        if (e != cudaSuccess) return e;
         info->launches = (a.sk_tiles > 0 ? 2 : 1) + repacked;
         if (a.sk_tiles > 0)
             info->plan = repacked ? "sgemm_repack_128x256_vec16_streamk"
                                   : (vec ? "sgemm_128x256_vec16_streamk" : "sgemm_128x256_vec4b_streamk");
         else
             info->plan = repacked ? "sgemm_repack_128x256_vec16" : (vec ? "sgemm_128x256_vec16" : "sgemm_128x256_vec4b");
+        if (strip == 1) {
+            // y = C[:, N0] over the rows of A, x = B[:, N0] (stride ldb, read element-wise)
+            const int vrow = aligned16(a.A) && (a.lda % 4 == 0);
+            e = launch_kernel(sgemv_rows_kernel, dim3((M + 7) / 8), dim3(256), 0, stream, M, K, alpha, a.A, a.lda,
+                              a.B + N0, a.ldb, beta, C + N0, ldc, vrow);
+            ++info->launches;
+        } else if (strip > 1) {
+            e = vec ? launch_tiled<64, 64, 2, 2, 4, 8, 3, true, false>(s2, stream)
+                    : launch_tiled<64, 64, 2, 2, 4, 8, 3, false, false>(s2, stream);
+            ++info->launches;
+        }
+        if (strip) {
+            // the plan of this thread's last call (valid until its next call)
+            static thread_local char plan_buf[96];
+            std::snprintf(plan_buf, sizeof(plan_buf), "%s+colstrip%s", info->plan, strip == 1 ? "1" : "");
+            info->plan = plan_buf;
+        }
     } else {
         // Small problems: 64x64 CTAs (4 warps of 32x32, 4x8 per thread), with
         // K split so that there are about as many CTAs as SMs, each split at

@@ -208,3 +208,23 @@ def test_tuned_f32_plans_are_exact(variant, splits):
     assert plan.endswith("+tuned"), plan
     ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=1.0, with_scale=False)
     np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), ref, err_msg=plan)
+
+
+@pytest.mark.parametrize("M,N,K,strip", [(2048, 2049, 1024, 1), (2048, 2088, 512, 40), (1800, 2305, 700, 1)])
+def test_f32_column_edge_strip_exact(M, N, K, strip):
+    # Big tiles cover the first N - r columns and the r-column edge strip runs
+    # on its own (a matrix-vector product for r = 1); C's padding (ldc > N)
+    # stays untouched.  Small integers: exact whatever the summation order.
+    ldc = N + 5
+    d = inputs.make(M, N, K, kind="f32", dist="smallint", seed=N + K, beta=1.0, ldc=ldc)
+    got, plan = run_f32(d, 1.0, 1.0, N=N)
+    assert plan.endswith("+colstrip1" if strip == 1 else "+colstrip"), plan
+    N0 = N - strip
+    rows = sample_rows(M, seed=5)
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=1.0, N=N, rows=rows, with_scale=False)
+    np.testing.assert_array_equal(got[rows, :N].astype(np.float64), ref, err_msg=plan)
+    # every row of the strip
+    ref_s, _ = oracle.gemm(d["A"], np.ascontiguousarray(d["B"][:, N0:N]), np.ascontiguousarray(d["C"][:, N0:N]),
+                           alpha=1.0, beta=1.0, with_scale=False)
+    np.testing.assert_array_equal(got[:, N0:N].astype(np.float64), ref_s, err_msg=plan)
+    np.testing.assert_array_equal(got[:, N:], d["C"][:, N:])
