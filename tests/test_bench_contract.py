@@ -70,3 +70,13 @@ def test_our_line_has_roofline_e2e_launches_and_clocks():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert r["gpu_launches"] >= 2 * r["steps"]  # at least one launch per GEMM of every timed step
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(r["clocks"])
+
+
+def test_nominal_tensor_peak_arithmetic():
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench._nominal_tensor_peak(8192.0, 152, 2070.0, 1500.0)
+    assert abs(r["nominal_peak"] - 8192 * 152 * 2070e6 / 1e12) < 1e-9
+    assert abs(r["frac_of_nominal"] - 1500.0 / r["nominal_peak"]) < 1e-12
+    assert "152 SMs" in r["nominal_source"]
+    assert bench._nominal_tensor_peak(None, 152, 2070.0, 1500.0) == {"nominal_peak": None}
