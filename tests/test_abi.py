@@ -195,3 +195,30 @@ def test_shipped_tuning_table_installs(L):
         assert n == len(g.tune_get()) and n >= 0
     finally:
         g.tune_set([])
+
+
+def test_missing_library_raises_instead_of_falling_back():
+    # a fresh interpreter whose library path points nowhere: the first call
+    # that needs the library raises; nothing computes on the CPU instead
+    import subprocess
+    import sys
+    code = ("import dense_gemm_11_gb300 as g\n"
+            "g.LIB_PATH = '/nonexistent/libgemm11.so'\n"
+            "try:\n"
+            "    g.status_string(0)\n"
+            "except RuntimeError as e:\n"
+            "    print('raised:', e)\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "raised:" in r.stdout and "not built" in r.stdout, r.stdout
+
+
+def test_package_never_reaches_the_oracle():
+    # the product path shares no code with the CPU oracle and never imports it
+    pkg = os.path.join(ROOT, "dense_gemm_11_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "gemm_oracle" not in text and "oracle_gemm" not in text, f
