@@ -80,3 +80,26 @@ def test_nominal_tensor_peak_arithmetic():
     assert abs(r["frac_of_nominal"] - 1500.0 / r["nominal_peak"]) < 1e-12
     assert "152 SMs" in r["nominal_source"]
     assert bench._nominal_tensor_peak(None, 152, 2070.0, 1500.0) == {"nominal_peak": None}
+
+
+def test_profile_summaries_name_commands_the_bench_accepts():
+    # every ncu summary gives the command that made it; its bench.py flags and
+    # profile cases must still exist, so the capture can be repeated
+    import re
+    sys.path.insert(0, ROOT)
+    from dense_gemm_11_gb300 import inputs
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    flags = set(re.findall(r'add_argument\("(--[\w-]+)"', src))
+    cases = set(inputs.WORKLOADS) | {"sgemm", "hgemm", "tf32x3"}
+    pdir = os.path.join(ROOT, "profiles")
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        text = open(os.path.join(pdir, f), encoding="utf-8").read()
+        cmds = re.findall(r"python bench\.py([^\n>&|]*)", text)
+        assert cmds, f"{f} names no bench.py command"
+        for c in cmds:
+            for flag in re.findall(r"(--[\w-]+)", c):
+                assert flag in flags, (f, flag)
+            for case in re.findall(r"--profile-case\s+(\S+)", c):
+                assert case in cases, (f, case)
