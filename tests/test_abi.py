@@ -222,3 +222,32 @@ def test_package_never_reaches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "gemm_oracle" not in text and "oracle_gemm" not in text, f
+
+
+@pytest.mark.parametrize("raw", ["gemm_f32_raw", "gemm_f32_3xtf32_raw"])
+def test_f32_argument_rules_on_random_tuples(L, raw):
+    # Seeded random argument tuples judged by the rules the header states:
+    # negative sizes and short leading dimensions are rejected first, an empty
+    # C is a no-op, then a NULL C (or a NULL A / B when there is a product)
+    # is rejected.  Tuples that would pass every host check are never called:
+    # the pointers here are fake and must not reach a kernel.
+    import numpy as np
+    f = getattr(g, raw)
+    rng = np.random.default_rng(71)
+    called = {"invalid": 0, "noop": 0}
+    for _ in range(4000):
+        M, N, K = (int(v) for v in rng.integers(-2, 6, size=3))
+        lda, ldb, ldc = (int(v) for v in rng.integers(-1, 7, size=3))
+        alpha = float(rng.choice([0.0, 1.0]))
+        A, B, C = (int(v) for v in rng.choice([0, FAKE], size=3))
+        if M < 0 or N < 0 or K < 0 or lda < max(1, K) or ldb < max(1, N) or ldc < max(1, N):
+            want = g.GEMM_ERR_INVALID_ARG
+        elif M == 0 or N == 0:
+            want = g.GEMM_OK
+        elif C == 0 or (K > 0 and alpha != 0.0 and (A == 0 or B == 0)):
+            want = g.GEMM_ERR_INVALID_ARG
+        else:
+            continue
+        assert f(M, N, K, alpha, A, lda, B, ldb, 0.5, C, ldc) == want, (M, N, K, lda, ldb, ldc, alpha, A, B, C)
+        called["noop" if want == g.GEMM_OK else "invalid"] += 1
+    assert called["invalid"] > 500 and called["noop"] > 50, called
