@@ -69,7 +69,7 @@ def test_batched_parity(batch, M, N, K, b_trans):
     act = (M + K) % 4
     got, C0, plan = run_batched(d, "f16", "f32", 0.75, 0.5, b_trans, act)
     ref, S = oracle_batch(d, C0, 0.75, 0.5, b_trans, act)
-    assert_within(got, ref, S, TOL_F16, f"{batch}x{M}x{N}x{K} trans={b_trans} [{plan}]")
+    assert_within(got, ref, S, TOL_F16, f"{batch}x{M}x{N}x{K} trans={b_trans} [{plan}]", bias=d.get("bias"))
 
 
 @pytest.mark.parametrize("b_trans", [False, True])
@@ -160,4 +160,4 @@ def test_batched_small_m_cluster_split(out, b_trans):
     got, C0, plan = run_batched(d, "bf16", out, 0.5, 1.5, b_trans, act=3)
     assert "clusterk" in plan, plan
     ref, S = oracle_batch(d, C0, 0.5, 1.5, b_trans, act=3)
-    assert_within(got, ref, S, TOL_F16, f"{out} trans={b_trans} [{plan}]", out=out)
+    assert_within(got, ref, S, TOL_F16, f"{out} trans={b_trans} [{plan}]", out=out, bias=d.get("bias"))

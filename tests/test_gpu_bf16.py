@@ -48,7 +48,7 @@ def check_workload(name, rows=None, exact=False):
     if exact:
         np.testing.assert_array_equal(sel.astype(np.float64), ref, err_msg=f"{name} [{plan}]")
         return plan
-    assert_within(sel, ref, S, TOL_F16, f"{name} [{plan}]")
+    assert_within(sel, ref, S, TOL_F16, f"{name} [{plan}]", bias=bias)
     return plan
 
 
@@ -74,7 +74,7 @@ def test_bf16_ragged_shapes(M, N, K, act):
     d = inputs.make(M, N, K, kind="bf16", dist="normal_k", seed=M * 7 + N + K, beta=0.0, bias=True)
     got, plan = run_bf16(d, 1.5, 0.0, d["bias"], act)
     ref, S = oracle.gemm(d["A"], d["B"], None, alpha=1.5, beta=0.0, bias=d["bias"], act=act)
-    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} act={act} [{plan}]")
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} act={act} [{plan}]", bias=d["bias"])
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 1024), (128, 1024, 4096), (384, 512, 640), (5, 64, 4096),
@@ -93,7 +93,7 @@ def test_bf16_cta_pair_ragged(M, N, K, act):
     got, plan = run_bf16(d, -0.75, 0.25, d["bias"], act)
     assert "pair" in plan
     ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=-0.75, beta=0.25, bias=d["bias"], act=act)
-    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} act={act} [{plan}]")
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} act={act} [{plan}]", bias=d["bias"])
 
 
 def test_bf16_values_outside_fp16_range():

@@ -47,7 +47,7 @@ def test_planner_splits_few_tiles_over_a_cluster(M, N, K, split):
     assert ("clusterk" in plan) == split, plan
     rows = sample_rows(M, seed=60)
     ref, S = oracle.gemm(d["A"][0], d["B"][0], None, alpha=0.5, bias=d["bias"], act=1, rows=rows)
-    assert_within(got[0][rows], ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+    assert_within(got[0][rows], ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]", bias=d["bias"])
 
 
 @pytest.mark.parametrize("bn,cs", [(256, 2), (256, 3), (256, 8), (192, 2), (192, 5), (128, 4), (128, 3), (256, 0)])
@@ -98,7 +98,7 @@ def test_batched_16bit_output_and_transposed_b(in_kind, out, b_trans):
     for z in range(batch):
         Bz = d["B"][z].T if b_trans else d["B"][z]
         ref, S = oracle.gemm(d["A"][z], Bz, C0[z], alpha=1.25, beta=-0.75, bias=d["bias"], act=3)
-        assert_within(got[z], ref, S, TOL_F16, f"z={z} {in_kind}->{out} trans={b_trans} [{plan}]", out=out)
+        assert_within(got[z], ref, S, TOL_F16, f"z={z} {in_kind}->{out} trans={b_trans} [{plan}]", out=out, bias=d["bias"])
 
 
 def test_deterministic_across_calls():

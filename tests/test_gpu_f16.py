@@ -40,7 +40,7 @@ def check_workload(name, rows=None, exact=False):
     if exact:
         np.testing.assert_array_equal(sel.astype(np.float64), ref, err_msg=f"{name} [{plan}]")
         return plan
-    assert_within(sel, ref, S, TOL_F16, f"{name} [{plan}]")
+    assert_within(sel, ref, S, TOL_F16, f"{name} [{plan}]", bias=bias)
     return plan
 
 
@@ -65,7 +65,7 @@ def test_f16_ragged_shapes(M, N, K):
     d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=M * 131 + N + K, beta=0.0, bias=True)
     got, plan = run_f16(d, 1.5, 0.0, d["bias"], 0)
     ref, S = oracle.gemm(d["A"], d["B"], None, alpha=1.5, beta=0.0, bias=d["bias"])
-    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]", bias=d["bias"])
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 1024), (128, 1024, 4096), (384, 512, 640), (5, 64, 4096),
@@ -83,7 +83,7 @@ def test_f16_beta_and_bias_epilogue(M, N, K, act):
     d = inputs.make(M, N, K, kind="f16", dist="normal_k", seed=7, beta=-0.5, bias=True)
     got, plan = run_f16(d, 0.5, -0.5, d["bias"], act)
     ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=0.5, beta=-0.5, bias=d["bias"], act=act)
-    assert_within(got, ref, S, TOL_F16, f"beta/bias act={act} [{plan}]")
+    assert_within(got, ref, S, TOL_F16, f"beta/bias act={act} [{plan}]", bias=d["bias"])
 
 
 @pytest.mark.parametrize("M,N,K", [(129, 9728, 128), (300, 8448, 200), (1000, 4000, 520), (4100, 4104, 64)])
@@ -92,7 +92,7 @@ def test_f16_cta_pair_ragged(M, N, K):
     got, plan = run_f16(d, -0.75, 0.25, d["bias"], 1)
     assert "pair" in plan
     ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=-0.75, beta=0.25, bias=d["bias"], act=1)
-    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]", bias=d["bias"])
 
 
 def test_f16_beta_zero_does_not_read_c():
@@ -112,7 +112,7 @@ def test_f16_alpha_zero_epilogue_only(act):
     g.gemm_f16_f32acc_epilogue(A, B, C, alpha=0.0, beta=2.0, bias=torch.from_numpy(bias).to(DEV), act=act)
     torch.cuda.synchronize()
     ref, S = oracle.gemm(np.zeros((33, 16)), np.zeros((16, 24)), C0, alpha=0.0, beta=2.0, bias=bias, act=act)
-    assert_within(C.cpu().numpy(), ref, S, 1e-6, f"alpha=0 act={act}")
+    assert_within(C.cpu().numpy(), ref, S, 1e-6, f"alpha=0 act={act}", bias=bias)
 
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (16, 4096, 4096), (128, 11008, 4096)])
@@ -145,7 +145,7 @@ def test_f16_unaligned_bias_pointer(M, N, K):
     g.gemm_f16_f32acc_epilogue(A, B, C, alpha=0.5, beta=0.0, bias=bias, act=1)
     assert g.check() == g.GEMM_OK
     ref, S = oracle.gemm(d["A"], d["B"], None, alpha=0.5, beta=0.0, bias=d["bias"], act=1)
-    assert_within(C.cpu().numpy(), ref, S, TOL_F16, f"unaligned bias [{g.last_plan()}]")
+    assert_within(C.cpu().numpy(), ref, S, TOL_F16, f"unaligned bias [{g.last_plan()}]", bias=d["bias"])
 
 
 @pytest.mark.parametrize("act", [1, 2, 3])
@@ -221,7 +221,7 @@ def test_f16_cluster_split_k(M, N, K):
     got, plan = run_f16(d, 1.25, 0.5, d["bias"], 1)
     assert "clusterk" in plan, plan
     ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.25, beta=0.5, bias=d["bias"], act=1)
-    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+    assert_within(got, ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]", bias=d["bias"])
 
 
 @pytest.mark.parametrize("M,N,K,act", [(2048, 4096, 256, 1), (1000, 4000, 512, 3), (4100, 4104, 64, 0), (513, 4104, 128, 2)])
@@ -231,7 +231,7 @@ def test_f16_short_k_pair_eight_epilogue_warps(M, N, K, act):
     assert "pair" in plan and plan.endswith("epi8"), plan
     rows = sample_rows(M, seed=49)
     ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=0.75, beta=-0.5, bias=d["bias"], act=act, rows=rows)
-    assert_within(got[rows], ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]")
+    assert_within(got[rows], ref, S, TOL_F16, f"{M}x{N}x{K} [{plan}]", bias=d["bias"])
 
 
 def test_f16_short_k_pair_exact():

@@ -79,7 +79,7 @@ def test_fuzz_tensor_core(case):
                              bias=d.get("bias"), act=act, rows=rows)
         sel = got[z] if rows is None else got[z][rows]
         assert_within(sel, ref, S, TOL_F16,
-                      f"case {case}: {batch}x{M}x{N}x{K} {in_kind}->{out} trans={b_trans} act={act} [{plan}]", out=out)
+                      f"case {case}: {batch}x{M}x{N}x{K} {in_kind}->{out} trans={b_trans} act={act} [{plan}]", out=out, bias=d.get("bias"))
 
 
 @pytest.mark.parametrize("case", range(12))

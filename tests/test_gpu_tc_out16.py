@@ -52,7 +52,7 @@ def test_out16_parity(in_kind, out, M, N, K):
     rows = sample_rows(M, seed=19) if M > 512 else None
     ref, S = oracle.gemm(d["A"], d["B"], C0, alpha=0.75, beta=0.5, bias=d["bias"], act=act, rows=rows)
     sel = got if rows is None else got[rows]
-    assert_within(sel, ref, S, TOL_F16, f"{in_kind}->{out} {M}x{N}x{K} act={act} [{plan}]", out=out)
+    assert_within(sel, ref, S, TOL_F16, f"{in_kind}->{out} {M}x{N}x{K} act={act} [{plan}]", out=out, bias=d["bias"])
 
 
 @pytest.mark.parametrize("out", ["f16", "bf16"])
@@ -91,7 +91,7 @@ def test_out16_alpha_zero_epilogue_only(out, act):
     torch.cuda.synchronize()
     assert g.last_plan() == "scale_c_batched"
     ref, S = oracle.gemm(np.zeros((33, 16)), np.zeros((16, 24)), C0, alpha=0.0, beta=-1.5, bias=bias, act=act)
-    assert_within(C.float().cpu().numpy(), ref, S, 1e-6, f"alpha=0 {out} act={act}", out=out)
+    assert_within(C.float().cpu().numpy(), ref, S, 1e-6, f"alpha=0 {out} act={act}", out=out, bias=bias)
 
 
 def test_out16_beta_zero_does_not_read_c():
@@ -131,7 +131,7 @@ def test_out16_pair_64_column_stores(out, M, N, K):
     assert plan.startswith("tc_pair_256x256") or plan.startswith("tc_pair_256x192"), plan
     rows = sample_rows(M, seed=51)
     ref, S = oracle.gemm(d["A"], d["B"], C0, alpha=1.25, beta=0.5, bias=d["bias"], act=3, rows=rows)
-    assert_within(got[rows], ref, S, TOL_F16, f"{out} {M}x{N}x{K} [{plan}]", out=out)
+    assert_within(got[rows], ref, S, TOL_F16, f"{out} {M}x{N}x{K} [{plan}]", out=out, bias=d["bias"])
 
 
 @pytest.mark.parametrize("out", ["f16", "bf16"])

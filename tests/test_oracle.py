@@ -21,10 +21,13 @@ import oracle
 
 
 def _exact(A, B, C0, alpha, beta, bias, K, N):
-    """Exact rational evaluation of alpha*A@B + beta*C0 + bias and of S."""
+    """Exact rational evaluation of alpha*A@B + beta*C0 + bias, of the error
+    scale S = |alpha| sum|a||b| + |beta||c| (the bias is not part of it) and of
+    the magnitude S + |bias| that bounds the double rounding of the value."""
     M = A.shape[0]
     out = [[None] * N for _ in range(M)]
     sc = [[None] * N for _ in range(M)]
+    mag = [[None] * N for _ in range(M)]
     fa, fb = Fraction(float(alpha)), Fraction(float(beta))
     for i in range(M):
         for j in range(N):
@@ -40,12 +43,14 @@ def _exact(A, B, C0, alpha, beta, bias, K, N):
                 c = Fraction(float(C0[i, j]))
                 v += fb * c
                 e += abs(fb) * abs(c)
+            m = e
             if bias is not None:
                 v += Fraction(float(bias[j]))
-                e += abs(Fraction(float(bias[j])))
+                m += abs(Fraction(float(bias[j])))
             out[i][j] = v
             sc[i][j] = e
-    return out, sc
+            mag[i][j] = m
+    return out, sc, mag
 
 
 TINY = [(1, 1, 1), (1, 5, 3), (3, 1, 7), (2, 3, 5), (7, 5, 3), (5, 7, 2), (8, 8, 8), (3, 11, 13)]
@@ -62,12 +67,12 @@ def test_bruteforce_fraction(shape, with_bias):
     bias = rng.normal(0, 0.1, N).astype(np.float32) if with_bias else None
     alpha, beta = 0.7, -1.3
     out, S = oracle.gemm(A, B, C0, alpha=alpha, beta=beta, bias=bias)
-    ex, exS = _exact(A, B, C0, alpha, beta, bias, K, N)
+    ex, exS, mag = _exact(A, B, C0, alpha, beta, bias, K, N)
     eps = np.finfo(np.float64).eps
     for i in range(M):
         for j in range(N):
             ref = ex[i][j]
-            bound = (K + 4) * eps * float(exS[i][j]) + 1e-300
+            bound = (K + 4) * eps * float(mag[i][j]) + 1e-300
             assert abs(Fraction(out[i, j]) - ref) <= Fraction(bound), (i, j)
             assert abs(S[i, j] - float(exS[i][j])) <= (K + 4) * eps * float(exS[i][j])
 
@@ -81,7 +86,7 @@ def test_bruteforce_with_leading_dims():
     B = rng.uniform(-1, 1, (K, ldb)).astype(np.float32)
     C0 = rng.uniform(-1, 1, (M, ldc)).astype(np.float32)
     out, _ = oracle.gemm(A, B, C0, alpha=1.5, beta=0.5, K=K, N=N)
-    ex, exS = _exact(A[:, :K], B[:, :N], C0[:, :N], 1.5, 0.5, None, K, N)
+    ex, exS, _ = _exact(A[:, :K], B[:, :N], C0[:, :N], 1.5, 0.5, None, K, N)
     eps = np.finfo(np.float64).eps
     for i in range(M):
         for j in range(N):
@@ -242,6 +247,33 @@ def test_relu_and_tanh_gelu():
     out, _ = oracle.gemm(np.zeros((1, 2), np.float32), np.zeros((2, 3), np.float32),
                          bias=np.array([-1.0, 0.0, 2.0], np.float32), act=2)
     np.testing.assert_array_equal(out, [[0.0, 0.0, 2.0]])
+
+
+def test_tanh_gelu_matches_an_independent_implementation():
+    """The tanh form of GELU against PyTorch's own CPU implementation in double
+    (a test-only library cross-check; nothing in the product calls it).  Its
+    coefficients (sqrt(2/pi) and 0.044715, Hendrycks and Gimpel) decide the
+    value at every |x| of order one, so a slip in either fails here."""
+    torch = pytest.importorskip("torch")
+    xs = [-6.0, -3.0, -1.5, -0.5, 0.25, 1.0, 2.5, 6.0]
+    ref = torch.nn.functional.gelu(torch.tensor(xs, dtype=torch.float64), approximate="tanh").tolist()
+    for x, r in zip(xs, ref):
+        assert abs(oracle.act(3, x) - r) <= 1e-15 * max(1.0, abs(x)), x
+
+
+def test_tanh_gelu_quartic_series_coefficient():
+    """Near 0, 0.5 x (1 + tanh(c (x + a x^3))) = x/2 + (c/2) x^2 + (c a / 2 - c^3 / 6) x^4 + O(x^6)
+    (tanh t = t - t^3/3 + ...), with c = sqrt(2/pi) and the cubic coefficient
+    a = 0.044715 of Hendrycks and Gimpel: the x^4 term is the only place a
+    enters at this order, so it pins a independently of any other evaluation.
+    At x = 2^-8 the O(x^6) remainder is 2.3e-6 of that term; a = 0.0447
+    instead of 0.044715 moves it by 9e-5."""
+    import math
+    c = math.sqrt(2.0 / math.pi)
+    x = 2.0 ** -8
+    quartic = (oracle.act(3, x) - x / 2 - c * x * x / 2) / x ** 4
+    want = c * 0.044715 / 2 - c ** 3 / 6
+    assert abs(quartic / want - 1.0) < 2e-5
 
 
 def test_round_to_f16_matches_numpy_binary16():
