@@ -408,6 +408,7 @@ int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const voi
                                      float *C, const float *bias, int act, void *stream) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (!valid_act(act)) return GEMM_ERR_INVALID_ARG;
+    if (M > 64) return GEMM_ERR_UNSUPPORTED;  // whatever alpha, K or N: this entry point is for M <= 64
     if (M == 0 || N == 0) {
         t_last_plan = "noop_empty";
         t_last_launches = 0;
@@ -420,7 +421,7 @@ int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const voi
         const bool ok = (K % 8 == 0) && (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) &&
                         ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) &&
                         ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
-        if (!ok || M > 64) return GEMM_ERR_UNSUPPORTED;
+        if (!ok) return GEMM_ERR_UNSUPPORTED;
     }
     DeviceState *ds = device_state();
     if (!ds) return fail_cuda(cudaErrorInvalidDevice);
@@ -496,6 +497,25 @@ int gemm_watchdog_selftest(int wait_ms, void *stream) {
     const cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return fail_cuda(e);
     t_last_plan = "watchdog_probe";
+    t_last_launches = 1;
+    return GEMM_OK;
+}
+
+int gemm_pipeline_stall_selftest(int M, int N, int K, const void *A, const void *B, float *C, int wait_ms,
+                                 void *stream) {
+    if (wait_ms < 1 || wait_ms > 2000) return GEMM_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || !A || !B || !C) return GEMM_ERR_INVALID_ARG;
+    const bool ok = (K % 8 == 0) && (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+    if (!ok) return GEMM_ERR_UNSUPPORTED;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    const cudaError_t e = run_hgemm_stall_selftest(M, N, K, A, B, C, static_cast<unsigned long long>(wait_ms) * 1000000ull,
+                                                   static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_plan = "tc_128x128_stalled_producer";
     t_last_launches = 1;
     return GEMM_OK;
 }

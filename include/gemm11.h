@@ -210,15 +210,22 @@ GEMM11_API int gemm_tc_strided_batched(int batch, int M, int N, int K, float alp
  * caller's other streams).
  *   Scratch: the split-K partial tiles of the small-M plan live in one
  *   file-scope device array of this library (4 MiB of fp32 partials plus
- *   4096 arrival counters, 4 MiB + 16 KiB); every GPU that loads the library
- *   holds it until the process exits.  A shape whose split-K plan needs more
- *   than that returns GEMM_ERR_SCRATCH_LIMIT without launching anything;
- *   M > 64 or the alignment rules of gemm_f16_f32acc_epilogue return
- *   GEMM_ERR_UNSUPPORTED.
- *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.  Every call zeroes the counters it uses (an async memset
- *   on `stream`) before its kernel.
+ *   4096 arrival counters, 4 MiB + 16 KiB); every GPU on which the library's
+ *   kernels have been loaded holds it until the process exits.  The K split
+ *   count is lowered until the partials fit in the array; a shape for which
+ *   not even two splits fit (on a 152-SM GPU only 33 <= M <= 64 with
+ *   8193 <= N <= 9728 and K >= 256) returns GEMM_ERR_SCRATCH_LIMIT without launching anything.
+ *   M > 64 (in every case, also with alpha == 0, K == 0 or N == 0) and the
+ *   alignment rules of gemm_f16_f32acc_epilogue return GEMM_ERR_UNSUPPORTED.
+ *   When the array reaches the GPU: under CUDA's default lazy module loading
+ *   the driver places the library's kernels -- and this array with them --
+ *   on a device when they are first used, which may be this entry point's
+ *   first call.  A caller that reserves a fixed memory budget should make one
+ *   warm-up call (or set CUDA_MODULE_LOADING=EAGER) before reserving it.
+ *   The first call on a device also looks up the array's device address
+ *   (with that device current; a failed lookup is retried on the next call);
+ *   make that first call before any stream capture.  Every call zeroes the
+ *   counters it uses (an async memset on `stream`) before its kernel.
  *   All calls share the one array: calls whose execution overlaps on the GPU
  *   (for example on two streams at once) race on it and give wrong results.
  *   Serialise them, e.g. by issuing them on one stream.
@@ -301,6 +308,28 @@ GEMM11_API int gemm_check(void *stream);
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG or GEMM_ERR_CUDA.
  */
 GEMM11_API int gemm_watchdog_selftest(int wait_ms, void *stream);
+
+/*
+ * gemm_pipeline_stall_selftest -- diagnostic: the timeout path of a real GEMM
+ * pipeline.  Enqueues on `stream` the single-CTA tensor-core plan of
+ * gemm_f16_f32acc_epilogue (128 x 128 tiles, no K split) for C = A x B, with
+ * its TMA producer switched off -- it issues no load and makes no arrival --
+ * and every bounded wait of the kernel limited to wait_ms milliseconds
+ * (1..2000) instead of the usual 2 s.  The MMA thread's wait for the first
+ * operand stage and the epilogue warps' wait for the accumulator run out;
+ * the kernel records the timeout in the device watchdog word, frees its
+ * tensor memory and returns without writing C (nothing is in flight: no copy
+ * was issued), so the next gemm_check(stream) returns GEMM_ERR_TIMEOUT and
+ * the context stays usable.  The DeepGEMM essay "企业官网建设流程全解析"
+ * (section 6.1) describes the asynchronous-pipeline hazards this guards.
+ *   A, B, C, M, N, K: as for gemm_f16_f32acc_epilogue (FP16 A and B, FP32 C,
+ *   M, N, K >= 1, K % 8 == 0, N % 8 == 0, 16-byte aligned pointers); A and B
+ *   are not read.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (wait_ms out of range, a size < 1, a
+ * NULL pointer), GEMM_ERR_UNSUPPORTED (alignment) or GEMM_ERR_CUDA.
+ */
+GEMM11_API int gemm_pipeline_stall_selftest(int M, int N, int K, const void *A, const void *B, float *C, int wait_ms,
+                                            void *stream);
 
 /*
  * gemm_tc_rate_probe -- diagnostic: the tensor core's dense FP16/BF16 rate

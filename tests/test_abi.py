@@ -76,6 +76,18 @@ def test_16bit_rejects_bad_args(L, raw):
     assert f(0, 8, 8, 1.0, 0, 0, 0.0, 0, act=3) == g.GEMM_OK
 
 
+def test_noalloc_rejects_m_above_64_in_every_case(L):
+    """The no-allocation entry point takes M <= 64 only, whatever else the call
+    asks for: also with alpha == 0, K == 0 or N == 0, where no product is
+    formed.  The check comes before any CUDA call."""
+    f = g.gemm_f16_noalloc_raw
+    assert f(65, 8, 8, 1.0, FAKE, FAKE, 0.0, FAKE) == g.GEMM_ERR_UNSUPPORTED
+    assert f(65, 8, 8, 0.0, FAKE, FAKE, 1.0, FAKE) == g.GEMM_ERR_UNSUPPORTED   # alpha == 0
+    assert f(65, 8, 0, 1.0, 0, 0, 1.0, FAKE) == g.GEMM_ERR_UNSUPPORTED         # K == 0
+    assert f(65, 0, 8, 1.0, 0, 0, 0.0, 0) == g.GEMM_ERR_UNSUPPORTED            # N == 0
+    assert f(64, 0, 8, 1.0, 0, 0, 0.0, 0) == g.GEMM_OK                         # M <= 64, empty: no-op
+
+
 def test_tc_rejects_bad_types(L):
     for ab in (-1, 0, 3):   # F32 operands are not a tensor-core input type here
         assert g.gemm_tc_raw(8, 8, 8, 1.0, FAKE, FAKE, ab, 0.0, FAKE, 0) == g.GEMM_ERR_INVALID_ARG
