@@ -53,7 +53,8 @@ EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_f16_f32acc_epilogue", "
                     "gemm_tc_f32acc_epilogue", "gemm_tc_strided_batched", "gemm_f16_f32acc_epilogue_noalloc",
                     "gemm_tune_set", "gemm_tune_get",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
-                    "gemm_last_plan", "gemm_last_launch_count", "gemm_tc_rate_probe")
+                    "gemm_last_plan", "gemm_last_launch_count", "gemm_tc_rate_probe",
+                    "gemm_pipeline_stall_selftest")
 
 _lock = threading.Lock()
 _lib = None
@@ -113,6 +114,9 @@ def lib():
             L.gemm_last_plan.argtypes = []
             L.gemm_last_launch_count.restype = c_int
             L.gemm_last_launch_count.argtypes = []
+            L.gemm_pipeline_stall_selftest.restype = c_int
+            L.gemm_pipeline_stall_selftest.argtypes = [c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int,
+                                                       c_void_p]
             L.gemm_tc_rate_probe.restype = c_int
             L.gemm_tc_rate_probe.argtypes = [c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
             _lib = L
@@ -399,6 +403,14 @@ def load_tuning(path: str) -> int:
 def watchdog_selftest(wait_ms: int = 20, stream=None) -> int:
     """Enqueue the watchdog probe (a wait that must time out after wait_ms); returns the status."""
     return int(lib().gemm_watchdog_selftest(int(wait_ms), _stream_handle(stream)))
+
+
+def pipeline_stall_selftest_raw(M, N, K, A_ptr, B_ptr, C_ptr, wait_ms=5, stream_ptr=0) -> int:
+    """Enqueue the single-CTA tensor-core GEMM with its TMA producer switched off
+    and every wait limited to wait_ms (the waits must run out); returns the status."""
+    return int(lib().gemm_pipeline_stall_selftest(int(M), int(N), int(K), ctypes.c_void_p(A_ptr),
+                                                  ctypes.c_void_p(B_ptr), ctypes.c_void_p(C_ptr), int(wait_ms),
+                                                  ctypes.c_void_p(stream_ptr)))
 
 
 def tc_rate_probe(iters: int = 4096, stream=None) -> float:

@@ -77,6 +77,11 @@ struct HgemmArgs {
     long long stride_c;
     int b_kmajor;  // 1: B is stored N x K (the product uses its transpose), 0: K x N
     int c64;       // 16-bit C stored in 32 x 64 boxes (128-byte rows; pair kernel, tile width % 64 == 0)
+    // Single-CTA kernel only: the limit of each of its bounded waits, and a
+    // diagnostic switch under which the TMA producer issues nothing at all (no
+    // load, no arrival), so that the MMA and epilogue waits must run out.
+    unsigned long long wait_ns = kWaitLimitNs;
+    int stall_producer = 0;
 };
 
 __host__ __device__ constexpr int tmem_cols_for(int bn) {
@@ -557,11 +562,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         // ------------------------------------------------ TMA producer
         int stage = 0;
         uint32_t phase = 0;
-        for (int idx = 0; !*abort_flag; ++idx) {
+        for (int idx = 0; !*abort_flag && !p.stall_producer; ++idx) {
             UnitCoord c;
             if ((Cfg::kPartInRing && idx > 0) || !next_unit(p, idx, kBnTile, SWAP, c)) break;
             for (int kb = c.kb0; kb < c.kb1; ++kb) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
                     flag_timeout(abort_flag, p.err);
                     break;
                 }
@@ -618,7 +623,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             if ((Cfg::kPartInRing && idx > 0) || !next_unit(p, idx, kBnTile, SWAP, c)) break;
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
-            if (!mbar_wait(&tempty[buf], acc_phase ^ 1u)) {
+            if (!mbar_wait(&tempty[buf], acc_phase ^ 1u, p.wait_ns)) {
                 flag_timeout(abort_flag, p.err);
                 break;
             }
@@ -626,7 +631,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
             bool ok = true;
             for (int kb = c.kb0; kb < c.kb1; ++kb) {
-                if (!mbar_wait(&full[stage], phase)) {
+                if (!mbar_wait(&full[stage], phase, p.wait_ns)) {
                     flag_timeout(abort_flag, p.err);
                     ok = false;
                     break;
@@ -689,7 +694,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             } else {
                 load_bias_lanes(p, c.n0, lane, [&](int i) { return ch_first + i * ch_step; }, blane);
             }
-            if (!mbar_wait(&tfull[buf], acc_phase)) {
+            if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns)) {
                 flag_timeout(abort_flag, p.err);
                 break;
             }
@@ -734,7 +739,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 const int nsp = p.splits;
                 if (lane < nsp) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), lane));
-                if (!mbar_wait_cluster(part_ready, 0)) {
+                if (!mbar_wait_cluster(part_ready, 0, p.wait_ns)) {
                     flag_timeout(abort_flag, p.err);
                     break;
                 }
@@ -755,7 +760,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             if constexpr (CSPLIT) {
                 // 1. this CTA's partial -> own shared memory, [column][row]
                 float *part = reinterpret_cast<float *>(sC);
-                if (local > 0 && !mbar_wait_cluster(part_consumed, (local - 1) & 1)) {
+                if (local > 0 && !mbar_wait_cluster(part_consumed, (local - 1) & 1, p.wait_ns)) {
                     flag_timeout(abort_flag, p.err);
                     break;
                 }
@@ -773,7 +778,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 const int nsp = p.splits;
                 if (lane < nsp) mbar_arrive_cluster(mapa_shared(smem_u32(part_ready), lane));
                 // 2. rows [rank * R, rank * R + R) of the sum of all partials, in split order
-                if (!mbar_wait_cluster(part_ready, local & 1)) {
+                if (!mbar_wait_cluster(part_ready, local & 1, p.wait_ns)) {
                     flag_timeout(abort_flag, p.err);
                     break;
                 }
@@ -911,7 +916,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         }
         if (CSPLIT && local > 0 && !*abort_flag) {
             // the peers must have read this CTA's last partial before it exits
-            if (!mbar_wait_cluster(part_consumed, (local - 1) & 1)) flag_timeout(abort_flag, p.err);
+            if (!mbar_wait_cluster(part_consumed, (local - 1) & 1, p.wait_ns)) flag_timeout(abort_flag, p.err);
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -922,11 +927,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         // every TMA copy this CTA issued must have landed before it exits
         for (int s = 0; s < STAGES; ++s)
             if (armed & (1u << s))
-                if (!mbar_wait(&full[s], (armed_parity >> s) & 1u)) flag_timeout(abort_flag, p.err);
+                if (!mbar_wait(&full[s], (armed_parity >> s) & 1u, p.wait_ns)) flag_timeout(abort_flag, p.err);
     }
     if (warp == 1 && lane == 0) {
         umma_commit(mma_done);  // completes when all MMAs issued above have finished
-        if (!mbar_wait(mma_done, 0)) flag_timeout(abort_flag, p.err);
+        if (!mbar_wait(mma_done, 0, p.wait_ns)) flag_timeout(abort_flag, p.err);
     }
     tc_fence_before();
     __syncthreads();
@@ -1956,9 +1961,8 @@ constexpr size_t kNoAllocBytes = kNoAllocCounters * sizeof(unsigned) + kNoAllocP
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 struct NoAllocSlot {
-    std::once_flag once;
-    unsigned char *base = nullptr;  // device address of g_noalloc_scratch on that device
-    cudaError_t err = cudaSuccess;
+    std::mutex mu;
+    unsigned char *base = nullptr;  // device address of g_noalloc_scratch; set only once a lookup succeeded
 };
 NoAllocSlot g_noalloc_slot[64];
 
@@ -1977,14 +1981,22 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     // Set-up, once per device, with that device current: host code cannot use
-    // the array's name as a device address, so look the address up.
+    // the array's name as a device address, so look the address up.  A failed
+    // lookup is not remembered; the next call on the device tries again.
     NoAllocSlot &slot = g_noalloc_slot[dev];
-    std::call_once(slot.once, [&slot] {
-        slot.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&slot.base), g_noalloc_scratch);
-    });
-    if (slot.err != cudaSuccess) return slot.err;
-    unsigned *counters = reinterpret_cast<unsigned *>(slot.base);
-    float *partials = reinterpret_cast<float *>(slot.base + kNoAllocCounters * sizeof(unsigned));
+    unsigned char *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(slot.mu);
+        if (!slot.base) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            slot.base = static_cast<unsigned char *>(p);
+        }
+        base = slot.base;
+    }
+    unsigned *counters = reinterpret_cast<unsigned *>(base);
+    float *partials = reinterpret_cast<float *>(base + kNoAllocCounters * sizeof(unsigned));
 
     const int sms = device_sm_count();
     HgemmArgs a{};
@@ -2009,15 +2021,20 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
     int splits = 1;
     if (tiles < sms) splits = std::max(1, std::min(sms / tiles, a.kb_total / 2));
     splits = std::min(splits, 32);
-    a.splits = splits;
-    a.units = tiles * splits;
     if (splits > 1) {
-        const size_t need_floats = static_cast<size_t>(tiles) * splits * kBM * bn;
-        const size_t need_counters = static_cast<size_t>(tiles) * 4;
-        if (need_floats > kNoAllocPartialFloats || need_counters > kNoAllocCounters) {
+        // As many K splits as the fixed array holds, up to the planner's count;
+        // a plan that cannot keep even two splits' partials there is rejected.
+        const size_t per_split = static_cast<size_t>(tiles) * kBM * bn;
+        splits = static_cast<int>(std::min<size_t>(splits, kNoAllocPartialFloats / per_split));
+        if (splits < 2 || static_cast<size_t>(tiles) * 4 > kNoAllocCounters) {
             *reject = 2;
             return cudaSuccess;
         }
+    }
+    a.splits = splits;
+    a.units = tiles * splits;
+    if (splits > 1) {
+        const size_t need_counters = static_cast<size_t>(tiles) * 4;
         // The array keeps the previous call's contents: the counters must start at zero.
         e = cudaMemsetAsync(counters, 0, need_counters * sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;
@@ -2043,6 +2060,50 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
     }
     info->launches = splits > 1 ? 2 : 1;  // counter clear + GEMM
     return e;
+}
+
+// ------------------------------------------------------------------ stalled-pipeline self-test
+// The single-CTA plan (128 x 128 tiles, no K split, FP16 operands, FP32 C)
+// with its producer switched off: no TMA load is issued and no arrival made,
+// so nothing is in flight when the MMA thread's wait for the first stage and
+// the epilogue's wait for the accumulator give up after wait_ns.  They record
+// the timeout in the watchdog word and leave their loops; the CTA frees its
+// tensor memory and returns.  C is not written.
+cudaError_t run_hgemm_stall_selftest(int M, int N, int K, const void *A, const void *B, float *C,
+                                     unsigned long long wait_ns, cudaStream_t stream) {
+    HgemmArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.alpha = 1.f;
+    a.C = C;
+    a.ldc = N;
+    a.c_type = kOutF32;
+    a.kb_total = (K + kBK - 1) / kBK;
+    a.err = watchdog_word();
+    a.batch = 1;
+    a.stride_c = static_cast<long long>(M) * N;
+    a.tiles_m = (M + kBM - 1) / kBM;
+    a.tiles_n = (N + 127) / 128;
+    if (static_cast<long long>(a.tiles_m) * a.tiles_n > (1LL << 26)) return cudaErrorNotSupported;
+    a.splits = 1;
+    a.units = a.tiles_m * a.tiles_n;
+    a.wait_ns = wait_ns;
+    a.stall_producer = 1;
+    TcGemm g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.A = A;
+    g.B = B;
+    g.C = C;
+    g.stride_c = a.stride_c;
+    g.c_type = kOutF32;
+    CUtensorMap ta, tb, tc;
+    if (!encode_a(&ta, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kBM) || !encode_b(&tb, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 128) ||
+        !encode_c(&tc, g, N))
+        return cudaErrorNotSupported;
+    return launch_hgemm<128, 6, false>(ta, tb, tc, a, std::min(a.units, device_sm_count()), stream);
 }
 
 }  // namespace gemm11

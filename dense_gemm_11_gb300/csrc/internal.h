@@ -119,6 +119,13 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
                                          float *C, const float *bias, int act, cudaStream_t stream, CallInfo *info,
                                          int *reject);
 
+// Diagnostic: the single-CTA tensor-core plan for C = A x B (FP16, 128 x 128
+// tiles, no K split) with its TMA producer issuing nothing and every bounded
+// wait of the kernel limited to wait_ns: the waits run out, the kernel
+// records a timeout in the watchdog word and returns without writing C.
+cudaError_t run_hgemm_stall_selftest(int M, int N, int K, const void *A, const void *B, float *C,
+                                     unsigned long long wait_ns, cudaStream_t stream);
+
 // C = beta * C over an M x N window (alpha == 0 or K == 0), with the epilogue
 // bias/act applied when given (the FP16 path), in sgemm.cu.
 cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float *bias, int act,
