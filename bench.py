@@ -35,6 +35,14 @@ WORKLOAD = ("square 4096^3 x2 per step: FP32 SGEMM (alpha 1, beta 3, C reset to 
             "run, A/B U[-1,1]) then FP16-in/FP32-acc GEMM (alpha 1, beta 0, A/B N(0,1/sqrt(K)) in fp16)")
 
 
+L2_NOTE = "flushed (256 MB write) before every GEMM, outside the timed intervals"
+
+
+def bench_config(world: int) -> dict:
+    """The workload description both arms print (identical dicts)."""
+    return {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE, "l2": L2_NOTE, "parallelism": f"replicas x{world}"}
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -109,56 +117,86 @@ def replica_throughput(flops_per_rank_step: float, world: int, ms_per_step_max: 
     return world * flops_per_rank_step / (ms_per_step_max * 1e-3) / 1e12
 
 
-def cpu_oracle_sample(target_s: float = 12.0):
-    """Time the oracle (as it stands) on rows of both 4096^3 GEMMs; about target_s seconds."""
-    import numpy as np
-
+def _oracle_inputs():
     import oracle
     from dense_gemm_11_gb300 import inputs
-    threads = oracle.default_threads()
     w32, w16 = inputs.WORKLOADS["f32_sq4096"], inputs.WORKLOADS["f16_4096"]
-    d32, d16 = inputs.make_workload(w32), inputs.make_workload(w16)
-    # calibrate on a warm sample of rows, then size the sample to the target time
+    return oracle, inputs.make_workload(w32), inputs.make_workload(w16)
+
+
+def _oracle_rows_for(seconds: float, oracle, d32, threads: int) -> int:
+    """Rows of each 4096^3 GEMM (both together) that the oracle evaluates in
+    about `seconds` on `threads` host threads (a multiple of threads, 1..4096)."""
+    import numpy as np
     rows = np.arange(4 * threads, dtype=np.int64)
-    oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows[:threads], threads=threads)
+    oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows[:threads], threads=threads)  # warm
     t0 = time.perf_counter()
     oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows, threads=threads)
     per_row = (time.perf_counter() - t0) / len(rows)
-    n = int(max(threads, min(SIZE, target_s / 2 / max(per_row, 1e-6))))
-    n = max(threads, (n // threads) * threads)
-    rows = np.linspace(0, SIZE - 1, n).astype(np.int64)
+    n = int(min(SIZE, seconds / 2 / max(per_row, 1e-6)))
+    return min(SIZE, max(threads, (n // threads) * threads))
+
+
+def _oracle_step(oracle, d32, d16, rows, threads):
+    """One step of the bench workload on the listed output rows of both GEMMs;
+    returns (seconds, fp32 seconds, fp16 seconds)."""
     t0 = time.perf_counter()
     oracle.gemm(d32["A"], d32["B"], d32["C"], alpha=1.0, beta=3.0, rows=rows, threads=threads)
     t1 = time.perf_counter()
     oracle.gemm(d16["A"], d16["B"], None, alpha=1.0, beta=0.0, rows=rows, threads=threads)
     t2 = time.perf_counter()
+    return t2 - t0, t1 - t0, t2 - t1
+
+
+def cpu_oracle_sample(target_s: float = 12.0):
+    """Time the oracle (as it stands) on rows of both 4096^3 GEMMs; about target_s seconds."""
+    import numpy as np
+    oracle, d32, d16 = _oracle_inputs()
+    threads = oracle.default_threads()
+    n = _oracle_rows_for(target_s, oracle, d32, threads)
+    rows = np.linspace(0, SIZE - 1, n).astype(np.int64)
+    secs, s32, s16 = _oracle_step(oracle, d32, d16, rows, threads)
     flops = 2 * (2 * n * SIZE * SIZE)
-    secs = t2 - t0
     return {
         "value": flops / secs / 1e12,
         "unit": "TFLOPS",
         "cores": threads,
         "kind": "oracle",
         "sample": f"{n} of 4096 output rows of each 4096^3 GEMM (fp32 and fp16-in), fp64 accumulation; "
-                  f"{secs:.1f} s on {threads} host threads ({t1 - t0:.1f} s fp32 + {t2 - t1:.1f} s fp16)",
+                  f"{secs:.1f} s on {threads} host threads ({s32:.1f} s fp32 + {s16:.1f} s fp16)",
     }
 
 
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm, on bounded row samples."""
+    """The CPU oracle as the reference arm.  Every step (warm-up and timed)
+    evaluates the same bounded sample of the workload -- n output rows of
+    each 4096^3 GEMM, n sized so that all warm-up and timed steps take about
+    --ref-budget-s seconds (100) -- and ms_per_step is the measured wall time
+    of those steps."""
     if rank != 0:
         return
-    samples = []
-    for _ in range(max(1, args.steps)):
-        samples.append(cpu_oracle_sample(target_s=8.0))
-    value = statistics.mean(s["value"] for s in samples)
-    ms = FLOPS_STEP / (value * 1e12) * 1e3
+    import numpy as np
+    oracle, d32, d16 = _oracle_inputs()
+    threads = oracle.default_threads()
+    n = _oracle_rows_for(args.ref_budget_s / (args.steps + args.warmup), oracle, d32, threads)
+    rows = np.linspace(0, SIZE - 1, n).astype(np.int64)
+    for _ in range(args.warmup):
+        _oracle_step(oracle, d32, d16, rows, threads)
+    secs = [_oracle_step(oracle, d32, d16, rows, threads)[0] for _ in range(args.steps)]
+    ms = statistics.mean(secs) * 1e3
+    flops_step = 2 * (2 * n * SIZE * SIZE)
+    value = flops_step / (ms * 1e-3) / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median":
+        statistics.median(secs) * 1e3, "ms_per_step_min": min(secs) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE},
-        "cpu_baseline": {**samples[-1], "value": value},
+        "config": bench_config(args.gpus),
+        "step_sample": f"each step evaluates {n} of the 4096 output rows of both GEMMs "
+                       f"({flops_step / 1e9:.1f} of {FLOPS_STEP / 1e9:.1f} GFLOP)",
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of 4096 output rows of each 4096^3 GEMM (fp32 and fp16-in) per step, "
+                                   f"fp64 accumulation, {threads} host threads; {args.steps} timed steps"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -246,14 +284,18 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"watchdog: {g.status_string(st)}")
     t32 = [e[0].elapsed_time(e[1]) for e in events]
     t16 = [e[2].elapsed_time(e[3]) for e in events]
-    ms_step = statistics.mean(a + b for a, b in zip(t32, t16))
+    t_step = [a + b for a, b in zip(t32, t16)]
+    ms_step = statistics.mean(t_step)
     gpu_launches = launches[0]
 
     # e2e through the public API: every step copies its inputs from pinned host
     # memory to the device, runs both GEMMs and reads both results back to
-    # pinned host memory.  Steps are pipelined over two device buffer sets and
-    # three streams (inputs of step i+1 travel while step i computes; results
-    # of step i travel back while step i+1 computes), as a serving loop would.
+    # pinned host memory.  Steps are pipelined over three device buffer sets
+    # and three streams (inputs of step i+1 travel while step i computes;
+    # results of step i travel back while step i+1 computes), as a serving
+    # loop would.  With three sets the inputs of step i+1 wait only for the
+    # results of step i-2, which left while step i-1 ran, so neither copy
+    # direction is chained to the other.
     hA32 = torch.from_numpy(d32["A"]).pin_memory()
     hB32 = torch.from_numpy(d32["B"]).pin_memory()
     hC32 = torch.from_numpy(d32["C"]).pin_memory()
@@ -263,13 +305,32 @@ def run_ours(args, rank, world, local_rank):
     oC16 = torch.empty(SIZE, SIZE).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hA32, hB32, hC32, hA16, hB16))
     d2h = sum(t.numel() * t.element_size() for t in (oC32, oC16))
-    bufs = [dict(A32=A32, B32=B32, C32=C32, A16=A16, B16=B16, C16=C16),
-            dict(A32=torch.empty_like(A32), B32=torch.empty_like(B32), C32=torch.empty_like(C32),
-                 A16=torch.empty_like(A16), B16=torch.empty_like(B16), C16=torch.empty_like(C16))]
+    NSETS = 3
+    bufs = [dict(A32=A32, B32=B32, C32=C32, A16=A16, B16=B16, C16=C16)] + [
+        dict(A32=torch.empty_like(A32), B32=torch.empty_like(B32), C32=torch.empty_like(C32),
+             A16=torch.empty_like(A16), B16=torch.empty_like(B16), C16=torch.empty_like(C16))
+        for _ in range(NSETS - 1)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(NSETS)]
+    ev_comp = [torch.cuda.Event() for _ in range(NSETS)]
+    ev_out = [torch.cuda.Event() for _ in range(NSETS)]
+
+    def copy_gbs(dst, src, st, reps=5):
+        """Best-of-reps GB/s of one pinned-host <-> device copy on its own stream."""
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            with torch.cuda.stream(st):
+                dst.copy_(src, non_blocking=True)
+            b.record(st)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        return src.numel() * src.element_size() / (best * 1e-3) / 1e9
+
+    h2d_gbs = copy_gbs(bufs[1]["A32"], hA32, s_in)
+    d2h_gbs = copy_gbs(oC32, bufs[1]["A32"], s_out)
 
     def e2e_run(n):
         """n pipelined steps; returns (start, end) events spanning all of them."""
@@ -277,32 +338,32 @@ def run_ours(args, rank, world, local_rank):
         e0.record(s_in)
         stream.wait_event(e0)
         s_out.wait_event(e0)
-        out_pending = [False, False]
+        out_pending = [False] * NSETS
 
         def load(i):
-            b = bufs[i % 2]
-            if out_pending[i % 2]:
-                s_in.wait_event(ev_out[i % 2])  # this set's previous results have left
+            b = bufs[i % NSETS]
+            if out_pending[i % NSETS]:
+                s_in.wait_event(ev_out[i % NSETS])  # this set's previous results have left
             with torch.cuda.stream(s_in):
                 for k, h in (("A32", hA32), ("B32", hB32), ("C32", hC32), ("A16", hA16), ("B16", hB16)):
                     b[k].copy_(h, non_blocking=True)
-            ev_in[i % 2].record(s_in)
+            ev_in[i % NSETS].record(s_in)
 
         load(0)
         for i in range(n):
             if i + 1 < n:
                 load(i + 1)
-            b = bufs[i % 2]
-            stream.wait_event(ev_in[i % 2])
+            b = bufs[i % NSETS]
+            stream.wait_event(ev_in[i % NSETS])
             g.gemm_f32(b["A32"], b["B32"], b["C32"], alpha=1.0, beta=3.0, stream=stream)
             g.gemm_f16_f32acc_epilogue(b["A16"], b["B16"], b["C16"], alpha=1.0, beta=0.0, stream=stream)
-            ev_comp[i % 2].record(stream)
-            s_out.wait_event(ev_comp[i % 2])
+            ev_comp[i % NSETS].record(stream)
+            s_out.wait_event(ev_comp[i % NSETS])
             with torch.cuda.stream(s_out):
                 oC32.copy_(b["C32"], non_blocking=True)
                 oC16.copy_(b["C16"], non_blocking=True)
-            ev_out[i % 2].record(s_out)
-            out_pending[i % 2] = True
+            ev_out[i % NSETS].record(s_out)
+            out_pending[i % NSETS] = True
         s_out.wait_stream(s_in)
         s_out.wait_stream(stream)
         e1.record(s_out)
@@ -316,12 +377,13 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / n_e2e
     # the results that came back are the GEMMs' own (spot check of one step)
     torch.cuda.synchronize(dev)
-    if not (torch.equal(oC16, bufs[(n_e2e - 1) % 2]["C16"].cpu()) and torch.isfinite(oC32[:4]).all()):
+    if not (torch.equal(oC16, bufs[(n_e2e - 1) % NSETS]["C16"].cpu()) and torch.isfinite(oC32[:4]).all()):
         raise RuntimeError("e2e: results read back do not match the device results")
 
     # max over ranks
-    ms_step, e2e_ms, ms32, ms16 = max_over_ranks(
-        [ms_step, e2e_ms, statistics.mean(t32), statistics.mean(t16)], dist, dev)
+    stats = [ms_step, e2e_ms, statistics.mean(t32), statistics.mean(t16), statistics.median(t_step), min(t_step),
+             statistics.median(t32), min(t32), statistics.median(t16), min(t16)]
+    (ms_step, e2e_ms, ms32, ms16, med_step, min_step, med32, min32, med16, min16) = max_over_ranks(stats, dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -342,19 +404,24 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_step,
+        "ms_per_step_median": med_step,
+        "ms_per_step_min": min_step,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "dtypes": {"sgemm": "f32 (FFMA)", "tensor_core": "f16 in, f32 accumulate"},
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
-                   "l2": "flushed (256 MB write) before every GEMM, outside the timed intervals",
-                   "parallelism": f"replicas x{world}", "plans": plans},
+        "config": bench_config(world),
+        "plans": plans,
         "paths": {
-            "sgemm_f32": {"ms": ms32, "tflops": ach32, "frac_of_fp32_peak_at_max_clock": ach32 / f32_peak_max,
+            "sgemm_f32": {"ms": ms32, "ms_median": med32, "ms_min": min32, "tflops": ach32,
+                          "tflops_at_median": FLOPS_ONE / (med32 * 1e-3) / 1e12,
+                          "frac_of_fp32_peak_at_max_clock": ach32 / f32_peak_max,
                           "frac_of_fp32_peak_at_observed_clock": (ach32 / f32_peak_obs) if f32_peak_obs else None},
-            "gemm_f16_f32acc": {"ms": ms16, "tflops": ach16, "frac_of_measured_bf16_peak": ach16 / tc_peak},
+            "gemm_f16_f32acc": {"ms": ms16, "ms_median": med16, "ms_min": min16, "tflops": ach16,
+                                "tflops_at_median": FLOPS_ONE / (med16 * 1e-3) / 1e12,
+                                "frac_of_measured_bf16_peak": ach16 / tc_peak},
         },
         "roofline": {"bound": "alu", "achieved": ach32, "peak": f32_peak_max, "unit": "TFLOP/s",
                      "frac": ach32 / f32_peak_max, "traffic": traffic.get("sgemm"),
@@ -367,8 +434,11 @@ def run_ours(args, rank, world, local_rank):
                             **_nominal_tensor_peak(tc_rate, sms, clocks.get("sm_max_mhz") or 2070.0, ach16)},
         "e2e": {"value": replica_throughput(FLOPS_STEP, world, e2e_ms), "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "pipelining": "two device buffer sets, three streams: inputs of step i+1 and results of "
-                              "step i-1 travel while step i computes"},
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                "copy_bound_ms": max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9)) * 1e3,
+                "copy_streams": "inputs on one stream, results on another, GEMMs on a third",
+                "pipelining": "three device buffer sets: inputs of step i+1 and results of step i-1 travel "
+                              "while step i computes"},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
@@ -583,6 +653,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=100.0,
+                    help="--impl reference: wall-time budget of all its warm-up and timed steps together")
     ap.add_argument("--profile-case", default=None,
                     help="launch one GEMM a few times (for ncu) and exit: sgemm, hgemm or tf32x3 (the 4096^3 "
                          "bench GEMMs) or a workload name of inputs.WORKLOADS")

@@ -22,7 +22,7 @@ def run_bench(*args, env=None):
 
 @pytest.fixture(scope="module")
 def reference_line():
-    lines = run_bench("--impl", "reference", "--steps", "1", "--warmup", "0")
+    lines = run_bench("--impl", "reference", "--steps", "2", "--warmup", "0", "--ref-budget-s", "4")
     assert len(lines) == 1
     return lines[0]
 
@@ -38,6 +38,15 @@ def test_reference_line_has_the_contract_keys(reference_line):
     assert r["warmup"] >= 3  # the timing rules' minimum, applied even when asked for fewer
     assert r["vs_baseline"] is None and r["data"] == "synthetic" and r["scaling"] == "weak"
     assert "workload" in r["config"]
+    assert r["steps"] == 2 and r["ms_per_step_min"] <= r["ms_per_step_median"]
+
+
+def test_both_arms_print_the_same_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    cfg = bench.bench_config(1)
+    assert cfg == json.loads(json.dumps(cfg))  # plain JSON, no plan names or other per-arm keys
+    assert set(cfg) == {"workload", "M", "N", "K", "l2", "parallelism"}
 
 
 def test_reference_line_describes_its_cpu_baseline(reference_line):
@@ -50,7 +59,8 @@ def test_reference_line_describes_its_cpu_baseline(reference_line):
 
 
 def test_reference_arm_prints_on_rank_zero_only():
-    assert run_bench("--impl", "reference", "--steps", "1", env={"RANK": "1", "WORLD_SIZE": "2"}) == []
+    assert run_bench("--impl", "reference", "--steps", "1", "--ref-budget-s", "2",
+                     env={"RANK": "1", "WORLD_SIZE": "2"}) == []
 
 
 @pytest.mark.gpu
