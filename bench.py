@@ -224,6 +224,12 @@ def run_ours(args, rank, world, local_rank):
         tc_rate = g.tc_rate_probe()
     except g.GemmError:
         tc_rate = None
+    # the FP32 FMA units' rate for the packed form gemm_f32 uses and for scalar
+    # FMAs (untimed; see gemm_fma_rate_probe)
+    try:
+        fma_rates = {"packed_ffma2": g.fma_rate_probe(True), "scalar_ffma": g.fma_rate_probe(False)}
+    except g.GemmError:
+        fma_rates = None
 
     w32, w16 = inputs.WORKLOADS["f32_sq4096"], inputs.WORKLOADS["f16_4096"]
     d32, d16 = inputs.make_workload(w32), inputs.make_workload(w16)
@@ -426,7 +432,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "alu", "achieved": ach32, "peak": f32_peak_max, "unit": "TFLOP/s",
                      "frac": ach32 / f32_peak_max, "traffic": traffic.get("sgemm"),
                      "kernel": "sgemm_tiled_kernel (FP32 FFMA)",
-                     "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 x {clocks.get('sm_max_mhz') or 2070.0} MHz"},
+                     "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 x {clocks.get('sm_max_mhz') or 2070.0} MHz",
+                     **_fma_ceiling(fma_rates, ach32, sms, clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0)},
         "roofline_tensor": {"bound": "tensor", "achieved": ach16, "peak": tc_peak, "unit": "TFLOP/s",
                             "frac": ach16 / tc_peak, "traffic": traffic.get("hgemm"),
                             "kernel": f"tcgen05 f16 GEMM, plan {plans.get('gemm_f16')}",
@@ -448,6 +455,17 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def _fma_ceiling(rates, achieved_tflops, sms, mhz):
+    """The SGEMM's FMAs per clock per SM (at the observed clock) against the
+    measured rates of the packed and scalar FMA forms (gemm_fma_rate_probe)."""
+    if not rates:
+        return {"fma_rate_probe": None}
+    per_clk = achieved_tflops * 1e12 / 2 / (sms * mhz * 1e6)
+    return {"fma_rate_probe": {**{k: round(v, 2) for k, v in rates.items()}, "unit": "FMA/clock/SM",
+                               "nominal": 128, "sgemm_fma_per_clock_per_sm": round(per_clk, 2),
+                               "sgemm_frac_of_packed_rate": per_clk / rates["packed_ffma2"]}}
 
 
 def _nominal_tensor_peak(rate, sms, mhz, achieved):

@@ -54,7 +54,7 @@ EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_f16_f32acc_epilogue", "
                     "gemm_tune_set", "gemm_tune_get",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count", "gemm_tc_rate_probe",
-                    "gemm_pipeline_stall_selftest")
+                    "gemm_pipeline_stall_selftest", "gemm_fma_rate_probe")
 
 _lock = threading.Lock()
 _lib = None
@@ -117,6 +117,8 @@ def lib():
             L.gemm_pipeline_stall_selftest.restype = c_int
             L.gemm_pipeline_stall_selftest.argtypes = [c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int,
                                                        c_void_p]
+            L.gemm_fma_rate_probe.restype = c_int
+            L.gemm_fma_rate_probe.argtypes = [c_int, c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
             L.gemm_tc_rate_probe.restype = c_int
             L.gemm_tc_rate_probe.argtypes = [c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
             _lib = L
@@ -411,6 +413,22 @@ def pipeline_stall_selftest_raw(M, N, K, A_ptr, B_ptr, C_ptr, wait_ms=5, stream_
     return int(lib().gemm_pipeline_stall_selftest(int(M), int(N), int(K), ctypes.c_void_p(A_ptr),
                                                   ctypes.c_void_p(B_ptr), ctypes.c_void_p(C_ptr), int(wait_ms),
                                                   ctypes.c_void_p(stream_ptr)))
+
+
+def fma_rate_probe(packed: bool = True, iters: int = 4096, stream=None) -> float:
+    """FP32 FMAs per clock per SM, measured with the packed two-wide FMA form
+    of gemm_f32's outer product (packed=True) or with scalar FMAs."""
+    out = ctypes.c_double(0.0)
+    st = lib().gemm_fma_rate_probe(1 if packed else 0, int(iters), ctypes.byref(out), _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_fma_rate_probe")
+    return float(out.value)
+
+
+def fma_rate_probe_raw(packed, iters, out_ptr, stream_ptr=0) -> int:
+    """Direct C-ABI call of gemm_fma_rate_probe (out_ptr: address of a double, or 0)."""
+    return int(lib().gemm_fma_rate_probe(int(packed), int(iters), ctypes.cast(out_ptr, ctypes.POINTER(ctypes.c_double)),
+                                         ctypes.c_void_p(stream_ptr)))
 
 
 def tc_rate_probe(iters: int = 4096, stream=None) -> float:

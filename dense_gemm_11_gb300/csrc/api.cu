@@ -520,6 +520,20 @@ int gemm_pipeline_stall_selftest(int M, int N, int K, const void *A, const void 
     return GEMM_OK;
 }
 
+int gemm_fma_rate_probe(int packed, int iters, double *fma_per_clock_per_sm, void *stream) {
+    if ((packed != 0 && packed != 1) || iters < 1 || iters > (1 << 20) || !fma_per_clock_per_sm)
+        return GEMM_ERR_INVALID_ARG;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    const cudaError_t e = run_fma_rate_probe(packed != 0, iters, fma_per_clock_per_sm, static_cast<cudaStream_t>(stream));
+    t_last_plan = packed ? "fma2_rate_probe" : "fma_rate_probe";
+    t_last_launches = 1;
+    if (e == cudaErrorLaunchTimeout) return GEMM_ERR_TIMEOUT;
+    if (e != cudaSuccess) return fail_cuda(e);
+    return GEMM_OK;
+}
+
 int gemm_tc_rate_probe(int iters, double *flop_per_clock_per_sm, void *stream) {
     if (iters < 1 || iters > (1 << 20) || !flop_per_clock_per_sm) return GEMM_ERR_INVALID_ARG;
     DeviceState *ds = device_state();

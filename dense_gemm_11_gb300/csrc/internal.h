@@ -141,5 +141,7 @@ cudaError_t run_scale_c_batched(int batch, int M, int N, float beta, void *C, lo
 // timing back-to-back 128 x 256 x 16 MMAs on every SM (probe.cu); synchronous
 // on `stream`.  cudaErrorLaunchTimeout if no SM finished within the bounded wait.
 cudaError_t run_tc_rate_probe(int iters, double *flop_per_clock_per_sm, cudaStream_t stream);
+// FP32 FMAs per clock per SM, packed (__ffma2_rn) or scalar, measured.
+cudaError_t run_fma_rate_probe(bool packed, int iters, double *fma_per_clock_per_sm, cudaStream_t stream);
 
 }  // namespace gemm11

@@ -1,4 +1,6 @@
-// probe.cu -- the tensor core's dense rate per SM, measured.
+// probe.cu -- measured rates per SM: the tensor core's dense FP16/BF16 rate
+// and the FP32 FMA units' rate for the two instruction forms an FP32 GEMM
+// can use (packed FFMA2 and scalar FFMA).
 //
 // The FP16 path's roofline is quoted against two peaks: the measured cuBLAS
 // bf16 throughput and a nominal dense peak, #SM x (FLOP per clock per SM) x
@@ -72,7 +74,94 @@ __global__ void __launch_bounds__(128, 1) tc_rate_probe_kernel(int iters, long l
     }
 }
 
+// FP32 FMA throughput with 8 warps per SM (two per scheduler, the SGEMM's
+// residency), 32 independent two-wide accumulator chains per thread and
+// operands in registers.  PACKED: one packed FMA (__ffma2_rn) per chain and
+// step with the same scalar in both lanes of one operand, the form of the
+// SGEMM's outer product (a_i * (b_j, b_j+1)); otherwise two scalar fmaf.
+// Each CTA times its loop with the SM cycle counter between two barriers.
+constexpr int kFmaProbeThreads = 256, kFmaProbeChains = 32;
+
+template <bool PACKED>
+__global__ void __launch_bounds__(kFmaProbeThreads, 1) fma_rate_probe_kernel(const float *in, int iters,
+                                                                             long long *cycles, float *sink) {
+    float av[4], bv[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) av[j] = in[j];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bv[j] = in[4 + j];
+    float2 acc[kFmaProbeChains];
+#pragma unroll
+    for (int c = 0; c < kFmaProbeChains; ++c) acc[c] = make_float2(0.f, 0.f);
+    __syncthreads();
+    const long long t0 = clock64();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int c = 0; c < kFmaProbeChains; ++c) {
+            const float a = av[c & 3];
+            const float2 b = make_float2(bv[(2 * c) & 15], bv[(2 * c + 1) & 15]);
+            if (PACKED) {
+                acc[c] = __ffma2_rn(make_float2(a, a), b, acc[c]);
+            } else {
+                acc[c].x = fmaf(a, b.x, acc[c].x);
+                acc[c].y = fmaf(a, b.y, acc[c].y);
+            }
+        }
+    }
+    __syncthreads();
+    const long long t1 = clock64();
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kFmaProbeChains; ++c) s += acc[c].x + acc[c].y;
+    sink[blockIdx.x * kFmaProbeThreads + threadIdx.x] = s;  // keeps the chains live
+    if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+// Median over the SMs of work / cycles from a device array of per-SM cycle counts.
+cudaError_t median_rate(const long long *d_cycles, int sms, double work, cudaStream_t stream, double *rate) {
+    long long *h = new long long[sms];
+    cudaError_t e = cudaMemcpyAsync(h, d_cycles, sizeof(long long) * sms, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) {
+        int n = 0;
+        for (int i = 0; i < sms; ++i)
+            if (h[i] > 0) h[n++] = h[i];
+        if (n == 0) {
+            e = cudaErrorLaunchTimeout;
+        } else {
+            std::nth_element(h, h + n / 2, h + n);
+            *rate = work / static_cast<double>(h[n / 2]);
+        }
+    }
+    delete[] h;
+    return e;
+}
+
 }  // namespace
+
+cudaError_t run_fma_rate_probe(bool packed, int iters, double *fma_per_clock_per_sm, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    long long *d_cycles = nullptr;
+    float *d_buf = nullptr;
+    cudaError_t e = cudaMalloc(&d_cycles, sizeof(long long) * sms);
+    if (e != cudaSuccess) return e;
+    e = cudaMalloc(&d_buf, sizeof(float) * (32 + static_cast<size_t>(sms) * kFmaProbeThreads));
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_buf, 0, sizeof(float) * 32, stream);
+    if (e == cudaSuccess) {
+        if (packed)
+            fma_rate_probe_kernel<true><<<sms, kFmaProbeThreads, 0, stream>>>(d_buf, iters, d_cycles, d_buf + 32);
+        else
+            fma_rate_probe_kernel<false><<<sms, kFmaProbeThreads, 0, stream>>>(d_buf, iters, d_cycles, d_buf + 32);
+        e = cudaPeekAtLastError();
+    }
+    if (e == cudaSuccess) {
+        const double fma = 2.0 * kFmaProbeChains * kFmaProbeThreads * static_cast<double>(iters);
+        e = median_rate(d_cycles, sms, fma, stream, fma_per_clock_per_sm);
+    }
+    cudaFree(d_buf);
+    cudaFree(d_cycles);
+    return e;
+}
 
 cudaError_t run_tc_rate_probe(int iters, double *flop_per_clock_per_sm, cudaStream_t stream) {
     const int sms = device_sm_count();
@@ -84,24 +173,10 @@ cudaError_t run_tc_rate_probe(int iters, double *flop_per_clock_per_sm, cudaStre
     if (e != cudaSuccess) return e;
     tc_rate_probe_kernel<<<sms, 128, kProbeSmem, stream>>>(iters, d_cycles);
     e = cudaPeekAtLastError();
-    long long *h = new long long[sms];
-    if (e == cudaSuccess) e = cudaMemcpyAsync(h, d_cycles, sizeof(long long) * sms, cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    // the median over the SMs of FLOP per clock
+    if (e == cudaSuccess)
+        e = median_rate(d_cycles, sms, 2.0 * kProbeM * kProbeN * kProbeK * 4.0 * iters, stream, flop_per_clock_per_sm);
     cudaFree(d_cycles);
-    if (e == cudaSuccess) {
-        // the median over the SMs of FLOP per clock
-        const double flop = 2.0 * kProbeM * kProbeN * kProbeK * 4.0 * iters;
-        int n = 0;
-        for (int i = 0; i < sms; ++i)
-            if (h[i] > 0) h[n++] = h[i];
-        if (n == 0) {
-            e = cudaErrorLaunchTimeout;
-        } else {
-            std::nth_element(h, h + n / 2, h + n);
-            *flop_per_clock_per_sm = flop / static_cast<double>(h[n / 2]);
-        }
-    }
-    delete[] h;
     return e;
 }
 

@@ -88,6 +88,16 @@ def test_noalloc_rejects_m_above_64_in_every_case(L):
     assert f(64, 0, 8, 1.0, 0, 0, 0.0, 0) == g.GEMM_OK                         # M <= 64, empty: no-op
 
 
+def test_rate_probes_reject_bad_arguments_without_cuda(L):
+    import ctypes
+    out = ctypes.c_double(0.0)
+    assert g.fma_rate_probe_raw(2, 1024, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.fma_rate_probe_raw(-1, 1024, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.fma_rate_probe_raw(1, 0, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.fma_rate_probe_raw(0, (1 << 20) + 1, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.fma_rate_probe_raw(1, 1024, 0) == g.GEMM_ERR_INVALID_ARG
+
+
 def test_tc_rejects_bad_types(L):
     for ab in (-1, 0, 3):   # F32 operands are not a tensor-core input type here
         assert g.gemm_tc_raw(8, 8, 8, 1.0, FAKE, FAKE, ab, 0.0, FAKE, 0) == g.GEMM_ERR_INVALID_ARG

@@ -113,3 +113,13 @@ def test_profile_summaries_name_commands_the_bench_accepts():
                 assert flag in flags, (f, flag)
             for case in re.findall(r"--profile-case\s+(\S+)", c):
                 assert case in cases, (f, case)
+
+
+def test_fma_ceiling_arithmetic():
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench._fma_ceiling({"packed_ffma2": 96.0, "scalar_ffma": 120.0}, 61.9, 152, 2070.0)["fma_rate_probe"]
+    per_clk = 61.9e12 / 2 / (152 * 2070e6)
+    assert abs(r["sgemm_fma_per_clock_per_sm"] - round(per_clk, 2)) < 1e-9
+    assert abs(r["sgemm_frac_of_packed_rate"] - per_clk / 96.0) < 1e-12
+    assert bench._fma_ceiling(None, 61.9, 152, 2070.0) == {"fma_rate_probe": None}

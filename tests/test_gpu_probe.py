@@ -1,5 +1,6 @@
-"""The tensor-core rate probe (gemm_tc_rate_probe): the dense kind::f16 rate
-per SM that the FP16 path's nominal peak is built from."""
+"""The rate probes: gemm_tc_rate_probe, the dense kind::f16 rate per SM that
+the FP16 path's nominal peak is built from, and gemm_fma_rate_probe, the FP32
+FMA throughput per SM of the packed (FFMA2) and scalar instruction forms."""
 import pytest
 
 pytestmark = pytest.mark.gpu
@@ -37,3 +38,22 @@ def test_bad_arguments():
     with pytest.raises(g.GemmError) as e:
         g.tc_rate_probe(0)
     assert e.value.status == g.GEMM_ERR_INVALID_ARG
+
+
+def test_fma_rate_probe_is_plausible():
+    # 128 FP32 FMAs per clock per SM is the nominal peak; neither form can pass
+    # it, and both reach a large part of it with independent chains
+    packed = g.fma_rate_probe(True, 2048)
+    scalar = g.fma_rate_probe(False, 2048)
+    assert 40.0 <= packed <= 128.5, packed
+    assert 40.0 <= scalar <= 128.5, scalar
+    again = g.fma_rate_probe(True, 4096)
+    assert abs(again - packed) / packed < 0.05, (packed, again)
+
+
+def test_fma_rate_probe_bad_arguments():
+    import ctypes
+    out = ctypes.c_double(0.0)
+    assert g.fma_rate_probe_raw(2, 1024, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.fma_rate_probe_raw(1, 0, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.fma_rate_probe_raw(1, 1024, 0) == g.GEMM_ERR_INVALID_ARG
