@@ -78,36 +78,51 @@ __device__ __forceinline__ float f4get(const float4 &v, int q) {
     return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
 }
 
-template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC>
+// KG > 1: the CTA holds KG groups of WARPS_M x WARPS_N warps that share one
+// tile; each pipeline stage carries KG consecutive 32-wide k slices and
+// group g takes slice g of every stage, so a tile's K is split among the
+// CTA's own warps (a small problem with few tiles still gives each scheduler
+// several warps).  The groups' partial tiles are added in shared memory,
+// groups in k order, before the epilogue.
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC, int KG = 1>
 struct SgemmTile {
-    static constexpr int kThreads = WARPS_M * WARPS_N * 32;
+    static constexpr int kGroupThreads = WARPS_M * WARPS_N * 32;  // one k group
+    static constexpr int kThreads = kGroupThreads * KG;
     static constexpr int kWM = 8 * TM;  // 8 lanes down M, TM rows each (8 apart)
     static constexpr int kWN = 4 * TN;  // 4 lanes across N, TN/4 float4 each (16 apart)
-    static constexpr int kAStage = BM * kBK;
-    static constexpr int kBStage = kBK * BN;
+    static constexpr int kAStage = BM * kBK * KG;
+    static constexpr int kBStage = kBK * BN * KG;
     static constexpr int kSmemBytes = STAGES * (kAStage + kBStage) * 4;
     static_assert(BM == WARPS_M * kWM && BN == WARPS_N * kWN, "tile does not match warp layout");
     static_assert(TN % 4 == 0, "TN must be a multiple of 4");
-    static_assert((BM * kBK / 4) % kThreads == 0 && (kBK * BN / 4) % kThreads == 0, "load split");
+    static_assert((BM * kBK / 4) % kGroupThreads == 0 && (kBK * BN / 4) % kGroupThreads == 0, "load split");
+    static_assert(KG == 1 || (KG - 1) * BM * BN * 4 <= kSmemBytes, "the groups' partial tiles fit in the ring");
 };
 
-template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC, bool PERSIST>
-__global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32 <= 128) ? 2 : 1)
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC, bool PERSIST, int KG = 1>
+__global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
+                                  (WARPS_M * WARPS_N * 32 * KG <= 128) ? 2
+                                  : KG > 1                            ? 512 / (WARPS_M * WARPS_N * 32 * KG)
+                                                                      : 1)
     sgemm_tiled_kernel(const SgemmArgs p) {
-    using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
-    constexpr int kThreads = T::kThreads;
+    using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC, KG>;
+    static_assert(KG == 1 || !PERSIST, "k groups: grid mode only");
+    // Loads and compute below are per k group: kThreads threads of group g
+    // copy and multiply the group's own 32-wide slice of each stage.
+    constexpr int kThreads = T::kGroupThreads;
     extern __shared__ __align__(128) float smem[];
     __shared__ int s_last;
-    float *As = smem;
-    float *Bs = smem + STAGES * T::kAStage;
+    const int g = KG > 1 ? static_cast<int>(threadIdx.x) / kThreads : 0;
+    float *As = smem + g * (BM * kBK);
+    float *Bs = smem + STAGES * T::kAStage + g * (kBK * BN);
 
-    const int tid = threadIdx.x;
+    const int tid = KG > 1 ? static_cast<int>(threadIdx.x) % kThreads : static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int wm = warp / WARPS_N, wn = warp % WARPS_N;
     const int lm = lane & 7, ln = lane >> 3;
     const int M = p.M, N = p.N, K = p.K;
-    const int KT = (K + kBK - 1) / kBK;
+    const int KT = (K + kBK * KG - 1) / (kBK * KG);  // pipeline stages of KG k slices
 
     // Per-thread copy coordinates.  A: 8 threads per 128-byte row, rows
     // kARowStep apart; B: BN/4 threads per row, rows kBRowStep apart.
@@ -118,6 +133,8 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32
     const int b_kr = tid / kBChunks, b_nc = tid % kBChunks;
     const uint32_t a_dst0 = smem_u32(As) + (a_row * kBK + ((a_kc ^ (a_row & 7)) << 2)) * 4;
     const uint32_t b_dst0 = smem_u32(Bs) + (b_kr * BN + b_nc * 4) * 4;
+    const int r_base = wm * T::kWM + lm;  // tile-local row of acc[0][*]
+    const int c_base = wn * T::kWN + ln * 4;
 
     float acc[TM][TN];
 
@@ -139,7 +156,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32
         const float *b_src = p.B + static_cast<size_t>(b_kr) * p.ldb + n0 + b_nc * 4;
 
         auto load_stage = [&](int stage, int kt) {
-            const int k0 = kt * kBK;
+            const int k0 = (kt * KG + g) * kBK;
             if constexpr (VEC) {
                 if (full_mn && k0 + kBK <= K) {
                     // interior slice: every copy is a full, in-bounds 16-byte chunk
@@ -286,10 +303,40 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32
             }
         }
         cp_async_wait<0>();
+        if constexpr (KG > 1) {
+            // Add the groups' partial tiles, in k order, into group 0's
+            // registers; the ring is free once every group has left the loop.
+            __syncthreads();
+            if (g > 0) {
+                float *red = smem + (g - 1) * (BM * BN);
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < TN / 4; ++jj)
+                        *reinterpret_cast<float4 *>(red + (r_base + 8 * i) * BN + c_base + 16 * jj) =
+                            make_float4(acc[i][jj * 4], acc[i][jj * 4 + 1], acc[i][jj * 4 + 2], acc[i][jj * 4 + 3]);
+            }
+            __syncthreads();
+            if (g == 0) {
+#pragma unroll 1
+                for (int gg = 1; gg < KG; ++gg) {
+                    const float *red = smem + (gg - 1) * (BM * BN);
+#pragma unroll
+                    for (int i = 0; i < TM; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < TN / 4; ++jj) {
+                            const float4 v =
+                                *reinterpret_cast<const float4 *>(red + (r_base + 8 * i) * BN + c_base + 16 * jj);
+                            acc[i][jj * 4] += v.x;
+                            acc[i][jj * 4 + 1] += v.y;
+                            acc[i][jj * 4 + 2] += v.z;
+                            acc[i][jj * 4 + 3] += v.w;
+                        }
+                }
+            }
+            __syncthreads();  // the next use of the ring overwrites the partials
+        }
     };
-
-    const int r_base = wm * T::kWM + lm;  // tile-local row of acc[0][*]
-    const int c_base = wn * T::kWN + ln * 4;
 
     // Epilogue: C = alpha * acc + beta * C (C not read when beta == 0).
     auto epilogue = [&](int m0, int n0) {
@@ -361,7 +408,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32
     auto arrive_last = [&](unsigned *counter, unsigned arrivals) -> bool {
         __threadfence();
         __syncthreads();
-        if (tid == 0) s_last = (atomicAdd(counter, 1u) == arrivals - 1u);
+        if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == arrivals - 1u);
         __syncthreads();
         const bool last = s_last != 0;
         if (last) __threadfence();
@@ -377,15 +424,19 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, (WARPS_M * WARPS_N * 32
         const int kt0 = static_cast<int>(static_cast<long long>(KT) * split / p.splits);
         const int kt1 = static_cast<int>(static_cast<long long>(KT) * (split + 1) / p.splits);
         mainloop(m0, n0, kt0, kt1);
+        // With k groups, group 0 holds the tile's sum; the other groups only
+        // take part in the CTA-wide barriers below.
         if (p.splits > 1) {
             // re-read the CTA coordinates here so they are not held across the main loop
             const int tile2 = ctaid_x(), split2 = ctaid_y();
             float *base = p.ws + static_cast<size_t>(tile2) * p.splits * (BM * BN);
-            store_partial(base + static_cast<size_t>(split2) * (BM * BN));
+            if (g == 0) store_partial(base + static_cast<size_t>(split2) * (BM * BN));
             if (!arrive_last(&p.counters[tile2], static_cast<unsigned>(p.splits))) return;
-            for (int sp = 0; sp < p.splits; ++sp) add_partial(base + static_cast<size_t>(sp) * (BM * BN), sp == 0);
-            if (tid == 0) p.counters[tile2] = 0u;  // ready for the next call on this stream
+            if (g == 0)
+                for (int sp = 0; sp < p.splits; ++sp) add_partial(base + static_cast<size_t>(sp) * (BM * BN), sp == 0);
+            if (threadIdx.x == 0) p.counters[tile2] = 0u;  // ready for the next call on this stream
         }
+        if (g != 0) return;
         tile_origin(ctaid_x(), m0, n0);
         epilogue(m0, n0);
     } else {
@@ -742,10 +793,10 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const float *__restric
     }
 }
 
-template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC, bool PERSIST>
+template <int BM, int BN, int WARPS_M, int WARPS_N, int TM, int TN, int STAGES, bool VEC, bool PERSIST, int KG = 1>
 cudaError_t launch_tiled(const SgemmArgs &a, cudaStream_t stream) {
-    using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC>;
-    auto kern = sgemm_tiled_kernel<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC, PERSIST>;
+    using T = SgemmTile<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC, KG>;
+    auto kern = sgemm_tiled_kernel<BM, BN, WARPS_M, WARPS_N, TM, TN, STAGES, VEC, PERSIST, KG>;
     static unsigned long long smem_set = 0;
     cudaError_t e = ensure_dynamic_smem(kern, T::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
@@ -967,6 +1018,21 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             std::snprintf(plan_buf, sizeof(plan_buf), "%s+colstrip%s", info->plan, strip == 1 ? "1" : "");
             info->plan = plan_buf;
         }
+    } else if (!info->tuned && (M + 63) / 64 * ((N + 63) / 64) * 2 <= sms &&
+               (M + 31) / 32 * ((N + 63) / 64) <= sms && K >= 256 && K <= 2048) {
+        // Few tiles and a short K (512^3, 256^3): 32x64 tiles, each shared by
+        // four k groups of 2 warps (4x8 per thread; group g takes the g-th 32-wide
+        // k slice of every stage), so that one wave of CTAs still gives each
+        // scheduler two warps; the groups' partials are added in shared memory.
+        // Measured on GB300 in CUDA-graph replays: 512^3 11.0 us (12.3 us for
+        // 64x64 tiles with 2 K splits), 256^3 7.6 us (8.5 us).
+        a.tiles_m = (M + 31) / 32;
+        a.tiles_n = (N + 63) / 64;
+        a.splits = 1;
+        e = vec ? launch_tiled<32, 64, 1, 2, 4, 8, 3, true, false, 4>(a, stream)
+                : launch_tiled<32, 64, 1, 2, 4, 8, 3, false, false, 4>(a, stream);
+        info->plan = repacked ? "sgemm_repack_32x64_kg4_vec16" : (vec ? "sgemm_32x64_kg4_vec16" : "sgemm_32x64_kg4_vec4b");
+        info->launches = 1 + repacked;
     } else {
         // Small problems: 64x64 CTAs (4 warps of 32x32, 4x8 per thread), with
         // K split so that there are about as many CTAs as SMs, each split at

@@ -228,3 +228,25 @@ def test_f32_column_edge_strip_exact(M, N, K, strip):
                            alpha=1.0, beta=1.0, with_scale=False)
     np.testing.assert_array_equal(got[:, N0:N].astype(np.float64), ref_s, err_msg=plan)
     np.testing.assert_array_equal(got[:, N:], d["C"][:, N:])
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 200, 500), (33, 129, 257), (100, 64, 2048), (512, 512, 512), (256, 256, 256)])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_f32_k_group_plan(M, N, K, offset):
+    # Few tiles, short K: 32x64 tiles whose K is split among four warp groups
+    # of the CTA (ragged K leaves some groups a zero-filled last slice);
+    # offset 1 puts every row off 16-byte alignment (the 4-byte copy path).
+    d = inputs.make(M, N, K, kind="f32", dist="normal", seed=M + N + K, beta=0.75)
+    got, plan = run_f32(d, -1.25, 0.75, offset=offset)
+    assert "kg4" in plan, plan
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=-1.25, beta=0.75)
+    assert_within(got, ref, S, TOL_F32, f"{M}x{N}x{K} [{plan}]")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 200, 500), (64, 640, 1024)])
+def test_f32_k_group_plan_small_integers_exact(M, N, K):
+    d = inputs.make(M, N, K, kind="f32", dist="smallint", seed=7, beta=2.0)
+    got, plan = run_f32(d, 1.0, 2.0)
+    assert "kg4" in plan, plan
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=2.0, with_scale=False)
+    np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
