@@ -22,7 +22,7 @@ import ctypes
 import os
 import threading
 
-from .build import LIB_PATH, build  # noqa: F401  (build() is part of the public API)
+from .build import DEBUG_LIB_PATH, LIB_PATH, build  # noqa: F401  (build() is part of the public API)
 
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = -1
@@ -30,6 +30,7 @@ GEMM_ERR_UNSUPPORTED = -2
 GEMM_ERR_CUDA = -3
 GEMM_ERR_TIMEOUT = -4
 GEMM_ERR_SCRATCH_LIMIT = -5
+GEMM_ERR_DEBUG_CHECK = -6
 GEMM_ACT_NONE = 0
 GEMM_ACT_GELU = 1
 GEMM_ACT_RELU = 2
@@ -54,7 +55,7 @@ EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_f16_f32acc_epilogue", "
                     "gemm_tune_set", "gemm_tune_get",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count", "gemm_tc_rate_probe",
-                    "gemm_pipeline_stall_selftest", "gemm_fma_rate_probe")
+                    "gemm_pipeline_stall_selftest", "gemm_fma_rate_probe", "gemm_debug_build")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,14 +70,23 @@ class GemmError(RuntimeError):
         super().__init__(f"{what}: {msg}")
 
 
+def library_path() -> str:
+    """The library this process uses: the debug build (libgemm11_debug.so)
+    when the environment variable GEMM11_DEBUG is 1, else libgemm11.so."""
+    return DEBUG_LIB_PATH if os.environ.get("GEMM11_DEBUG", "0") == "1" else LIB_PATH
+
+
 def lib():
-    """The loaded libgemm11.so (ctypes).  Raises if it has not been built."""
+    """The loaded library (ctypes): libgemm11.so, or libgemm11_debug.so with
+    GEMM11_DEBUG=1.  Raises if it has not been built."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(f"libgemm11.so is not built ({LIB_PATH}); call dense_gemm_11_gb300.build()")
-            L = ctypes.CDLL(LIB_PATH)
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); call "
+                                   "dense_gemm_11_gb300.build()")
+            L = ctypes.CDLL(path)
             c_int, c_float, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
             L.gemm_f32.restype = c_int
             L.gemm_f32.argtypes = [c_int, c_int, c_int, c_float, c_void_p, c_int, c_void_p, c_int, c_float,
@@ -117,12 +127,19 @@ def lib():
             L.gemm_pipeline_stall_selftest.restype = c_int
             L.gemm_pipeline_stall_selftest.argtypes = [c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int,
                                                        c_void_p]
+            L.gemm_debug_build.restype = c_int
+            L.gemm_debug_build.argtypes = []
             L.gemm_fma_rate_probe.restype = c_int
             L.gemm_fma_rate_probe.argtypes = [c_int, c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
             L.gemm_tc_rate_probe.restype = c_int
             L.gemm_tc_rate_probe.argtypes = [c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
             _lib = L
     return _lib
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the GEMM11_DEBUG build."""
+    return bool(lib().gemm_debug_build())
 
 
 def status_string(status: int) -> str:

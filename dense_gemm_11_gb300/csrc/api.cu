@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -30,6 +31,23 @@ __global__ void watchdog_probe_kernel(unsigned *err, unsigned long long limit_ns
     fence_mbarrier_init();
     if (!mbar_wait(&bar, 0, limit_ns)) atomicOr(err, kWatchdogTimeout);
 }
+
+// GEMM11_DEBUG builds: guard bands of kCanaryBytes before and after every
+// library-owned scratch buffer, filled with kCanaryByte; every call checks
+// them after its own work (canary_check_kernel) and reports a corrupted band.
+constexpr size_t kCanaryBytes = 4096;
+constexpr unsigned char kCanaryByte = 0xA5;
+constexpr unsigned kCanaryWord = 0xA5A5A5A5u;
+
+__global__ void canary_check_kernel(const unsigned *lo, const unsigned *hi, int words, unsigned *err) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x)
+        if (lo[i] != kCanaryWord || hi[i] != kCanaryWord) atomicOr(err, kDebugCanaryFault);
+}
+
+// Test hook of debug builds: overwrite the first word of a guard band (memory
+// that the library allocated, so the write is in bounds) to show the check
+// catches it.
+__global__ void canary_poke_kernel(unsigned *word) { *word = 0u; }
 
 thread_local int t_last_cuda_error = 0;
 thread_local const char *t_last_plan = "none";
@@ -67,6 +85,37 @@ struct ScratchEntry {
 };
 std::mutex g_scratch_mu;
 std::map<std::pair<int, uintptr_t>, ScratchEntry> g_scratch;
+
+// Library scratch allocation: plain cudaMalloc in release builds; debug
+// builds put a filled guard band of kCanaryBytes on both sides and hand out
+// the address past the first band.
+cudaError_t scratch_alloc(void **user, size_t bytes) {
+    if (!kDebugBuild) return cudaMalloc(user, bytes);
+    unsigned char *raw = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&raw), bytes + 2 * kCanaryBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(raw, kCanaryByte, kCanaryBytes);
+    if (e == cudaSuccess) e = cudaMemset(raw + kCanaryBytes + bytes, kCanaryByte, kCanaryBytes);
+    if (e != cudaSuccess) {
+        cudaFree(raw);
+        return e;
+    }
+    *user = raw + kCanaryBytes;
+    return cudaSuccess;
+}
+void scratch_free(void *user) {
+    if (!user) return;
+    cudaFree(kDebugBuild ? static_cast<unsigned char *>(user) - kCanaryBytes : user);
+}
+// Enqueue the guard-band check of one buffer (debug builds).
+cudaError_t check_bands(const void *user, size_t bytes, unsigned *err, cudaStream_t stream) {
+    if (!user) return cudaSuccess;
+    const unsigned char *u = static_cast<const unsigned char *>(user);
+    canary_check_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<const unsigned *>(u - kCanaryBytes),
+                                               reinterpret_cast<const unsigned *>(u + bytes),
+                                               static_cast<int>(kCanaryBytes / 4), err);
+    return cudaPeekAtLastError();
+}
 
 int current_device() {
     int d = 0;
@@ -114,22 +163,22 @@ cudaError_t acquire_scratch(cudaStream_t stream, size_t partial_floats, size_t n
         // Work already queued on this stream may still use the old buffer.
         cudaError_t r = cudaStreamSynchronize(stream);
         if (r != cudaSuccess) return r;
-        if (e.partials) cudaFree(e.partials);
+        scratch_free(e.partials);
         e.partials = nullptr;
         e.partial_floats = 0;
         size_t want = partial_floats + partial_floats / 4;
-        r = cudaMalloc(&e.partials, want * sizeof(float));
+        r = scratch_alloc(reinterpret_cast<void **>(&e.partials), want * sizeof(float));
         if (r != cudaSuccess) return r;
         e.partial_floats = want;
     }
     if (e.ncounters < ncounters) {
         cudaError_t r = cudaStreamSynchronize(stream);
         if (r != cudaSuccess) return r;
-        if (e.counters) cudaFree(e.counters);
+        scratch_free(e.counters);
         e.counters = nullptr;
         e.ncounters = 0;
         size_t want = ncounters < 1024 ? 1024 : ncounters + ncounters / 4;
-        r = cudaMalloc(&e.counters, want * sizeof(unsigned));
+        r = scratch_alloc(reinterpret_cast<void **>(&e.counters), want * sizeof(unsigned));
         if (r != cudaSuccess) return r;
         r = cudaMemset(e.counters, 0, want * sizeof(unsigned));
         if (r != cudaSuccess) return r;
@@ -148,10 +197,10 @@ cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **
     if (e.operand_floats < floats) {
         cudaError_t r = cudaStreamSynchronize(stream);  // queued work may still read the old buffer
         if (r != cudaSuccess) return r;
-        if (e.operands) cudaFree(e.operands);
+        scratch_free(e.operands);
         e.operands = nullptr;
         e.operand_floats = 0;
-        r = cudaMalloc(&e.operands, floats * sizeof(float));
+        r = scratch_alloc(reinterpret_cast<void **>(&e.operands), floats * sizeof(float));
         if (r != cudaSuccess) return r;
         e.operand_floats = floats;
     }
@@ -159,6 +208,69 @@ cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **
     return cudaSuccess;
 }
 
+size_t debug_shrink_c() {
+    if (!kDebugBuild) return 0;
+    const char *v = std::getenv("GEMM11_DEBUG_SHRINK_C");
+    return v ? static_cast<size_t>(std::strtoull(v, nullptr, 10)) : 0;
+}
+
+namespace {
+
+// Read and clear the current device's status word after synchronising
+// `stream`; maps its bits to a status.  A non-zero word also resets the
+// split-K arrival counters (a CTA that gave up may have left them non-zero).
+int read_status_word(DeviceState *ds, cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    unsigned word = 0;
+    e = cudaMemcpy(&word, ds->watchdog, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (word == 0) return GEMM_OK;
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        for (auto &kv : g_scratch)
+            if (kv.first.first == dev && kv.second.counters) {
+                e = cudaMemset(kv.second.counters, 0, kv.second.ncounters * sizeof(unsigned));
+                if (e != cudaSuccess) return fail_cuda(e);
+            }
+    }
+    const unsigned zero = 0;
+    e = cudaMemcpy(ds->watchdog, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return (word & (kDebugBoundsFault | kDebugCanaryFault)) ? GEMM_ERR_DEBUG_CHECK : GEMM_ERR_TIMEOUT;
+}
+
+// The end of every call that enqueued work: record its plan; GEMM11_DEBUG
+// builds also check the guard bands of this stream's scratch, wait for the
+// call's work and report what the device-side checks found ("start fully
+// synchronous").
+int finish_call(const CallInfo &info, cudaStream_t stream) {
+    record_plan(info);
+    if (!kDebugBuild) return GEMM_OK;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        auto it = g_scratch.find({dev, reinterpret_cast<uintptr_t>(stream)});
+        if (it != g_scratch.end()) {
+            ScratchEntry &se = it->second;
+            const char *poke = std::getenv("GEMM11_DEBUG_POKE_CANARY");
+            if (poke && poke[0] == '1' && se.partials) {
+                canary_poke_kernel<<<1, 1, 0, stream>>>(reinterpret_cast<unsigned *>(se.partials + se.partial_floats));
+            }
+            cudaError_t e = check_bands(se.partials, se.partial_floats * sizeof(float), ds->watchdog, stream);
+            if (e == cudaSuccess) e = check_bands(se.counters, se.ncounters * sizeof(unsigned), ds->watchdog, stream);
+            if (e == cudaSuccess)
+                e = check_bands(se.operands, se.operand_floats * sizeof(float), ds->watchdog, stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+        }
+    }
+    return read_status_word(ds, stream);
+}
+
+}  // namespace
 }  // namespace gemm11
 
 using namespace gemm11;
@@ -266,8 +378,7 @@ int gemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const fl
     cudaError_t e = product ? run_gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, &info)
                             : run_scale_c(M, N, beta, C, ldc, nullptr, 0, s, &info);
     if (e != cudaSuccess) return fail_cuda(e);
-    record_plan(info);
-    return GEMM_OK;
+    return finish_call(info, s);
 }
 
 int gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
@@ -295,8 +406,7 @@ int gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda, c
                             : run_scale_c(M, N, beta, C, ldc, nullptr, 0, s, &info);
     if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return fail_cuda(e);
-    record_plan(info);
-    return GEMM_OK;
+    return finish_call(info, s);
 }
 
 }  // extern "C"
@@ -350,8 +460,7 @@ int gemm_tc_checked(const TcGemm &g, int ab_type, void *stream) {
         if (e == cudaErrorNotSupported) return GEMM_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return fail_cuda(e);
-    record_plan(info);
-    return GEMM_OK;
+    return finish_call(info, s);
 }
 
 TcGemm tc_single(int M, int N, int K, float alpha, const void *A, const void *B, float beta, void *C, int c_type,
@@ -439,8 +548,7 @@ int gemm_f16_f32acc_epilogue_noalloc(int M, int N, int K, float alpha, const voi
         if (e == cudaSuccess && reject == 2) return GEMM_ERR_SCRATCH_LIMIT;
     }
     if (e != cudaSuccess) return fail_cuda(e);
-    record_plan(info);
-    return GEMM_OK;
+    return finish_call(info, s);
 }
 
 const char *gemm_status_string(int status) {
@@ -449,6 +557,9 @@ const char *gemm_status_string(int status) {
         case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
         case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: arguments outside this path's constraints";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime call failed";
+        case GEMM_ERR_DEBUG_CHECK:
+            return "GEMM_ERR_DEBUG_CHECK: a device-side check of a GEMM11_DEBUG build failed (index out of range or "
+                   "a scratch guard band overwritten)";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a bounded in-kernel wait ran out";
         case GEMM_ERR_SCRATCH_LIMIT:
             return "GEMM_ERR_SCRATCH_LIMIT: the shape needs more split-K scratch than the fixed no-allocation "
@@ -459,32 +570,13 @@ const char *gemm_status_string(int status) {
 
 int gemm_last_cuda_error(void) { return t_last_cuda_error; }
 
+int gemm_debug_build(void) { return kDebugBuild ? 1 : 0; }
+
 int gemm_check(void *stream) {
     DeviceState *ds = device_state();
     if (!ds) return fail_cuda(cudaErrorInvalidDevice);
     if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail_cuda(e);
-    unsigned word = 0;
-    e = cudaMemcpy(&word, ds->watchdog, sizeof(word), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return fail_cuda(e);
-    if (word != 0) {
-        // A CTA that gave up may have left split-K arrival counters non-zero.
-        const int dev = current_device();
-        {
-            std::lock_guard<std::mutex> lock(g_scratch_mu);
-            for (auto &kv : g_scratch)
-                if (kv.first.first == dev && kv.second.counters) {
-                    e = cudaMemset(kv.second.counters, 0, kv.second.ncounters * sizeof(unsigned));
-                    if (e != cudaSuccess) return fail_cuda(e);
-                }
-        }
-        const unsigned zero = 0;
-        e = cudaMemcpy(ds->watchdog, &zero, sizeof(zero), cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) return fail_cuda(e);
-        return GEMM_ERR_TIMEOUT;
-    }
-    return GEMM_OK;
+    return read_status_word(ds, static_cast<cudaStream_t>(stream));
 }
 
 int gemm_watchdog_selftest(int wait_ms, void *stream) {

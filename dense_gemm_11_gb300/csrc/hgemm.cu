@@ -82,7 +82,16 @@ struct HgemmArgs {
     // load, no arrival), so that the MMA and epilogue waits must run out.
     unsigned long long wait_ns = kWaitLimitNs;
     int stall_producer = 0;
+    // Checked only by GEMM11_DEBUG builds (0 = unchecked): elements of C over
+    // the whole batch, and floats of ws.
+    size_t c_extent = 0, ws_floats = 0;
 };
+
+// Host: the C extent a debug build checks stores against.
+inline size_t c_extent_of(const HgemmArgs &a) {
+    return static_cast<size_t>(a.batch - 1) * static_cast<size_t>(a.stride_c) + static_cast<size_t>(a.M - 1) * a.ldc +
+           static_cast<size_t>(a.N);
+}
 
 __host__ __device__ constexpr int tmem_cols_for(int bn) {
     return (2 * bn <= 32) ? 32 : (2 * bn <= 64) ? 64 : (2 * bn <= 128) ? 128 : (2 * bn <= 256) ? 256 : 512;
@@ -129,6 +138,12 @@ struct HgemmCfg {
 struct UnitCoord {
     int tile, split, m0, n0, kb0, kb1, batch;
 };
+
+// An element store to C, skipped (and recorded) by debug builds when the
+// index lies outside C.
+__device__ __forceinline__ void store_c(const HgemmArgs &p, size_t ci, float v) {
+    if (debug_in_bounds(p.c_extent == 0 || ci < p.c_extent, p.err)) store_out(p.C, ci, p.c_type, v);
+}
 
 // Tile number (over the whole batch) -> matrix index and tile origin.
 __device__ __forceinline__ void tile_origin(const HgemmArgs &p, int tile, int bn_tile, bool swap, UnitCoord &c) {
@@ -394,7 +409,7 @@ __device__ __forceinline__ void swap_csplit_reduce(const HgemmArgs &p, const Uni
         if (gm < p.M) {
             const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
             const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-            store_out(p.C, ci, p.c_type, epi_value(a, p, cold, b_n));
+            store_c(p, ci, epi_value(a, p, cold, b_n));
         }
     }
 }
@@ -480,6 +495,7 @@ __device__ __forceinline__ void csplit_reduce_rows(const HgemmArgs &p, const Uni
         v[1] = epi_value(v[1], p, cold[1], b4.y);
         v[2] = epi_value(v[2], p, cold[2], b4.z);
         v[3] = epi_value(v[3], p, cold[3], b4.w);
+        if (!debug_in_bounds(p.c_extent == 0 || ci + 4 <= p.c_extent, p.err)) continue;
         if (p.c_type == kOutF32) {
             *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + ci) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
@@ -598,6 +614,14 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 }
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                // GEMM11_DEBUG builds keep one stage in flight: the next load
+                // waits until the MMA has consumed this one.  (Not in cluster
+                // split-K, whose peers read each other's shared memory: its
+                // pipeline keeps its depth.)
+                if (kDebugBuild && !CSPLIT && !mbar_wait(&empty[stage], phase, p.wait_ns)) {
+                    flag_timeout(abort_flag, p.err);
+                    break;
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -791,15 +815,22 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                     swap_csplit_reduce<BN, 8>(p, c, smem_u32(part), smem_u32(part_consumed), cbase, et, b_n);
                 continue;
             }
-            const bool partial = EPI == 4 && p.splits > 1;  // the planner splits only with 4 warps
+            bool partial = EPI == 4 && p.splits > 1;  // the planner splits only with 4 warps
             float *part = nullptr;
             if (partial) part = p.ws + (static_cast<size_t>(c.tile) * p.splits + c.split) * (kBM * BN);
+            // debug builds: a slot outside the scratch is neither written nor counted
+            const bool part_ok =
+                !partial || debug_in_bounds(p.ws_floats == 0 ||
+                                                (static_cast<size_t>(c.tile) * p.splits + c.split + 1) * (kBM * BN) <=
+                                                    p.ws_floats,
+                                            p.err);
 #pragma unroll 1
             for (int ch = ch_first; ch < BN / 32; ch += ch_step) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_row + ch * 32, r);
                 tmem_wait_ld();
                 if (partial) {
+                    if (!part_ok) continue;
                     // scratch layout per unit: [chunk][column j][row 0..127] -> coalesced
                     float *dst = part + ch * 32 * kBM + row_in_tile;
 #pragma unroll
@@ -825,7 +856,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                             if (gm < p.M) {
                                 const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
                                 const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                                store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b_n));
+                                store_c(p, ci, epi_value(v[j], p, cold, b_n));
                             }
                         }
                     }
@@ -836,7 +867,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
 
-            if (partial) {
+            if (partial && part_ok) {
                 // The last contributor to arrive on this 32-row slice of the
                 // tile adds all contributions in k order (split index).
                 const int n_contrib = p.splits;
@@ -904,7 +935,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                                     if (gm < p.M) {
                                         const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
                                         const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                                        store_out(p.C, ci, p.c_type, epi_value(v[j], p, cold, b_n));
+                                        store_c(p, ci, epi_value(v[j], p, cold, b_n));
                                     }
                                 }
                             }
@@ -1099,6 +1130,13 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 }
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                // GEMM11_DEBUG builds: one stage in flight (the MMA's commit
+                // arrives on both CTAs' empty barriers)
+                if (kDebugBuild && !mbar_wait(&empty[stage], phase, p.wait_ns)) {
+                    flag_timeout(abort_flag, p.err);
+                    ok = false;
+                    break;
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -1600,6 +1638,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     a.zb = g.stride_b ? 1 : 0;
     a.stride_c = g.stride_c;
     a.b_kmajor = g.b_trans ? 1 : 0;
+    a.c_extent = c_extent_of(a);
 
     // Tile table.  M <= 64: transposed product with MMA N = M rounded up to
     // 32 or 64 (K split over a cluster when its tiles fill at most half the
@@ -1771,6 +1810,7 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
         if (e != cudaSuccess) return e;
         a.ws = sc.partials;
         a.counters = sc.counters;
+        a.ws_floats = static_cast<size_t>(tiles) * splits * kBM * bn;
     }
     const int grid = std::min(a.units, sms);
 
@@ -1913,6 +1953,7 @@ cudaError_t run_gemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
     a.za = a.zb = 0;
     a.stride_c = static_cast<long long>(M) * ldc;
     a.b_kmajor = 1;
+    a.c_extent = c_extent_of(a);
     a.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
     a.tiles_n = (N + BN - 1) / BN;
     const long long t2 = static_cast<long long>(a.tiles_m) * a.tiles_n;
@@ -2014,6 +2055,7 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
     a.batch = 1;
     a.za = a.zb = 0;
     a.stride_c = static_cast<long long>(M) * N;
+    a.c_extent = c_extent_of(a);
     const int bn = M <= 32 ? 32 : 64;
     a.tiles_m = 1;
     a.tiles_n = (N + kBM - 1) / kBM;
@@ -2039,6 +2081,7 @@ cudaError_t run_gemm_f16_small_m_noalloc(int M, int N, int K, float alpha, const
         e = cudaMemsetAsync(counters, 0, need_counters * sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;
         a.ws = partials;
+        a.ws_floats = static_cast<size_t>(tiles) * splits * kBM * bn;
         a.counters = counters;
     }
     TcGemm g;
@@ -2083,6 +2126,7 @@ cudaError_t run_hgemm_stall_selftest(int M, int N, int K, const void *A, const v
     a.err = watchdog_word();
     a.batch = 1;
     a.stride_c = static_cast<long long>(M) * N;
+    a.c_extent = c_extent_of(a);
     a.tiles_m = (M + kBM - 1) / kBM;
     a.tiles_n = (N + 127) / 128;
     if (static_cast<long long>(a.tiles_m) * a.tiles_n > (1LL << 26)) return cudaErrorNotSupported;

@@ -26,6 +26,12 @@ cudaError_t acquire_operand_scratch(cudaStream_t stream, size_t floats, float **
 // Device address of the current device's watchdog word.
 unsigned *watchdog_word();
 
+// GEMM11_DEBUG builds only: elements by which gemm_f32 shrinks the C extent
+// its kernels check stores against (environment GEMM11_DEBUG_SHRINK_C, 0 if
+// unset), so that a test can watch a device-side bounds check fire and skip
+// the stores past it.  Release builds return 0 and never read it.
+size_t debug_shrink_c();
+
 // Plain launch through cudaLaunchKernelEx with an error check.  (The grid
 // kernels here are not launched with programmatic stream serialization: their
 // CTAs are placed several per SM, and letting the next kernel's CTAs take

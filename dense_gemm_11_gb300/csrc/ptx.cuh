@@ -13,6 +13,30 @@ namespace gemm11 {
 
 // Bit set in the device watchdog word when a bounded wait gives up.
 constexpr unsigned kWatchdogTimeout = 1u;
+
+// GEMM11_DEBUG builds (compiled with -DGEMM11_DEBUG=1): device-side checks of
+// the indices of global stores and of library scratch accesses.  A failing
+// check sets kDebugBoundsFault in the same device status word and the access
+// is skipped (nothing traps); kDebugCanaryFault marks a guard band around
+// library scratch found overwritten.  Release builds compile the checks away.
+#ifndef GEMM11_DEBUG
+#define GEMM11_DEBUG 0
+#endif
+constexpr bool kDebugBuild = GEMM11_DEBUG != 0;
+constexpr unsigned kDebugBoundsFault = 2u;
+constexpr unsigned kDebugCanaryFault = 4u;
+
+// True when the access may proceed: always in release builds; in debug
+// builds only when `ok`, otherwise the fault is recorded in *err.
+__device__ __forceinline__ bool debug_in_bounds(bool ok, unsigned *err) {
+    if constexpr (kDebugBuild) {
+        if (!ok) {
+            if (err) atomicOr(err, kDebugBoundsFault);
+            return false;
+        }
+    }
+    return true;
+}
 // A single wait longer than this (nanoseconds of %globaltimer) is treated as
 // a stalled pipeline.  No legitimate wait in these kernels comes close.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

@@ -61,6 +61,10 @@ struct SgemmArgs {
     int c_vec;       // C rows 16-byte aligned
     float *ws;
     unsigned *counters;
+    // Checked only by GEMM11_DEBUG builds (0 = unchecked): elements of C from
+    // this argument block's C pointer, floats of ws; err receives the fault bit.
+    size_t c_extent, ws_floats;
+    unsigned *err;
 };
 
 __device__ __forceinline__ int ctaid_x() {
@@ -260,7 +264,10 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
             cp_async_commit();
         }
         for (int it = 0; it < nkt; ++it) {
-            cp_async_wait<STAGES - 2>();
+            // GEMM11_DEBUG builds wait for every copy in flight ("start fully
+            // synchronous"): the ring still prefetches, but no stage is read
+            // while any copy is outstanding.
+            cp_async_wait<kDebugBuild ? 0 : STAGES - 2>();
             __syncthreads();
             const int nxt = it + STAGES - 1;
             if (nxt < nkt) load_stage(nxt % STAGES, kt0 + nxt);
@@ -349,7 +356,9 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
 #pragma unroll
             for (int jj = 0; jj < TN / 4; ++jj) {
                 const int gc = n0 + c_base + 16 * jj;
+                const size_t ci = static_cast<size_t>(gr) * p.ldc + gc;
                 if (p.c_vec && gc + 3 < N) {
+                    if (!debug_in_bounds(p.c_extent == 0 || ci + 4 <= p.c_extent, p.err)) continue;
                     float4 v = make_float4(alpha * acc[i][jj * 4], alpha * acc[i][jj * 4 + 1],
                                            alpha * acc[i][jj * 4 + 2], alpha * acc[i][jj * 4 + 3]);
                     if (beta != 0.f) {
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        if (gc + e < N) {
+                        if (gc + e < N && debug_in_bounds(p.c_extent == 0 || ci + e < p.c_extent, p.err)) {
                             float v = alpha * acc[i][jj * 4 + e];
                             if (beta != 0.f) v = fmaf(beta, crow[gc + e], v);
                             crow[gc + e] = v;
@@ -374,8 +383,13 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
         }
     };
 
+    // A partial tile's scratch slot lies inside the scratch (debug builds check).
+    auto slot_ok = [&](const float *slot) {
+        return debug_in_bounds(p.ws_floats == 0 || static_cast<size_t>(slot - p.ws) + BM * BN <= p.ws_floats, p.err);
+    };
     // Raw partial tile -> scratch slot (tile-local [BM][BN], row-major).
     auto store_partial = [&](float *slot) {
+        if (!slot_ok(slot)) return;
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -385,6 +399,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
     };
     // acc += slot (L2 reads: the slot was written by another CTA).
     auto add_partial = [&](const float *slot, bool first) {
+        if (!slot_ok(slot)) return;
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -527,8 +542,9 @@ __global__ void __launch_bounds__(256) sgemm_streamk_fixup_kernel(const SgemmArg
         const int c = (v % kVecPerRow) * 4;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < n_own; ++i) {
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(
-                p.ws + static_cast<size_t>(s_slot[i]) * (BM * BN) + r * BN + c));
+            const size_t wi = static_cast<size_t>(s_slot[i]) * (BM * BN) + r * BN + c;
+            if (!debug_in_bounds(p.ws_floats == 0 || wi + 4 <= p.ws_floats, p.err)) continue;
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.ws + wi));
             if (i == 0) {
                 s = x;
             } else {
@@ -544,7 +560,8 @@ __global__ void __launch_bounds__(256) sgemm_streamk_fixup_kernel(const SgemmArg
         const float sv[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            if (gc + e < p.N) {
+            if (gc + e < p.N &&
+                debug_in_bounds(p.c_extent == 0 || static_cast<size_t>(gr) * p.ldc + gc + e < p.c_extent, p.err)) {
                 float val = p.alpha * sv[e];
                 if (p.beta != 0.f) val = fmaf(p.beta, crow[gc + e], val);
                 crow[gc + e] = val;
@@ -882,6 +899,9 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
     a.ldb = ldb;
     a.ldc = ldc;
     a.c_vec = aligned16(C) && (ldc % 4 == 0);
+    a.err = watchdog_word();
+    a.c_extent = static_cast<size_t>(M - 1) * ldc + N;
+    if (kDebugBuild) a.c_extent -= std::min<size_t>(a.c_extent, debug_shrink_c());
     bool vec = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
     const int KT = (K + kBK - 1) / kBK;
     int repacked = 0;
@@ -968,6 +988,7 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             s2.N = strip;
             s2.B = a.B + N0;
             s2.C = C + N0;
+            s2.c_extent = a.c_extent > static_cast<size_t>(N0) ? a.c_extent - N0 : 1;
             s2.c_vec = aligned16(s2.C) && (ldc % 4 == 0);
             s2.tiles_m = (M + 63) / 64;
             s2.tiles_n = 1;
@@ -985,8 +1006,10 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             if (e != cudaSuccess) return e;
             a.ws = sc.partials;
             a.counters = sc.counters;
+            a.ws_floats = main_floats;
             s2.ws = sc.partials + main_floats;
             s2.counters = sc.counters;
+            s2.ws_floats = strip_floats;
         }
         e = vec ? launch_tiled<128, 256, 2, 4, 8, 16, 3, true, true>(a, stream)
                 : launch_tiled<128, 256, 2, 4, 8, 16, 3, false, true>(a, stream);
@@ -1054,6 +1077,7 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             if (e != cudaSuccess) return e;
             a.ws = sc.partials;
             a.counters = sc.counters;
+            a.ws_floats = static_cast<size_t>(tiles) * splits * 64 * 64;
         }
         e = vec ? launch_tiled<64, 64, 2, 2, 4, 8, 3, true, false>(a, stream)
                 : launch_tiled<64, 64, 2, 2, 4, 8, 3, false, false>(a, stream);

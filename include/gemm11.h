@@ -35,6 +35,25 @@
  *   - Split-K shapes use a library-owned workspace, allocated lazily once per
  *     (device, stream) and reused; calls on one stream are serialised by the
  *     stream, calls on different streams use different workspaces.
+ *   - Debug build.  The same sources compiled with GEMM11_DEBUG=1 give
+ *     libgemm11_debug.so (the Python binding loads it when the environment
+ *     variable GEMM11_DEBUG is 1).  The DeepGEMM essay "企业官网建设流程全解析"
+ *     (section 6.1) advises starting fully synchronous and relaxing later;
+ *     this build is the synchronous end of that:
+ *       - the pipelines keep one operand stage in flight (the FP32 path
+ *         waits for every outstanding copy before it reads a stage; the
+ *         tensor-core producers wait for the MMA to consume each stage);
+ *       - stores to C and accesses to library scratch check their index
+ *         against the extent; a failing check records a fault bit in the
+ *         device status word and the access is skipped (nothing traps);
+ *       - library scratch is allocated with guard bands of 4 KiB on both
+ *         sides, filled with 0xA5 and checked after every call;
+ *       - every compute call synchronises its stream before it returns and
+ *         returns GEMM_ERR_DEBUG_CHECK (index or guard band) or
+ *         GEMM_ERR_TIMEOUT when the device reported one.  Calls are therefore
+ *         blocking in this build.
+ *     Release builds compile all of this away (gemm_debug_build() tells them
+ *     apart).
  */
 #ifndef GEMM11_H
 #define GEMM11_H
@@ -55,7 +74,8 @@ typedef enum {
     GEMM_ERR_UNSUPPORTED = -2, /* valid arguments this path cannot take (alignment) */
     GEMM_ERR_CUDA = -3,        /* a CUDA runtime call failed; see gemm_last_cuda_error() */
     GEMM_ERR_TIMEOUT = -4,     /* a bounded in-kernel wait ran out (from gemm_check) */
-    GEMM_ERR_SCRATCH_LIMIT = -5 /* the no-allocation entry point's fixed scratch is too small */
+    GEMM_ERR_SCRATCH_LIMIT = -5, /* the no-allocation entry point's fixed scratch is too small */
+    GEMM_ERR_DEBUG_CHECK = -6   /* GEMM11_DEBUG builds: a device-side check failed (see below) */
 } gemm_status;
 
 typedef enum {
@@ -283,6 +303,9 @@ GEMM11_API int gemm_tune_set(const gemm_tune_entry *entries, int n);
  * returns the number of entries in the table. */
 GEMM11_API int gemm_tune_get(gemm_tune_entry *out, int capacity);
 
+/* 1 in a GEMM11_DEBUG build of the library, 0 in a release build. */
+GEMM11_API int gemm_debug_build(void);
+
 /* Text for a gemm_status value (static storage, never NULL). */
 GEMM11_API const char *gemm_status_string(int status);
 
@@ -292,8 +315,9 @@ GEMM11_API int gemm_last_cuda_error(void);
 /*
  * gemm_check -- synchronise `stream`, then read and clear the current
  * device's watchdog word.  Returns GEMM_ERR_TIMEOUT if a bounded wait ran out
- * in any kernel since the previous check, GEMM_ERR_CUDA if the synchronisation
- * failed, GEMM_OK otherwise.
+ * in any kernel since the previous check (GEMM_ERR_DEBUG_CHECK instead when a
+ * debug build's device-side check failed), GEMM_ERR_CUDA if the
+ * synchronisation failed, GEMM_OK otherwise.
  */
 GEMM11_API int gemm_check(void *stream);
 

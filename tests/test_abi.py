@@ -98,6 +98,34 @@ def test_rate_probes_reject_bad_arguments_without_cuda(L):
     assert g.fma_rate_probe_raw(1, 1024, 0) == g.GEMM_ERR_INVALID_ARG
 
 
+def test_debug_build_exports_every_symbol_and_says_so(L):
+    """The GEMM11_DEBUG variant (libgemm11_debug.so) is the same C ABI; only
+    gemm_debug_build() tells the two apart."""
+    from dense_gemm_11_gb300.build import DEBUG_LIB_PATH
+    if not os.path.exists(DEBUG_LIB_PATH):
+        g.build(debug=True)
+    D = ctypes.CDLL(DEBUG_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(D, name), name
+    D.gemm_debug_build.restype = ctypes.c_int
+    L.gemm_debug_build.restype = ctypes.c_int
+    assert D.gemm_debug_build() == 1 and L.gemm_debug_build() == 0
+    # argument checks behave alike (no CUDA call is made)
+    D.gemm_f32.restype = ctypes.c_int
+    D.gemm_f32.argtypes = L.gemm_f32.argtypes
+    assert D.gemm_f32(-1, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, None) == g.GEMM_ERR_INVALID_ARG
+    D.gemm_status_string.restype = ctypes.c_char_p
+    assert b"GEMM11_DEBUG" in D.gemm_status_string(g.GEMM_ERR_DEBUG_CHECK)
+
+
+def test_status_codes_match_the_header():
+    text = open(HEADER).read()
+    for name in ("GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
+                 "GEMM_ERR_SCRATCH_LIMIT", "GEMM_ERR_DEBUG_CHECK"):
+        m = re.search(name + r"\s*=\s*(-?\d+)", text)
+        assert m and int(m.group(1)) == getattr(g, name), name
+
+
 def test_tc_rejects_bad_types(L):
     for ab in (-1, 0, 3):   # F32 operands are not a tensor-core input type here
         assert g.gemm_tc_raw(8, 8, 8, 1.0, FAKE, FAKE, ab, 0.0, FAKE, 0) == g.GEMM_ERR_INVALID_ARG
