@@ -54,9 +54,12 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms while running.
+    Each sample carries nvidia-smi's timestamp; window(t0, t1) limits the
+    summary to the samples taken inside a wall-clock interval (the timed
+    region), falling back to all samples when none falls inside it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -64,12 +67,13 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.out = os.path.join("/tmp", f"gemm11_clocks_{os.getpid()}.csv")
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
@@ -82,6 +86,18 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
+    def window(self, t0: float, t1: float):
+        """Restrict the summary to samples between the wall-clock times t0 and t1."""
+        self.t0, self.t1 = t0, t1
+
+    @staticmethod
+    def _stamp(text: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except Exception:
+            return None
+
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -89,18 +105,24 @@ class ClockSampler:
         try:
             for line in open(self.out):
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                if len(parts) >= 10 and parts[2].replace(".", "").isdigit():
                     rows.append(parts)
         except Exception:
             pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows]
-        smax = max(float(r[2]) for r in rows)
+        inside = rows
+        if self.t0 is not None:
+            inside = [r for r in rows if (t := self._stamp(r[0])) is not None and self.t0 <= t <= self.t1]
+        scope = "timed region" if inside and self.t0 is not None else "whole run"
+        use = inside or rows
+        sm = [float(r[2]) for r in use]
+        smax = max(float(r[3]) for r in use)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+        reasons = sorted({names[i] for r in use for i in range(4) if r[6 + i].lower() == "active"})
+        power = [float(r[4]) for r in use if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons, "samples": len(use),
+                "samples_scope": scope, "sampling_ms": 20, "power_w_max": max(power) if power else None}
 
 
 def max_over_ranks(values, dist=None, device=None):
@@ -279,10 +301,12 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
         t_wall0 = time.perf_counter()
+        t_epoch0 = time.time()
         for s in range(args.steps):
             step(events[s])
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
+        clk.window(t_epoch0, time.time())
         if dist:
             dist.barrier()
     st = g.check(stream)

@@ -123,3 +123,24 @@ def test_fma_ceiling_arithmetic():
     assert abs(r["sgemm_fma_per_clock_per_sm"] - round(per_clk, 2)) < 1e-9
     assert abs(r["sgemm_frac_of_packed_rate"] - per_clk / 96.0) < 1e-12
     assert bench._fma_ceiling(None, 61.9, 152, 2070.0) == {"fma_rate_probe": None}
+
+
+def test_clock_sampler_summarises_the_timed_window(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler(0)
+    cs.out = str(tmp_path / "clk.csv")
+    cs.proc = object()  # a sampler that ran
+    lines = ["2026/12/02 10:00:00.000, 0, 1500, 2070, 300.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "2026/12/02 10:00:01.000, 0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active",
+             "2026/12/02 10:00:01.020, 0, 2060, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "2026/12/02 10:00:05.000, 0, 1200, 2070, 100.0, 0x0, Active, Not Active, Not Active, Not Active"]
+    open(cs.out, "w").write("\n".join(lines) + "\n")
+    t0 = cs._stamp("2026/12/02 10:00:00.900")
+    t1 = cs._stamp("2026/12/02 10:00:01.100")
+    cs.window(t0, t1)
+    r = cs.summary()
+    assert r["samples"] == 2 and r["samples_scope"] == "timed region"
+    assert r["sm_mhz"] == 2065.0 and r["reasons"] == ["sw_power_cap"] and r["power_w_max"] == 950.0
+    cs.window(t1 + 10, t1 + 11)  # nothing inside: every sample is used
+    assert cs.summary()["samples_scope"] == "whole run" and cs.summary()["samples"] == 4
