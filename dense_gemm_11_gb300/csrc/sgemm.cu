@@ -61,11 +61,51 @@ struct SgemmArgs {
     int c_vec;       // C rows 16-byte aligned
     float *ws;
     unsigned *counters;
-    // Checked only by GEMM11_DEBUG builds (0 = unchecked): elements of C from
-    // this argument block's C pointer, floats of ws; err receives the fault bit.
+#if GEMM11_DEBUG
+    // GEMM11_DEBUG builds only (0 = unchecked): elements of C from this
+    // argument block's C pointer, floats of ws; err receives the fault bit.
+    // Release builds leave the fields out: the persistent kernel sits at its
+    // register limit, and a larger argument block alone moved it to spilling.
     size_t c_extent, ws_floats;
     unsigned *err;
+#endif
 };
+
+// The debug fields, as constants in release builds.
+__host__ __device__ __forceinline__ size_t sg_c_extent(const SgemmArgs &p) {
+#if GEMM11_DEBUG
+    return p.c_extent;
+#else
+    (void)p;
+    return 0;
+#endif
+}
+__host__ __device__ __forceinline__ size_t sg_ws_floats(const SgemmArgs &p) {
+#if GEMM11_DEBUG
+    return p.ws_floats;
+#else
+    (void)p;
+    return 0;
+#endif
+}
+__host__ __device__ __forceinline__ unsigned *sg_err(const SgemmArgs &p) {
+#if GEMM11_DEBUG
+    return p.err;
+#else
+    (void)p;
+    return nullptr;
+#endif
+}
+// Host: set the debug fields (no-op in release builds).
+inline void sg_set_debug(SgemmArgs &a, size_t c_extent, size_t ws_floats, unsigned *err) {
+#if GEMM11_DEBUG
+    a.c_extent = c_extent;
+    a.ws_floats = ws_floats;
+    a.err = err;
+#else
+    (void)a, (void)c_extent, (void)ws_floats, (void)err;
+#endif
+}
 
 __device__ __forceinline__ int ctaid_x() {
     int v;
@@ -137,8 +177,6 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
     const int b_kr = tid / kBChunks, b_nc = tid % kBChunks;
     const uint32_t a_dst0 = smem_u32(As) + (a_row * kBK + ((a_kc ^ (a_row & 7)) << 2)) * 4;
     const uint32_t b_dst0 = smem_u32(Bs) + (b_kr * BN + b_nc * 4) * 4;
-    const int r_base = wm * T::kWM + lm;  // tile-local row of acc[0][*]
-    const int c_base = wn * T::kWN + ln * 4;
 
     float acc[TM][TN];
 
@@ -313,6 +351,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
         if constexpr (KG > 1) {
             // Add the groups' partial tiles, in k order, into group 0's
             // registers; the ring is free once every group has left the loop.
+            const int r_base = wm * T::kWM + lm, c_base = wn * T::kWN + ln * 4;
             __syncthreads();
             if (g > 0) {
                 float *red = smem + (g - 1) * (BM * BN);
@@ -345,6 +384,9 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
         }
     };
 
+    const int r_base = wm * T::kWM + lm;  // tile-local row of acc[0][*]
+    const int c_base = wn * T::kWN + ln * 4;
+
     // Epilogue: C = alpha * acc + beta * C (C not read when beta == 0).
     auto epilogue = [&](int m0, int n0) {
         const float alpha = p.alpha, beta = p.beta;
@@ -358,7 +400,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
                 const int gc = n0 + c_base + 16 * jj;
                 const size_t ci = static_cast<size_t>(gr) * p.ldc + gc;
                 if (p.c_vec && gc + 3 < N) {
-                    if (!debug_in_bounds(p.c_extent == 0 || ci + 4 <= p.c_extent, p.err)) continue;
+                    if (!debug_in_bounds(sg_c_extent(p) == 0 || ci + 4 <= sg_c_extent(p), sg_err(p))) continue;
                     float4 v = make_float4(alpha * acc[i][jj * 4], alpha * acc[i][jj * 4 + 1],
                                            alpha * acc[i][jj * 4 + 2], alpha * acc[i][jj * 4 + 3]);
                     if (beta != 0.f) {
@@ -372,7 +414,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        if (gc + e < N && debug_in_bounds(p.c_extent == 0 || ci + e < p.c_extent, p.err)) {
+                        if (gc + e < N && debug_in_bounds(sg_c_extent(p) == 0 || ci + e < sg_c_extent(p), sg_err(p))) {
                             float v = alpha * acc[i][jj * 4 + e];
                             if (beta != 0.f) v = fmaf(beta, crow[gc + e], v);
                             crow[gc + e] = v;
@@ -385,7 +427,8 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32 * KG,
 
     // A partial tile's scratch slot lies inside the scratch (debug builds check).
     auto slot_ok = [&](const float *slot) {
-        return debug_in_bounds(p.ws_floats == 0 || static_cast<size_t>(slot - p.ws) + BM * BN <= p.ws_floats, p.err);
+        return debug_in_bounds(sg_ws_floats(p) == 0 || static_cast<size_t>(slot - p.ws) + BM * BN <= sg_ws_floats(p),
+                               sg_err(p));
     };
     // Raw partial tile -> scratch slot (tile-local [BM][BN], row-major).
     auto store_partial = [&](float *slot) {
@@ -543,7 +586,7 @@ __global__ void __launch_bounds__(256) sgemm_streamk_fixup_kernel(const SgemmArg
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < n_own; ++i) {
             const size_t wi = static_cast<size_t>(s_slot[i]) * (BM * BN) + r * BN + c;
-            if (!debug_in_bounds(p.ws_floats == 0 || wi + 4 <= p.ws_floats, p.err)) continue;
+            if (!debug_in_bounds(sg_ws_floats(p) == 0 || wi + 4 <= sg_ws_floats(p), sg_err(p))) continue;
             const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.ws + wi));
             if (i == 0) {
                 s = x;
@@ -561,7 +604,8 @@ __global__ void __launch_bounds__(256) sgemm_streamk_fixup_kernel(const SgemmArg
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             if (gc + e < p.N &&
-                debug_in_bounds(p.c_extent == 0 || static_cast<size_t>(gr) * p.ldc + gc + e < p.c_extent, p.err)) {
+                debug_in_bounds(sg_c_extent(p) == 0 || static_cast<size_t>(gr) * p.ldc + gc + e < sg_c_extent(p),
+                                sg_err(p))) {
                 float val = p.alpha * sv[e];
                 if (p.beta != 0.f) val = fmaf(p.beta, crow[gc + e], val);
                 crow[gc + e] = val;
@@ -899,9 +943,10 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
     a.ldb = ldb;
     a.ldc = ldc;
     a.c_vec = aligned16(C) && (ldc % 4 == 0);
-    a.err = watchdog_word();
-    a.c_extent = static_cast<size_t>(M - 1) * ldc + N;
-    if (kDebugBuild) a.c_extent -= std::min<size_t>(a.c_extent, debug_shrink_c());
+    // checked extent of C (debug builds; a test hook may shrink it)
+    size_t c_extent = static_cast<size_t>(M - 1) * ldc + N;
+    if (kDebugBuild) c_extent -= std::min<size_t>(c_extent, debug_shrink_c());
+    sg_set_debug(a, c_extent, 0, watchdog_word());
     bool vec = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
     const int KT = (K + kBK - 1) / kBK;
     int repacked = 0;
@@ -988,7 +1033,7 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             s2.N = strip;
             s2.B = a.B + N0;
             s2.C = C + N0;
-            s2.c_extent = a.c_extent > static_cast<size_t>(N0) ? a.c_extent - N0 : 1;
+            sg_set_debug(s2, c_extent > static_cast<size_t>(N0) ? c_extent - N0 : 1, 0, watchdog_word());
             s2.c_vec = aligned16(s2.C) && (ldc % 4 == 0);
             s2.tiles_m = (M + 63) / 64;
             s2.tiles_n = 1;
@@ -1006,10 +1051,10 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             if (e != cudaSuccess) return e;
             a.ws = sc.partials;
             a.counters = sc.counters;
-            a.ws_floats = main_floats;
+            sg_set_debug(a, c_extent, main_floats, watchdog_word());
             s2.ws = sc.partials + main_floats;
             s2.counters = sc.counters;
-            s2.ws_floats = strip_floats;
+            sg_set_debug(s2, c_extent > static_cast<size_t>(N0) ? c_extent - N0 : 1, strip_floats, watchdog_word());
         }
         e = vec ? launch_tiled<128, 256, 2, 4, 8, 16, 3, true, true>(a, stream)
                 : launch_tiled<128, 256, 2, 4, 8, 16, 3, false, true>(a, stream);
@@ -1077,7 +1122,7 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
             if (e != cudaSuccess) return e;
             a.ws = sc.partials;
             a.counters = sc.counters;
-            a.ws_floats = static_cast<size_t>(tiles) * splits * 64 * 64;
+            sg_set_debug(a, c_extent, static_cast<size_t>(tiles) * splits * 64 * 64, watchdog_word());
         }
         e = vec ? launch_tiled<64, 64, 2, 2, 4, 8, 3, true, false>(a, stream)
                 : launch_tiled<64, 64, 2, 2, 4, 8, 3, false, false>(a, stream);
