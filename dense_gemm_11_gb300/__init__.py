@@ -433,8 +433,9 @@ def pipeline_stall_selftest_raw(M, N, K, A_ptr, B_ptr, C_ptr, wait_ms=5, stream_
 
 
 def fma_rate_probe(packed: bool = True, iters: int = 4096, stream=None) -> float:
-    """FP32 FMAs per clock per SM, measured with the packed two-wide FMA form
-    of gemm_f32's outer product (packed=True) or with scalar FMAs."""
+    """FP32 FMAs per clock per SM of an 8 x 8 outer product in registers,
+    measured with the packed two-wide FMA form gemm_f32 uses (packed=True)
+    or with scalar FMAs."""
     out = ctypes.c_double(0.0)
     st = lib().gemm_fma_rate_probe(1 if packed else 0, int(iters), ctypes.byref(out), _stream_handle(stream))
     if st != GEMM_OK:

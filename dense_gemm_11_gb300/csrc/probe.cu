@@ -74,37 +74,47 @@ __global__ void __launch_bounds__(128, 1) tc_rate_probe_kernel(int iters, long l
     }
 }
 
-// FP32 FMA throughput with 8 warps per SM (two per scheduler, the SGEMM's
-// residency), 32 independent two-wide accumulator chains per thread and
-// operands in registers.  PACKED: one packed FMA (__ffma2_rn) per chain and
-// step with the same scalar in both lanes of one operand, the form of the
-// SGEMM's outer product (a_i * (b_j, b_j+1)); otherwise two scalar fmaf.
-// Each CTA times its loop with the SM cycle counter between two barriers.
-constexpr int kFmaProbeThreads = 256, kFmaProbeChains = 32;
+// FP32 FMA throughput of an outer product in registers: 8 warps per SM
+// (two per scheduler, the SGEMM's residency; the CTA requests more than half
+// an SM's shared memory, so no SM holds two), and per thread 8 values a_i
+// times 8 values b_j into 64 accumulators per step, a_i reused across
+// consecutive instructions as in the SGEMM's inner loop.  PACKED: 32 packed
+// FMAs (__ffma2_rn) per step, (a_i, a_i) * (b_2jj, b_2jj+1), the SGEMM's form;
+// otherwise 64 scalar fmaf.  No memory traffic inside the timed loop.  Each
+// CTA times its loop with the SM cycle counter between two barriers.
+constexpr int kFmaProbeThreads = 256;
 
 template <bool PACKED>
 __global__ void __launch_bounds__(kFmaProbeThreads, 1) fma_rate_probe_kernel(const float *in, int iters,
                                                                              long long *cycles, float *sink) {
-    float av[4], bv[16];
+    float a[8], b[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) av[j] = in[j];
+    for (int j = 0; j < 8; ++j) {
+        a[j] = in[j];
+        b[j] = in[8 + j];
+    }
+    float acc[8][8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) bv[j] = in[4 + j];
-    float2 acc[kFmaProbeChains];
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int c = 0; c < kFmaProbeChains; ++c) acc[c] = make_float2(0.f, 0.f);
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
     __syncthreads();
     const long long t0 = clock64();
     for (int it = 0; it < iters; ++it) {
 #pragma unroll
-        for (int c = 0; c < kFmaProbeChains; ++c) {
-            const float a = av[c & 3];
-            const float2 b = make_float2(bv[(2 * c) & 15], bv[(2 * c + 1) & 15]);
-            if (PACKED) {
-                acc[c] = __ffma2_rn(make_float2(a, a), b, acc[c]);
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (PACKED) {
+                const float2 a2 = make_float2(a[i], a[i]);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float2 c = __ffma2_rn(a2, make_float2(b[2 * jj], b[2 * jj + 1]),
+                                                make_float2(acc[i][2 * jj], acc[i][2 * jj + 1]));
+                    acc[i][2 * jj] = c.x;
+                    acc[i][2 * jj + 1] = c.y;
+                }
             } else {
-                acc[c].x = fmaf(a, b.x, acc[c].x);
-                acc[c].y = fmaf(a, b.y, acc[c].y);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
             }
         }
     }
@@ -112,7 +122,9 @@ __global__ void __launch_bounds__(kFmaProbeThreads, 1) fma_rate_probe_kernel(con
     const long long t1 = clock64();
     float s = 0.f;
 #pragma unroll
-    for (int c = 0; c < kFmaProbeChains; ++c) s += acc[c].x + acc[c].y;
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += acc[i][j];
     sink[blockIdx.x * kFmaProbeThreads + threadIdx.x] = s;  // keeps the chains live
     if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
@@ -148,14 +160,21 @@ cudaError_t run_fma_rate_probe(bool packed, int iters, double *fma_per_clock_per
     e = cudaMalloc(&d_buf, sizeof(float) * (32 + static_cast<size_t>(sms) * kFmaProbeThreads));
     if (e == cudaSuccess) e = cudaMemsetAsync(d_buf, 0, sizeof(float) * 32, stream);
     if (e == cudaSuccess) {
-        if (packed)
-            fma_rate_probe_kernel<true><<<sms, kFmaProbeThreads, 0, stream>>>(d_buf, iters, d_cycles, d_buf + 32);
-        else
-            fma_rate_probe_kernel<false><<<sms, kFmaProbeThreads, 0, stream>>>(d_buf, iters, d_cycles, d_buf + 32);
-        e = cudaPeekAtLastError();
+        static unsigned long long smem_set_packed = 0, smem_set_scalar = 0;
+        e = packed ? ensure_dynamic_smem(fma_rate_probe_kernel<true>, kProbeSmem, smem_set_packed)
+                   : ensure_dynamic_smem(fma_rate_probe_kernel<false>, kProbeSmem, smem_set_scalar);
+        if (e == cudaSuccess) {
+            if (packed)
+                fma_rate_probe_kernel<true><<<sms, kFmaProbeThreads, kProbeSmem, stream>>>(d_buf, iters, d_cycles,
+                                                                                          d_buf + 32);
+            else
+                fma_rate_probe_kernel<false><<<sms, kFmaProbeThreads, kProbeSmem, stream>>>(d_buf, iters, d_cycles,
+                                                                                           d_buf + 32);
+            e = cudaPeekAtLastError();
+        }
     }
     if (e == cudaSuccess) {
-        const double fma = 2.0 * kFmaProbeChains * kFmaProbeThreads * static_cast<double>(iters);
+        const double fma = 64.0 * kFmaProbeThreads * static_cast<double>(iters);
         e = median_rate(d_cycles, sms, fma, stream, fma_per_clock_per_sm);
     }
     cudaFree(d_buf);

@@ -374,14 +374,15 @@ GEMM11_API int gemm_tc_rate_probe(int iters, double *flop_per_clock_per_sm, void
 
 /*
  * gemm_fma_rate_probe -- diagnostic: the FP32 FMA units' throughput per SM,
- * measured, for the instruction form an FP32 GEMM's outer product can use:
- * packed = 1, the two-wide FMA (__ffma2_rn, one FMA on each of two lanes)
- * with the same scalar in both lanes of one operand -- gemm_f32's form;
- * packed = 0, scalar FMAs.  One CTA of 8 warps per SM (gemm_f32's residency)
- * runs 32 independent accumulator chains per thread for `iters` steps on
- * register operands (no memory traffic) and times them with the SM cycle
- * counter; *fma_per_clock_per_sm receives the median over the SMs of FMAs
- * per clock (the nominal peak is 128 per SM per clock: 4 schedulers x 32
+ * measured on an outer product in registers, for the instruction form an
+ * FP32 GEMM can use: packed = 1, the two-wide FMA (__ffma2_rn, one FMA on
+ * each of two lanes) with the same scalar in both lanes of one operand --
+ * gemm_f32's form; packed = 0, scalar FMAs.  One CTA of 8 warps per SM
+ * (gemm_f32's residency); each thread multiplies 8 values a_i by 8 values
+ * b_j into 64 accumulators per step, a_i reused across consecutive
+ * instructions, for `iters` steps (no memory traffic), timed with the SM
+ * cycle counter; *fma_per_clock_per_sm receives the median over the SMs of
+ * FMAs per clock (the nominal peak is 128 per SM per clock: 4 schedulers x 32
  * lanes).  gemm_f32's FFMA-pipe roofline is quoted against the nominal peak;
  * this measures how much of it each instruction form reaches at all.
  * Synchronous on `stream` (allocates and frees a small device buffer).
