@@ -55,7 +55,8 @@ EXPORTED_SYMBOLS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_f16_f32acc_epilogue", "
                     "gemm_tune_set", "gemm_tune_get",
                     "gemm_status_string", "gemm_last_cuda_error", "gemm_check", "gemm_watchdog_selftest",
                     "gemm_last_plan", "gemm_last_launch_count", "gemm_tc_rate_probe",
-                    "gemm_pipeline_stall_selftest", "gemm_fma_rate_probe", "gemm_debug_build")
+                    "gemm_pipeline_stall_selftest", "gemm_fma_rate_probe", "gemm_tma_read_probe",
+                    "gemm_debug_build")
 
 _lock = threading.Lock()
 _lib = None
@@ -133,6 +134,9 @@ def lib():
             L.gemm_fma_rate_probe.argtypes = [c_int, c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
             L.gemm_tc_rate_probe.restype = c_int
             L.gemm_tc_rate_probe.argtypes = [c_int, ctypes.POINTER(ctypes.c_double), c_void_p]
+            L.gemm_tma_read_probe.restype = c_int
+            L.gemm_tma_read_probe.argtypes = [c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(ctypes.c_double),
+                                              ctypes.POINTER(ctypes.c_double), c_void_p]
             _lib = L
     return _lib
 
@@ -441,6 +445,30 @@ def fma_rate_probe(packed: bool = True, iters: int = 4096, stream=None) -> float
     if st != GEMM_OK:
         raise GemmError(st, "gemm_fma_rate_probe")
     return float(out.value)
+
+
+def tma_read_probe(clusters: int, multicast: bool = False, stages: int = 4, kblocks: int = 512,
+                   region_mb: int = 24, stream=None) -> dict:
+    """Bytes per SM clock that each CTA receives through TMA (median over the
+    CTAs) and the total GB/s, for `clusters` clusters of 2 CTAs streaming
+    `kblocks` 32 KB stages (the 64-wide k block of a 256-row panel of a
+    K-major FP16 operand with 4096-element rows, two 128-row boxes) from a
+    `region_mb` MB region (24 MB stays in L2), each CTA loading its own copy
+    or (multicast=True) one box per CTA multicast to both."""
+    per_sm, total = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    st = lib().gemm_tma_read_probe(int(clusters), 1 if multicast else 0, int(stages), int(kblocks), int(region_mb),
+                                   ctypes.byref(per_sm), ctypes.byref(total), _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_tma_read_probe")
+    return {"bytes_per_clock_per_sm": float(per_sm.value), "total_gbs": float(total.value)}
+
+
+def tma_read_probe_raw(clusters, multicast, stages, kblocks, region_mb, per_sm_ptr, total_ptr, stream_ptr=0) -> int:
+    """Direct C-ABI call of gemm_tma_read_probe (pointers: addresses of doubles, or 0)."""
+    dp = ctypes.POINTER(ctypes.c_double)
+    return int(lib().gemm_tma_read_probe(int(clusters), int(multicast), int(stages), int(kblocks), int(region_mb),
+                                         ctypes.cast(per_sm_ptr, dp), ctypes.cast(total_ptr, dp),
+                                         ctypes.c_void_p(stream_ptr)))
 
 
 def fma_rate_probe_raw(packed, iters, out_ptr, stream_ptr=0) -> int:

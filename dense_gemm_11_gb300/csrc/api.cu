@@ -639,6 +639,24 @@ int gemm_tc_rate_probe(int iters, double *flop_per_clock_per_sm, void *stream) {
     return GEMM_OK;
 }
 
+int gemm_tma_read_probe(int clusters, int multicast, int stages, int kblocks, int region_mb,
+                        double *bytes_per_clock_per_sm, double *total_gbs, void *stream) {
+    if (clusters < 1 || (multicast != 0 && multicast != 1) || stages < 1 || stages > 6 || kblocks < 1 ||
+        kblocks > (1 << 16) || region_mb < 2 || region_mb > 4096 || !bytes_per_clock_per_sm || !total_gbs)
+        return GEMM_ERR_INVALID_ARG;
+    DeviceState *ds = device_state();
+    if (!ds) return fail_cuda(cudaErrorInvalidDevice);
+    if (ds->init_error != cudaSuccess) return fail_cuda(ds->init_error);
+    if (2 * clusters > device_sm_count()) return GEMM_ERR_INVALID_ARG;
+    const cudaError_t e = run_tma_read_probe(clusters, multicast != 0, stages, kblocks, region_mb,
+                                             bytes_per_clock_per_sm, total_gbs, static_cast<cudaStream_t>(stream));
+    t_last_plan = multicast ? "tma_read_probe_multicast" : "tma_read_probe";
+    t_last_launches = 2;
+    if (e == cudaErrorLaunchTimeout) return GEMM_ERR_TIMEOUT;
+    if (e != cudaSuccess) return fail_cuda(e);
+    return GEMM_OK;
+}
+
 const char *gemm_last_plan(void) { return t_last_plan; }
 
 int gemm_last_launch_count(void) { return t_last_launches; }

@@ -149,5 +149,11 @@ cudaError_t run_scale_c_batched(int batch, int M, int N, float beta, void *C, lo
 cudaError_t run_tc_rate_probe(int iters, double *flop_per_clock_per_sm, cudaStream_t stream);
 // FP32 FMAs per clock per SM, packed (__ffma2_rn) or scalar, measured.
 cudaError_t run_fma_rate_probe(bool packed, int iters, double *fma_per_clock_per_sm, cudaStream_t stream);
+// TMA read rate per SM (bytes per SM clock, median over the CTAs) and in
+// total (GB/s, CUDA events) for `clusters` clusters of 2 CTAs streaming
+// `kblocks` 32 KB stages from a `region_mb` MB region, with or without
+// cluster multicast; synchronous on `stream`.
+cudaError_t run_tma_read_probe(int clusters, bool multicast, int stages, int kblocks, int region_mb,
+                               double *bytes_per_clock_per_sm, double *total_gbs, cudaStream_t stream);
 
 }  // namespace gemm11

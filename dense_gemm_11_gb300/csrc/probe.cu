@@ -12,8 +12,15 @@
 // the completion of the last (tcgen05.commit on an mbarrier, a bounded wait).
 // Nothing is loaded from global memory, so the figure is the tensor pipe's
 // issue-limited throughput.
+//
+// The third probe measures the bytes a CTA receives per SM clock through the
+// TMA unit (tma_read_probe_kernel), with and without cluster multicast: the
+// operand feed that bounds the memory-bound tensor-core plans.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -149,7 +156,169 @@ cudaError_t median_rate(const long long *d_cycles, int sms, double work, cudaStr
     return e;
 }
 
+// TMA read rate: clusters of 2 CTAs, one per SM; each CTA needs the same
+// 32 KB per stage and streams `kblocks` stages through a `stages`-deep ring
+// whose consumer releases each stage as soon as it lands.  The data is a
+// K-major operand as the tensor-core plans read it: a row-major FP16 matrix
+// with K = 4096 (8 KB rows), 128-byte swizzle; a stage is the k block
+// (64 k, 128 bytes of each row) of a 256-row panel, as two boxes of 128 rows
+// x 64 k; successive stages walk k, and after 64 k blocks the next panel.
+// Each cluster reads its own run of panels (disjoint while the region holds
+// them all: a large region streams from HBM); the panels wrap around a
+// region of `panels` panels, so a small region stays in L2.  multicast = 0: each CTA loads both
+// boxes itself; 1: CTA r loads box r with .multicast::cluster into both CTAs
+// (every stage then waits for both CTAs to have released it).  The consumer
+// thread times its loop with the SM cycle counter; every wait is bounded (a
+// timeout leaves -1 for that CTA).
+constexpr int kTmaProbeStageBytes = 32768;
+constexpr int kTmaProbeK = 4096;                 // elements per row
+constexpr int kTmaProbeRowBytes = kTmaProbeK * 2;
+constexpr int kTmaProbeKBlocks = kTmaProbeK / 64;  // k blocks per panel
+
+struct TmaProbeArgs {
+    int kblocks, stages, multicast, panels;
+    long long *cycles;
+};
+
+__device__ __forceinline__ void tma_load_2d_multicast(const CUtensorMap *map, uint64_t *bar, void *smem_dst, int x,
+                                                      int y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+        "{%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(64, 1) tma_read_probe_kernel(const __grid_constant__ CUtensorMap tm, TmaProbeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + 8;
+    uint8_t *ring = smem + 1024;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = static_cast<int>(blockIdx.x >> 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], a.multicast ? 2 : 1);
+        }
+        fence_mbarrier_init();
+    }
+    cluster_sync();
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.kblocks && ok; ++i) {
+            const int s = i % a.stages;
+            if (i >= a.stages) ok = mbar_wait(&empty[s], ((i / a.stages) - 1) & 1);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&full[s], kTmaProbeStageBytes);
+            uint8_t *dst = ring + static_cast<size_t>(s) * kTmaProbeStageBytes;
+            const int x = (i % kTmaProbeKBlocks) * 64;
+            const int ppc = (a.kblocks + kTmaProbeKBlocks - 1) / kTmaProbeKBlocks;  // panels per cluster
+            const int y0 = static_cast<int>((static_cast<long long>(cid) * ppc + i / kTmaProbeKBlocks) % a.panels) * 256;
+            if (a.multicast) {
+                tma_load_2d_multicast(&tm, &full[s], dst + rank * 16384, x, y0 + static_cast<int>(rank) * 128, 0x3);
+            } else {
+                tma_load_2d(&tm, &full[s], dst, x, y0);
+                tma_load_2d(&tm, &full[s], dst + 16384, x, y0 + 128);
+            }
+        }
+    } else if (threadIdx.x == 32) {
+        const long long t0 = clock64();
+        for (int i = 0; i < a.kblocks && ok; ++i) {
+            const int s = i % a.stages;
+            ok = mbar_wait(&full[s], (i / a.stages) & 1);
+            if (!ok) break;
+            mbar_arrive(&empty[s]);
+            if (a.multicast) mbar_arrive_cluster(mapa_shared(smem_u32(&empty[s]), rank ^ 1u));
+        }
+        a.cycles[blockIdx.x] = ok ? clock64() - t0 : -1;
+    }
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while its peer may still write or arrive into it
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 probe_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
 }  // namespace
+
+cudaError_t run_tma_read_probe(int clusters, bool multicast, int stages, int kblocks, int region_mb,
+                               double *bytes_per_clock_per_sm, double *total_gbs, cudaStream_t stream) {
+    auto enc = probe_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const int panels = region_mb / 2;  // 256 rows of 8 KB = 2 MB each
+    const size_t region = static_cast<size_t>(panels) * 256 * kTmaProbeRowBytes;
+    const int rows_region = panels * 256;  // every box [x, x + 64) x [y, y + 128) lies inside
+    uint8_t *buf = nullptr;
+    long long *d_cycles = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e = cudaMalloc(&buf, region);
+    if (e == cudaSuccess) e = cudaMalloc(&d_cycles, sizeof(long long) * 2 * clusters);
+    if (e == cudaSuccess) e = cudaMemsetAsync(buf, 0, region, stream);
+    if (e == cudaSuccess) e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    CUtensorMap tm;
+    if (e == cudaSuccess) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(kTmaProbeK), static_cast<cuuint64_t>(rows_region)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(kTmaProbeRowBytes)};
+        cuuint32_t box[2] = {64, 128}, estr[2] = {1, 1};
+        if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, buf, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            e = cudaErrorInvalidValue;
+    }
+    // the opt-in is made once per device, for the deepest ring (6 stages)
+    const int smem = std::max(2048 + stages * kTmaProbeStageBytes, kProbeSmem);
+    static unsigned long long smem_set = 0;
+    if (e == cudaSuccess) e = ensure_dynamic_smem(tma_read_probe_kernel, 2048 + 6 * kTmaProbeStageBytes, smem_set);
+    if (e == cudaSuccess) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * clusters, 1, 1);
+        cfg.blockDim = dim3(64, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        TmaProbeArgs args{kblocks, stages, multicast ? 1 : 0, panels, d_cycles};
+        // one warm-up launch (a small region is then resident in L2), one timed
+        e = cudaLaunchKernelEx(&cfg, tma_read_probe_kernel, tm, args);
+        if (e == cudaSuccess) e = cudaEventRecord(e0, stream);
+        if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, tma_read_probe_kernel, tm, args);
+        if (e == cudaSuccess) e = cudaEventRecord(e1, stream);
+        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    }
+    if (e == cudaSuccess) {
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, e0, e1);
+        if (e == cudaSuccess) {
+            const double per_cta = static_cast<double>(kblocks) * kTmaProbeStageBytes;
+            *total_gbs = 2.0 * clusters * per_cta / (static_cast<double>(ms) * 1e6);
+            e = median_rate(d_cycles, 2 * clusters, per_cta, stream, bytes_per_clock_per_sm);
+        }
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(d_cycles);
+    cudaFree(buf);
+    return e;
+}
 
 cudaError_t run_fma_rate_probe(bool packed, int iters, double *fma_per_clock_per_sm, cudaStream_t stream) {
     const int sms = device_sm_count();

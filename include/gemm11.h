@@ -393,6 +393,31 @@ GEMM11_API int gemm_tc_rate_probe(int iters, double *flop_per_clock_per_sm, void
 GEMM11_API int gemm_fma_rate_probe(int packed, int iters, double *fma_per_clock_per_sm, void *stream);
 
 /*
+ * gemm_tma_read_probe -- diagnostic: the operand feed of the tensor-core
+ * plans, measured.  `clusters` clusters of 2 CTAs (one CTA per SM) each need
+ * the same 32 KB per stage and stream `kblocks` stages through a
+ * `stages`-deep ring of shared memory (TMA loads, mbarrier full/empty
+ * handshake, every wait bounded; the consumer releases each stage as soon as
+ * it lands).  The data is read as a K-major GEMM operand: a row-major FP16
+ * matrix with 4096-element rows, 128-byte swizzle, each stage the 64-wide k
+ * block of a 256-row panel as two boxes of 128 rows x 64 k; the stages walk
+ * k, then the next panel, each cluster its own run of panels, wrapping
+ * around a region of region_mb MB (region_mb / 2 panels) of a buffer the
+ * probe allocates (24 MB stays in L2; 1024 MB streams from HBM).  multicast = 0: each CTA loads
+ * both boxes itself; multicast = 1: CTA r loads box r once with cluster
+ * multicast into both CTAs.  *bytes_per_clock_per_sm receives the median
+ * over the CTAs of bytes received per SM clock (cycle counter around the
+ * consumer's loop); *total_gbs the bytes all CTAs received over the launch's
+ * CUDA-event time.  One warm-up launch precedes the timed one.  Synchronous
+ * on `stream`.  clusters in 1..(SMs / 2), multicast in {0, 1}, stages in
+ * 1..6, kblocks in 1..65536, region_mb in 2..4096.  Returns GEMM_OK,
+ * GEMM_ERR_INVALID_ARG, GEMM_ERR_TIMEOUT (no CTA finished within the bounded
+ * waits) or GEMM_ERR_CUDA.
+ */
+GEMM11_API int gemm_tma_read_probe(int clusters, int multicast, int stages, int kblocks, int region_mb,
+                                   double *bytes_per_clock_per_sm, double *total_gbs, void *stream);
+
+/*
  * Introspection for tests and benchmarks: the name of the kernel plan the
  * calling thread's last successful call used (static storage), and how many
  * kernels that call launched.

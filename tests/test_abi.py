@@ -96,6 +96,19 @@ def test_rate_probes_reject_bad_arguments_without_cuda(L):
     assert g.fma_rate_probe_raw(1, 0, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
     assert g.fma_rate_probe_raw(0, (1 << 20) + 1, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
     assert g.fma_rate_probe_raw(1, 1024, 0) == g.GEMM_ERR_INVALID_ARG
+    a, b = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    pa, pb = ctypes.addressof(a), ctypes.addressof(b)
+    f = g.tma_read_probe_raw
+    assert f(0, 0, 4, 64, 24, pa, pb) == g.GEMM_ERR_INVALID_ARG        # clusters
+    assert f(1, 2, 4, 64, 24, pa, pb) == g.GEMM_ERR_INVALID_ARG        # multicast
+    assert f(1, 0, 0, 64, 24, pa, pb) == g.GEMM_ERR_INVALID_ARG        # stages
+    assert f(1, 0, 7, 64, 24, pa, pb) == g.GEMM_ERR_INVALID_ARG
+    assert f(1, 0, 4, 0, 24, pa, pb) == g.GEMM_ERR_INVALID_ARG         # kblocks
+    assert f(1, 0, 4, 65537, 24, pa, pb) == g.GEMM_ERR_INVALID_ARG
+    assert f(1, 0, 4, 64, 1, pa, pb) == g.GEMM_ERR_INVALID_ARG         # region
+    assert f(1, 0, 4, 64, 4097, pa, pb) == g.GEMM_ERR_INVALID_ARG
+    assert f(1, 0, 4, 64, 24, 0, pb) == g.GEMM_ERR_INVALID_ARG         # outputs
+    assert f(1, 0, 4, 64, 24, pa, 0) == g.GEMM_ERR_INVALID_ARG
 
 
 def test_debug_build_exports_every_symbol_and_says_so(L):

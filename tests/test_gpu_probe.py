@@ -1,6 +1,7 @@
 """The rate probes: gemm_tc_rate_probe, the dense kind::f16 rate per SM that
-the FP16 path's nominal peak is built from, and gemm_fma_rate_probe, the FP32
-FMA throughput per SM of the packed (FFMA2) and scalar instruction forms."""
+the FP16 path's nominal peak is built from, gemm_fma_rate_probe, the FP32
+FMA throughput per SM of the packed (FFMA2) and scalar instruction forms, and
+gemm_tma_read_probe, the bytes per SM clock a CTA receives through TMA."""
 import pytest
 
 pytestmark = pytest.mark.gpu
@@ -57,3 +58,25 @@ def test_fma_rate_probe_bad_arguments():
     assert g.fma_rate_probe_raw(2, 1024, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
     assert g.fma_rate_probe_raw(1, 0, ctypes.addressof(out)) == g.GEMM_ERR_INVALID_ARG
     assert g.fma_rate_probe_raw(1, 1024, 0) == g.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("multicast", [False, True])
+@pytest.mark.parametrize("region_mb", [24, 1024])
+def test_tma_read_probe_is_plausible(multicast, region_mb):
+    # a CTA cannot receive more than a few hundred bytes per SM clock; the
+    # figure is stable from one launch to the next
+    r = g.tma_read_probe(8, multicast=multicast, stages=4, kblocks=256, region_mb=region_mb)
+    assert 4.0 <= r["bytes_per_clock_per_sm"] <= 512.0, r
+    assert r["total_gbs"] > 0.0, r
+    again = g.tma_read_probe(8, multicast=multicast, stages=4, kblocks=256, region_mb=region_mb)
+    assert abs(again["bytes_per_clock_per_sm"] - r["bytes_per_clock_per_sm"]) <= 0.15 * r["bytes_per_clock_per_sm"], \
+        (r, again)
+
+
+def test_tma_read_probe_every_sm():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    r = g.tma_read_probe(sms // 2, stages=6, kblocks=512, region_mb=24)
+    assert r["bytes_per_clock_per_sm"] > 0.0 and r["total_gbs"] > 0.0, r
+    with pytest.raises(g.GemmError) as e:
+        g.tma_read_probe(sms // 2 + 1)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
