@@ -688,6 +688,22 @@ def run_sweep(reps: int, only=None):
         torch.cuda.empty_cache()
 
 
+def run_tma_probe_table(kblocks):
+    """The TMA read probe (gemm_tma_read_probe) over own-copy and multicast loads,
+    an L2-resident (24 MB) and an HBM (2048 MB) region, 1 to 76 clusters of two
+    CTAs and 2 to 6 stages in flight: one JSON line per case."""
+    import torch
+    import dense_gemm_11_gb300 as g
+    torch.cuda.set_device(0)
+    for mc in (False, True):
+        for region in (24, 2048):
+            for cl in (1, 8, 38, 76):
+                for st in (2, 4, 6):
+                    r = g.tma_read_probe(cl, multicast=mc, stages=st, kblocks=kblocks, region_mb=region)
+                    print(json.dumps(dict(clusters=cl, multicast=int(mc), stages=st, region_mb=region, **r)),
+                          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -703,7 +719,12 @@ def main():
     ap.add_argument("--repeats", type=int, default=2)
     ap.add_argument("--sweep", action="store_true", help="time every named workload, one JSON line each")
     ap.add_argument("--workloads", default="", help="comma-separated workload names for --sweep (default: all)")
+    ap.add_argument("--tma-probe", action="store_true",
+                    help="run the TMA read probe over loads, regions, clusters and stages, one JSON line each")
     args = ap.parse_args()
+    if args.tma_probe:
+        run_tma_probe_table(1024)
+        return
     if args.sweep:
         run_sweep(max(3, args.steps // 10), [w for w in args.workloads.split(",") if w])
         return
