@@ -250,3 +250,27 @@ def test_f32_k_group_plan_small_integers_exact(M, N, K):
     assert "kg4" in plan, plan
     ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=2.0, with_scale=False)
     np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=plan)
+
+
+# M == 1 (a row vector times B): ragged N and K, a leading dimension past N,
+# beta != 0; every column against the oracle.
+@pytest.mark.parametrize("N,K,ldb", [(4000, 3001, None), (6000, 2048, 6004), (11008, 4096, None),
+                                     (12345, 1500, 12352), (2000, 4096, None), (20000, 1024, None)])
+def test_f32_m1_shapes(N, K, ldb):
+    d = inputs.make(1, N, K, kind="f32", dist="uniform", seed=60, beta=0.5, ldb=ldb)
+    got, p = run_f32(d, 0.7, 0.5, K=K, N=N)
+    ref, S = oracle.gemm(d["A"], d["B"], d["C"], alpha=0.7, beta=0.5, K=K, N=N)
+    assert_within(got[:, :N], ref, S, TOL_F32, f"1 x {N} x {K} [{p}]")
+
+
+@pytest.mark.parametrize("N,K", [(6000, 2048), (11008, 4099)])
+def test_f32_m1_exact_and_beta_zero(N, K):
+    d = inputs.make(1, N, K, kind="f32", dist="smallint", seed=61, beta=2.0)
+    got, p = run_f32(d, 1.0, 2.0)
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=2.0, with_scale=False)
+    np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=p)
+    # beta == 0 never reads C (NaN there stays out of the result)
+    d0 = inputs.make(1, N, K, kind="f32", dist="normal", seed=62, beta=0.0)
+    assert np.isnan(d0["C"]).all()
+    got0, p0 = run_f32(d0, 0.5, 0.0)
+    assert np.isfinite(got0).all(), p0
