@@ -117,7 +117,9 @@ struct HgemmCfg {
     static constexpr int kThreads = 64 + 32 * EPI;
     static constexpr int kNBuf = EPI == 4 ? 2 : 1;  // 4 KB staging buffers per epilogue warp
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows of 128 B
-    static constexpr int kBBytes = BN * kBK * 2;   // BN rows (or k-rows) of 128 B
+    // B: BN rows of 128 B (K-major), or whole 64-column boxes of 64 k-rows
+    // (MN-major; with BN = 96 the second box reaches 32 columns past the tile)
+    static constexpr int kBBytes = SWAP ? BN * kBK * 2 : (BN + 63) / 64 * 64 * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr bool kPartInRing = CSPLIT && !SWAP;
     static constexpr int kCStageBytes =
@@ -127,7 +129,6 @@ struct HgemmCfg {
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kCStageBytes + kBarBytes;
     static constexpr int kTmemCols = tmem_cols_for(BN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (and 32-column TMEM reads)");
-    static_assert(SWAP || BN % 64 == 0, "B tile is loaded in 64-column boxes");
     static_assert(STAGES <= 8, "stage bookkeeping uses 8-bit masks");
     static_assert(!kPartInRing || STAGES * kStageBytes >= kBM * BN * 4, "the partial tile fits in the operand ring");
     static_assert(!kPartInRing || BN % 64 == 0, "partial rows are 32-column groups of 8 swizzled 16-byte chunks");
@@ -587,6 +588,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
+        // bytes per stage: a K-major B tile is BN rows, an MN-major one whole boxes
+        const uint32_t stage_tx = (!SWAP && p.b_kmajor) ? Cfg::kABytes + BN * kBK * 2 : Cfg::kStageBytes;
         int stage = 0;
         uint32_t phase = 0;
         for (int idx = 0; !*abort_flag && !p.stall_producer; ++idx) {
@@ -597,7 +600,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                     flag_timeout(abort_flag, p.err);
                     break;
                 }
-                mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+                mbar_arrive_expect_tx(&full[stage], stage_tx);
                 if (idx == 0 && kb == c.kb0) pdl_wait();  // the operands may come from the previous kernel
                 const int k0 = kb * kBK;
                 uint8_t *a_dst = sA + stage * Cfg::kABytes;
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                         tma_load_3d(&tm_b, &full[stage], b_dst, k0, c.n0, zb);  // BN rows of 64 k
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
+                        for (int j = 0; j < (BN + 63) / 64; ++j)
                             tma_load_3d(&tm_b, &full[stage], b_dst + j * 8192, c.n0 + 64 * j, k0, zb);
                     }
                 } else {
@@ -1656,7 +1659,8 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
     // Tile table.  M <= 64: transposed product with MMA N = M rounded up to
     // 32 or 64 (K split over a cluster when its tiles fill at most half the
     // SMs).  M > 128 with enough pair tiles: CTA pairs.  Otherwise 128-row
-    // tiles, 128 x 256 (128 x 128 when that puts more SMs to work), K split
+    // tiles, 128 x 256 (128 x 128, or 128 x 96 with at most one tile per SM,
+    // when that puts more SMs to work), K split
     // over a cluster when a time model says it pays (pick_cluster_split).
     // Every CTA is persistent and takes whole tiles round-robin (tiles of all
     // matrices of a batch in one sequence).  A tuned plan for this exact
@@ -1679,6 +1683,14 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
         // streaming B (measured at 128 x 11008 x 4096: 36.5 us vs 48.8 us).
         const long long t256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256) * g.batch;
         bn = (N > 128 && t256 >= sms / 2) ? 256 : 128;
+        // Fewer 128-wide tiles than SMs and K of 16 k blocks or more: 96-wide
+        // tiles, still at most one per SM, put more SMs to work streaming B
+        // (128 x 11008 x 4096: 115 tiles instead of 86, 24.2 -> 23.5 us;
+        // 120 x 9000 x 520, 9 k blocks: 9.8 -> 10.1 us, so not there).
+        const long long rows_t = static_cast<long long>((M + kBM - 1) / kBM) * g.batch;
+        if (!tuned && bn == 128 && a.kb_total >= 16 && rows_t * ((N + 127) / 128) < sms &&
+            rows_t * ((N + 95) / 96) <= sms)
+            bn = 96;
         if (tuned && tp.variant == 2 && tp.bn) bn = tp.bn;
     }
     const int bn_tile = swap ? kBM : bn;
@@ -1850,6 +1862,10 @@ cudaError_t run_gemm_f16(const TcGemm &g, cudaStream_t stream, CallInfo *info) {
             e = epi8 ? launch_hgemm<256, 4, false, false, 8>(ta, tb, tc, a, grid, stream)
                      : launch_hgemm<256, 4, false>(ta, tb, tc, a, grid, stream);
             info->plan = splits > 1 ? "tc_128x256_splitk" : (epi8 ? "tc_128x256_epi8" : "tc_128x256");
+        } else if (bn == 96) {
+            e = epi8 ? launch_hgemm<96, 6, false, false, 8>(ta, tb, tc, a, grid, stream)
+                     : launch_hgemm<96, 6, false>(ta, tb, tc, a, grid, stream);
+            info->plan = splits > 1 ? "tc_128x96_splitk" : (epi8 ? "tc_128x96_epi8" : "tc_128x96");
         } else {
             e = epi8 ? launch_hgemm<128, 6, false, false, 8>(ta, tb, tc, a, grid, stream)
                      : launch_hgemm<128, 6, false>(ta, tb, tc, a, grid, stream);

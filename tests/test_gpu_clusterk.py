@@ -111,3 +111,40 @@ def test_deterministic_across_calls():
     torch.cuda.synchronize()
     assert "clusterk" in g.last_plan()
     assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("M,N,K,b_trans,out", [(128, 11008, 1024, False, "f32"), (100, 3000, 1000, False, "f32"),
+                                               (100, 3000, 1000, True, "f32"), (96, 8192, 2048, True, "bf16"),
+                                               (120, 9000, 1040, False, "f16")])
+def test_96_wide_whole_tiles(M, N, K, b_trans, out):
+    # fewer 128-wide tiles than SMs, 16 k blocks or more and no cluster split:
+    # 96-wide tiles, one per SM.  Stored K x N, B's second 64-column box reaches 32 columns past
+    # the tile (past N on the last one); stored N x K, the box is 96 rows.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    in_kind = "bf16" if out == "bf16" else "f16"
+    # small integers: exact sums, one rounding to a 16-bit C
+    d = inputs.make_batched(1, M, N, K, kind=in_kind, dist="smallint", seed=M + N, beta=1.0, b_trans=b_trans)
+    got, C0, plan = run(d, 1.0, 1.0, in_kind=in_kind, out=out, b_trans=b_trans)
+    if sms == 152:
+        assert plan == "tc_128x96_epi8", plan
+    B = d["B"][0].T if b_trans else d["B"][0]
+    ref, _ = oracle.gemm(d["A"][0], B, C0[0], alpha=1.0, beta=1.0, with_scale=False)
+    if out != "f32":
+        ref = oracle.round_to(out, ref)
+    np.testing.assert_array_equal(got[0], ref, err_msg=plan)
+    # normal data with bias and an activation
+    d = inputs.make_batched(1, M, N, K, kind=in_kind, seed=M + N + 1, beta=-0.5, bias=True, b_trans=b_trans)
+    got, C0, plan = run(d, 0.75, -0.5, act=1, in_kind=in_kind, out=out, b_trans=b_trans)
+    B = d["B"][0].T if b_trans else d["B"][0]
+    ref, S = oracle.gemm(d["A"][0], B, C0[0], alpha=0.75, beta=-0.5, bias=d["bias"], act=1)
+    assert_within(got[0], ref, S, TOL_F16, f"{M}x{N}x{K} {out} trans={b_trans} [{plan}]", out=out, bias=d["bias"])
+
+
+def test_short_k_keeps_128_wide_tiles():
+    # 9 k blocks: 128-wide whole tiles (96-wide measured slower there)
+    d = inputs.make_batched(1, 120, 9000, 520, kind="f16", dist="smallint", seed=66, beta=0.0)
+    got, C0, plan = run(d, 1.0, 0.0)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert plan == "tc_128x128_epi8", plan
+    ref, _ = oracle.gemm(d["A"][0], d["B"][0], None, with_scale=False)
+    np.testing.assert_array_equal(got[0], ref, err_msg=plan)
