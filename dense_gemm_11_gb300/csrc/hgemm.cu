@@ -418,8 +418,24 @@ __device__ __forceinline__ void swap_csplit_reduce(const HgemmArgs &p, const Uni
         }
 #pragma unroll
         for (int i = 0; i + 4 < NCOL; ++i) acc[i] = acc[i + 4];
+        // epi_value's arithmetic, with the activation's branch taken once for
+        // the four values so that their chains interleave
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = epi_value(v[i], p, cold[i], b_n);
+        for (int i = 0; i < 4; ++i) {
+            v[i] = p.alpha * v[i];
+            if (p.beta != 0.f) v[i] = fmaf(p.beta, cold[i], v[i]);
+            v[i] += b_n;
+        }
+        if (p.act == 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = gelu_erf(v[i]);
+        } else if (p.act == 3) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = gelu_tanh(v[i]);
+        } else if (p.act == 2) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = fmaxf(v[i], 0.f);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if (g + NSP * (j4 + i) < p.M) store_c(p, ci[i], v[i]);
