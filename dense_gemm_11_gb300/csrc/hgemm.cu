@@ -355,12 +355,52 @@ __device__ __forceinline__ void store_row_unit64(const uint4 (&w)[8], const CUte
     }
 }
 
-__device__ __forceinline__ float epi_value(float acc, const HgemmArgs &p, float cold, float b) {
-    float v = p.alpha * acc;
-    if (p.beta != 0.f) v = fmaf(p.beta, cold, v);
-    v += b;
-    v = apply_activation(p.act, v);
-    return v;
+// act(alpha * v + beta * cold + b) for four values, the activation's branch
+// taken once for all four so that their chains interleave (a branch per value
+// makes the four run one after another).
+__device__ __forceinline__ void epi_values4(float (&v)[4], const HgemmArgs &p, const float (&cold)[4],
+                                            const float (&b)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = p.alpha * v[i];
+        if (p.beta != 0.f) v[i] = fmaf(p.beta, cold[i], v[i]);
+        v[i] += b[i];
+    }
+    if (p.act == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = gelu_erf(v[i]);
+    } else if (p.act == 3) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = gelu_tanh(v[i]);
+    } else if (p.act == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = fmaxf(v[i], 0.f);
+    }
+}
+
+// Transposed tile, this thread owning column gn of C: rows ch * 32 + j of C
+// (j < 32, below M) get act(alpha * v[j] + beta * C + bias), four rows at a
+// time through epi_values4.
+__device__ __forceinline__ void store_col_rows32(const float (&v)[32], const HgemmArgs &p, int ch, int gn,
+                                                 size_t cbase, float b_n) {
+    const float b4[4] = {b_n, b_n, b_n, b_n};
+#pragma unroll
+    for (int j4 = 0; j4 < 32; j4 += 4) {
+        if (ch * 32 + j4 >= p.M) break;  // rows m grow with j
+        float w[4], cold[4];
+        size_t ci[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gm = ch * 32 + j4 + i;
+            ci[i] = cbase + static_cast<size_t>(gm) * p.ldc + gn;
+            cold[i] = (p.beta != 0.f && gm < p.M) ? load_out(p.C, ci[i], p.c_type) : 0.f;
+            w[i] = v[j4 + i];
+        }
+        epi_values4(w, p, cold, b4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (ch * 32 + j4 + i < p.M) store_c(p, ci[i], w[i]);
+    }
 }
 
 // Cluster split-K of the transposed small-M product: CTA `c.split` sums tile
@@ -418,24 +458,8 @@ __device__ __forceinline__ void swap_csplit_reduce(const HgemmArgs &p, const Uni
         }
 #pragma unroll
         for (int i = 0; i + 4 < NCOL; ++i) acc[i] = acc[i + 4];
-        // epi_value's arithmetic, with the activation's branch taken once for
-        // the four values so that their chains interleave
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[i] = p.alpha * v[i];
-            if (p.beta != 0.f) v[i] = fmaf(p.beta, cold[i], v[i]);
-            v[i] += b_n;
-        }
-        if (p.act == 1) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = gelu_erf(v[i]);
-        } else if (p.act == 3) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = gelu_tanh(v[i]);
-        } else if (p.act == 2) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = fmaxf(v[i], 0.f);
-        }
+        const float b4[4] = {b_n, b_n, b_n, b_n};
+        epi_values4(v, p, cold, b4);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if (g + NSP * (j4 + i) < p.M) store_c(p, ci[i], v[i]);
@@ -519,10 +543,8 @@ __device__ __forceinline__ void csplit_reduce_rows(const HgemmArgs &p, const Uni
         }
         float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (p.bias) b4 = *reinterpret_cast<const float4 *>(sbias + 4 * g);
-        v[0] = epi_value(v[0], p, cold[0], b4.x);
-        v[1] = epi_value(v[1], p, cold[1], b4.y);
-        v[2] = epi_value(v[2], p, cold[2], b4.z);
-        v[3] = epi_value(v[3], p, cold[3], b4.w);
+        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+        epi_values4(v, p, cold, bv);
         if (!debug_in_bounds(p.c_extent == 0 || ci + 4 <= p.c_extent, p.err)) continue;
         if (p.c_type == kOutF32) {
             *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + ci) = make_float4(v[0], v[1], v[2], v[3]);
@@ -881,17 +903,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 } else {
                     // transposed: this thread owns column n of C, registers walk rows m
                     const int gn = c.n0 + row_in_tile;
-                    if (gn < p.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int gm = ch * 32 + j;
-                            if (gm < p.M) {
-                                const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
-                                const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                                store_c(p, ci, epi_value(v[j], p, cold, b_n));
-                            }
-                        }
-                    }
+                    if (gn < p.N) store_col_rows32(v, p, ch, gn, cbase, b_n);
                 }
             }
             // Accumulator buffer free for the MMA warp.
@@ -960,17 +972,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                             store_row_chunk<Cfg::kNBuf>(v, p, &tm_c, stage_base, n_staged, lane, c.m0 + q * 32, col0, c.batch);
                         } else {
                             const int gn = c.n0 + row_in_tile;
-                            if (gn < p.N) {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) {
-                                    const int gm = ch * 32 + j;
-                                    if (gm < p.M) {
-                                        const size_t ci = cbase + static_cast<size_t>(gm) * p.ldc + gn;
-                                        const float cold = p.beta != 0.f ? load_out(p.C, ci, p.c_type) : 0.f;
-                                        store_c(p, ci, epi_value(v[j], p, cold, b_n));
-                                    }
-                                }
-                            }
+                            if (gn < p.N) store_col_rows32(v, p, ch, gn, cbase, b_n);
                         }
                     }
                     if (lane == 0) p.counters[cnt_idx] = 0u;
