@@ -811,6 +811,89 @@ __global__ void __launch_bounds__(256) sgemv_cols_kernel(int N, int K, float alp
     }
 }
 
+// M == 1 with K split over the S CTAs of a thread-block cluster (2 <= S <= 8):
+// CTA r of a cluster owns rows [K r / S, K (r + 1) / S) of the cluster's 128
+// columns (4 per lane; its WARPS warps take interleaved rows and are added in
+// warp order) and leaves its sum in shared memory; after a cluster barrier,
+// CTA 0 adds the S sums in rank order through distributed shared memory and
+// writes y.  No global scratch, atomics or memory fences.  (The split-K
+// kernel above spends ~1.8 us on its fence and arrival count and ~1.3 us on
+// the last CTA's sum of 19 partials at 1 x 4096 x 4096, per-CTA timer
+// stamps.)  Launched with programmatic dependent launch: it waits for the
+// previous kernel of the stream before its first global access.
+template <int S, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) sgemv_cols_cluster_kernel(int N, int K, float alpha,
+                                                                        const float *__restrict__ x,
+                                                                        const float *__restrict__ B, int ldb,
+                                                                        float beta, float *y, int vec) {
+    __shared__ float4 red[WARPS][32];
+    __shared__ float4 part[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int col = (blockIdx.x / S) * 128 + lane * 4;
+    const int k0 = static_cast<int>(static_cast<long long>(K) * rank / S);
+    const int k1 = static_cast<int>(static_cast<long long>(K) * (rank + 1) / S);
+    pdl_wait();
+    pdl_launch_dependents();
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (vec && col + 3 < N) {
+#pragma unroll 16
+        for (int k = k0 + warp; k < k1; k += WARPS) {
+            const float xv = __ldg(x + k);
+            const float4 bv = __ldcs(reinterpret_cast<const float4 *>(B + static_cast<size_t>(k) * ldb + col));
+            s.x = fmaf(xv, bv.x, s.x);
+            s.y = fmaf(xv, bv.y, s.y);
+            s.z = fmaf(xv, bv.z, s.z);
+            s.w = fmaf(xv, bv.w, s.w);
+        }
+    } else if (col < N) {
+        for (int k = k0 + warp; k < k1; k += WARPS) {
+            const float xv = __ldg(x + k);
+            const float *br = B + static_cast<size_t>(k) * ldb + col;
+            s.x = fmaf(xv, br[0], s.x);
+            if (col + 1 < N) s.y = fmaf(xv, br[1], s.y);
+            if (col + 2 < N) s.z = fmaf(xv, br[2], s.z);
+            if (col + 3 < N) s.w = fmaf(xv, br[3], s.w);
+        }
+    }
+    red[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0) {
+        float4 t = red[0][lane];
+#pragma unroll
+        for (int w = 1; w < WARPS; ++w) {
+            const float4 v = red[w][lane];
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        part[lane] = t;
+    }
+    cluster_sync();  // every CTA's sum written and visible to the cluster
+    if (rank == 0 && warp == 0) {
+        float4 t = part[lane];
+#pragma unroll
+        for (int q = 1; q < S; ++q) {
+            const float4 v = ld_shared_cluster_v4(mapa_shared(smem_u32(&part[lane]), static_cast<uint32_t>(q)));
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (col + e < N) {
+                float v = alpha * tv[e];
+                if (beta != 0.f) v = fmaf(beta, y[col + e], v);
+                y[col + e] = v;
+            }
+        }
+    }
+    cluster_sync();  // the peers' sums stay in place until CTA 0 has read them
+}
+
 // alpha == 0 or K == 0: C = act(beta * C + bias) (beta == 0 writes without reading).
 __global__ void scale_c_kernel(int M, int N, float beta, float *C, int ldc, const float *bias, int act) {
     const long long total = static_cast<long long>(M) * N;
@@ -867,6 +950,51 @@ cudaError_t launch_tiled(const SgemmArgs &a, cudaStream_t stream) {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+template <int S, int WARPS>
+cudaError_t launch_gemv_cluster(int col_blocks, int N, int K, float alpha, const float *x, const float *B, int ldb,
+                                float beta, float *y, int vec, cudaStream_t stream) {
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(col_blocks * S, 1, 1);
+    cfg.blockDim = dim3(WARPS * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sgemv_cols_cluster_kernel<S, WARPS>, N, K, alpha, x, B, ldb, beta, y, vec);
+    if (e != cudaSuccess) return e;
+    return cudaPeekAtLastError();
+}
+
+// 16 warps per CTA when the clusters give fewer than ~3 CTAs per SM, so that
+// as many loads stay in flight as with more, smaller CTAs.
+template <int S>
+cudaError_t launch_gemv_cluster_w(int col_blocks, int N, int K, float alpha, const float *x, const float *B, int ldb,
+                                  float beta, float *y, int vec, cudaStream_t stream) {
+    if (col_blocks * S < 3 * device_sm_count())
+        return launch_gemv_cluster<S, 16>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+    return launch_gemv_cluster<S, 8>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+}
+
+cudaError_t launch_gemv_cluster_any(int s, int col_blocks, int N, int K, float alpha, const float *x, const float *B,
+                                    int ldb, float beta, float *y, int vec, cudaStream_t stream) {
+    switch (s) {
+        case 2: return launch_gemv_cluster_w<2>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+        case 3: return launch_gemv_cluster_w<3>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+        case 4: return launch_gemv_cluster_w<4>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+        case 5: return launch_gemv_cluster_w<5>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+        case 6: return launch_gemv_cluster_w<6>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+        case 7: return launch_gemv_cluster_w<7>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+        default: return launch_gemv_cluster_w<8>(col_blocks, N, K, alpha, x, B, ldb, beta, y, vec, stream);
+    }
+}
+
 }  // namespace
 
 cudaError_t run_scale_c(int M, int N, float beta, float *C, int ldc, const float *bias, int act,
@@ -919,6 +1047,15 @@ cudaError_t run_gemm_f32(int M, int N, int K, float alpha, const float *A, int l
         // enough CTAs for every SM to stream B: about 4 per SM, each K chunk >= 64 rows
         int splits = std::max(1, std::min((4 * sms + col_blocks - 1) / col_blocks, K / 64));
         splits = std::min(splits, 64);
+        // Up to 8 splits, while that still gives every SM a CTA: the splits of a
+        // column block are the CTAs of one cluster, summed through distributed
+        // shared memory.
+        if (splits > 1 && col_blocks * 8 >= sms) {
+            const int cs = std::min(splits, 8);
+            info->plan = "sgemv_cols_clusterk";
+            info->launches = 1;
+            return launch_gemv_cluster_any(cs, col_blocks, N, K, alpha, A, B, ldb, beta, C, vec, stream);
+        }
         Scratch sc;
         if (splits > 1) {
             cudaError_t e = acquire_scratch(stream, static_cast<size_t>(col_blocks) * splits * 128, col_blocks, &sc);

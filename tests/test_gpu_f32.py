@@ -274,3 +274,18 @@ def test_f32_m1_exact_and_beta_zero(N, K):
     assert np.isnan(d0["C"]).all()
     got0, p0 = run_f32(d0, 0.5, 0.0)
     assert np.isfinite(got0).all(), p0
+
+
+@pytest.mark.parametrize("N,K,plan", [(4096, 4096, "sgemv_cols_clusterk"), (11008, 4096, "sgemv_cols_clusterk"),
+                                      (3000, 4097, "sgemv_cols_clusterk"), (2000, 4096, "sgemv_cols_splitk"),
+                                      (4096, 100, "sgemv_cols")])
+def test_f32_m1_plans_exact(N, K, plan):
+    # K split over a cluster (up to 8 CTAs, sums through distributed shared
+    # memory) while every SM still gets a CTA; otherwise the global split-K
+    # kernel, or no split for short K
+    d = inputs.make(1, N, K, kind="f32", dist="smallint", seed=63, beta=-1.0)
+    got, p = run_f32(d, 1.0, -1.0)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert p == plan, p
+    ref, _ = oracle.gemm(d["A"], d["B"], d["C"], alpha=1.0, beta=-1.0, with_scale=False)
+    np.testing.assert_array_equal(got.astype(np.float64), ref, err_msg=p)
